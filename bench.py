@@ -1,0 +1,495 @@
+"""Benchmark of the FP8 paged KV-cache hot path on GB300.
+
+Workload (the long-context case): one sequence of 32768 tokens, Hq=32,
+Hkv=8, dh=128, block_size=16, 32 layers of independent seeded bf16 N(0,1)
+K/V with per-head E4M3 scales (amax/448).  One step = the whole hot path over
+all 32 layers: quantize-and-scatter all 32768 tokens of every layer into its
+FP8 paged cache (2 GiB of cache in total), then one decode-attention step per
+layer over that cache.  Every layer's cache is written before the first
+decode, so a layer's pages are evicted from L2 by the other layers' traffic
+(about 6 GiB per step, inputs far larger than the 129 MB L2).
+
+Prints one JSON line.  ``value`` is the step's algorithmic HBM bytes (write
++ decode) over the device-timed step; the decode-attention and KV-write
+figures of the metric are reported beside it, each from CUDA events around
+its own calls.  ``--impl reference`` times the CPU oracle on the host cores
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = ("FP8 paged decode-attn HBM GB/s (% of GB300 peak); KV-write GB/s; KV tok/s")
+CFG = 4
+LAYERS = workloads.NUM_LAYERS[CFG]
+HQ, HKV, DH = workloads.SHAPES[CFG]
+SEQ = 32768
+BS = 16
+E = 1  # FP8 element bytes
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+
+def write_bytes(n_tokens: int) -> int:
+    """Per token: read bf16 K and V, write FP8 K and V, read its int64 slot."""
+    return n_tokens * (2 * HKV * DH * 2 + 2 * HKV * DH * E + 8)
+
+
+def decode_bytes(n_tokens: int, n_heads: int = HQ) -> int:
+    """KV read of the attended tokens (all KV heads), Q read and O write (bf16),
+    block-table entries, seq_len, scales."""
+    kv_heads = max(1, n_heads * HKV // HQ)
+    return (n_tokens * 2 * kv_heads * DH * E + n_heads * DH * 2 * 2
+            + ((n_tokens + BS - 1) // BS) * 4 + 4 + 2 * HKV * 4)
+
+
+STEP_WRITE_BYTES = LAYERS * write_bytes(SEQ)
+STEP_DECODE_BYTES = LAYERS * decode_bytes(SEQ)
+STEP_BYTES = STEP_WRITE_BYTES + STEP_DECODE_BYTES
+
+WORKLOAD = {
+    "workload": "long context: 1 seq x 32768 tokens, 32 layers, Hq=32 Hkv=8 dh=128 bs=16, "
+                "FP8 E4M3 per-head scales; step = write all 32768 tokens of every layer, then "
+                "one decode step per layer",
+    "layers": LAYERS, "seqs": 1, "seq_len": SEQ, "num_q_heads": HQ, "num_kv_heads": HKV,
+    "head_dim": DH, "block_size": BS, "kv_cache_dtype": "fp8_e4m3", "scales": "per-head amax/448",
+    "l2": "inputs larger than L2 (about 6.3 GB moved per step)",
+}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_quantized_paged_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_hash") != kernel_source_hash():
+            return None
+        return d["kernels"][kernel]["bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- ranks
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Slowest rank's value (the job's time) via an all-reduce MAX."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank moves the same bytes per step; the job's time
+    per step is the slowest rank's."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------- inputs
+
+
+def make_inputs(n_layers: int):
+    st = workloads.structure(CFG)
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        layers = list(ex.map(lambda l: workloads.make_layer(CFG, l, st=st), range(n_layers)))
+    return st, layers
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import fp8_quantized_paged_gb300 as kvq
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    st, layers = make_inputs(LAYERS)
+    stream = torch.cuda.current_stream()
+
+    def up(a, pin=False):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(a)
+        return t.pin_memory() if pin else t.to(dev)
+
+    slots = up(st.slot_mapping)
+    bt = up(st.block_tables)
+    sl = up(st.seq_lens)
+    L = []
+    for lay in layers:
+        L.append(dict(k=up(lay.k), v=up(lay.v), q=up(lay.q), ks=up(lay.k_scale),
+                      vs=up(lay.v_scale),
+                      kc=kvq.new_cache(st.num_blocks, HKV, DH, kvq.KVQ_FMT_E4M3, dev),
+                      vc=kvq.new_cache(st.num_blocks, HKV, DH, kvq.KVQ_FMT_E4M3, dev),
+                      out=torch.empty((1, HQ, DH), dtype=torch.bfloat16, device=dev)))
+    ws = kvq.new_workspace(1, HQ, HKV, DH, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    E4, PH = kvq.KVQ_FMT_E4M3, kvq.KVQ_SCALE_PER_HEAD
+    launches_per_step = LAYERS * 3  # write kernel; decode + reduce kernels
+
+    ev_w = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(LAYERS)]
+    ev_d = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(LAYERS)]
+    acc = {"write_ms": 0.0, "decode_ms": 0.0}
+
+    def step(timed):
+        for i, x in enumerate(L):
+            if timed:
+                ev_w[i][0].record(stream)
+            kvq.kvq_write(x["k"], x["v"], slots, x["kc"], x["vc"], x["ks"], x["vs"], PH, E4,
+                          dev_status=status)
+            if timed:
+                ev_w[i][1].record(stream)
+        for i, x in enumerate(L):
+            if timed:
+                ev_d[i][0].record(stream)
+            kvq.kvq_decode_attn(x["q"], x["kc"], x["vc"], bt, sl, None, x["ks"], x["vs"], PH, E4,
+                                0, ws, x["out"], dev_status=status)
+            if timed:
+                ev_d[i][1].record(stream)
+        if timed:
+            torch.cuda.synchronize()
+            acc["write_ms"] += sum(a.elapsed_time(b) for a, b in ev_w)
+            acc["decode_ms"] += sum(a.elapsed_time(b) for a, b in ev_d)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def rank_max(x):
+        return max_over_ranks(x, world, dev)
+
+    for _ in range(max(args.warmup, 3)):
+        step(False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # ---- device-resident timed region (per-call events inside, whole-step events around)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(False)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        total_ms = t0.elapsed_time(t1)
+        # per-call split, measured in separate timed passes (events add gaps)
+        for _ in range(args.steps):
+            step(True)
+    barrier()
+    total_ms = rank_max(total_ms)
+    ms_step = total_ms / args.steps
+    write_ms = rank_max(acc["write_ms"] / args.steps)
+    decode_ms = rank_max(acc["decode_ms"] / args.steps)
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barrier,
+                  rank_max)
+
+    peak, peak_src = measured_peaks()
+    write_launch_us = write_ms * 1e3 / LAYERS
+    decode_launch_us = decode_ms * 1e3 / LAYERS
+    w_ach = write_bytes(SEQ) / (write_launch_us * 1e-6) / 1e9
+    d_ach = decode_bytes(SEQ) / (decode_launch_us * 1e-6) / 1e9
+
+    def roof(name, ach, per_launch_bytes):
+        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": per_launch_bytes,
+                "traffic": recorded_traffic(name)}
+
+    dominant = "kvq_write" if write_ms >= decode_ms else "kvq_decode_attn"
+    res = {
+        "metric": METRIC,
+        "value": round(whole_job_gbs(world, STEP_BYTES, ms_step), 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3 cache, f16 MMA / f32 accumulate",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q, per-head amax/448 scales)",
+        "config": dict(WORKLOAD, parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "decode_attn": {"gbs": round(d_ach, 1), "frac_of_peak": round(d_ach / peak, 4),
+                        "us_per_layer": round(decode_launch_us, 2),
+                        "kv_tok_s": round(SEQ / (decode_launch_us * 1e-6), 0)},
+        "kv_write": {"gbs": round(w_ach, 1), "frac_of_peak": round(w_ach / peak, 4),
+                     "us_per_layer": round(write_launch_us, 2),
+                     "tok_s": round(SEQ / (write_launch_us * 1e-6), 0)},
+        "kv_tok_s": round(world * SEQ * LAYERS / (decode_ms * 1e-3), 0),
+        "roofline": roof(dominant, w_ach if dominant == "kvq_write" else d_ach,
+                         write_bytes(SEQ) if dominant == "kvq_write" else decode_bytes(SEQ)),
+        "roofline_decode": roof("kvq_decode_attn", d_ach, decode_bytes(SEQ)),
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(layers[0], st, args.cpu_seconds)
+    return res
+
+
+def run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barrier,
+            rank_max):
+    """Host buffers in, host result out: per step, copy every layer's K/V/Q from
+    pinned host memory (copy stream, one event per layer), run the same calls,
+    read the outputs back."""
+    hk = [torch.from_numpy(np.ascontiguousarray(l.k).view(np.int16)).pin_memory() for l in layers]
+    hv = [torch.from_numpy(np.ascontiguousarray(l.v).view(np.int16)).pin_memory() for l in layers]
+    hq = [torch.from_numpy(np.ascontiguousarray(l.q).view(np.int16)).pin_memory() for l in layers]
+    hslot = torch.from_numpy(st.slot_mapping).pin_memory()
+    hout = torch.empty((LAYERS, HQ, DH), dtype=torch.int16).pin_memory()
+    slot_d = torch.empty_like(hslot, device=dev)
+    bt = torch.from_numpy(st.block_tables).to(dev)
+    sl = torch.from_numpy(st.seq_lens).to(dev)
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
+    E4, PH = kvq.KVQ_FMT_E4M3, kvq.KVQ_SCALE_PER_HEAD
+    ready = [torch.cuda.Event() for _ in range(LAYERS)]
+    h2d = sum(x.numel() * 2 for x in hk + hv + hq) + hslot.numel() * 8
+    d2h = hout.numel() * 2
+
+    def step():
+        with torch.cuda.stream(copy):
+            copy.wait_stream(comp)
+            slot_d.copy_(hslot, non_blocking=True)
+            for i, x in enumerate(L):
+                x["k"].view(torch.int16).copy_(hk[i], non_blocking=True)
+                x["v"].view(torch.int16).copy_(hv[i], non_blocking=True)
+                x["q"].view(torch.int16).copy_(hq[i], non_blocking=True)
+                ready[i].record(copy)
+        for i, x in enumerate(L):
+            comp.wait_event(ready[i])
+            kvq.kvq_write(x["k"], x["v"], slot_d, x["kc"], x["vc"], x["ks"], x["vs"], PH, E4,
+                          dev_status=status)
+        for i, x in enumerate(L):
+            kvq.kvq_decode_attn(x["q"], x["kc"], x["vc"], bt, sl, None, x["ks"], x["vs"], PH, E4,
+                                0, ws, x["out"], dev_status=status)
+        for i, x in enumerate(L):
+            hout[i].copy_(x["out"][0].view(torch.int16), non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(2, min(args.steps, args.e2e_steps))
+    barrier()
+    t = time.perf_counter()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    el = rank_max(time.perf_counter() - t)
+    return {"value": round(whole_job_gbs(world, STEP_BYTES, el * 1e3 / n), 1), "unit": "GB/s",
+            "ms_per_step": round(el * 1e3 / n, 3), "steps": n,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample_step(lay, st, n_write_tokens, heads):
+    """One bounded sample of the workload on the CPU oracle: quantize-and-scatter
+    the first n_write_tokens tokens of the layer, and decode `heads` query heads
+    over the layer's full 32768-token cache.  Returns algorithmic bytes."""
+    import oracle
+    K = np.zeros((st.num_blocks, HKV, BS, DH), np.uint8)
+    V = np.zeros_like(K)
+    # the decode reads a fully written cache: write every token once (untimed
+    # by the caller only in the sense that it is counted as write bytes)
+    oracle.write(lay.k[:n_write_tokens], lay.v[:n_write_tokens], st.slot_mapping[:n_write_tokens],
+                 K, V, lay.k_scale, lay.v_scale, lay.gran, lay.fmt)
+    pairs = np.array([[0, h] for h in heads], np.int32)
+    oracle.decode_attn(lay.q, K, V, st.block_tables, st.seq_lens, lay.k_scale, lay.v_scale,
+                       lay.gran, lay.fmt, pairs=pairs)
+    return write_bytes(n_write_tokens) + decode_bytes(SEQ, len(heads))
+
+
+def cpu_baseline(lay, st, seconds):
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    done_bytes, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        done_bytes += oracle_sample_step(lay, st, SEQ, range(HQ))
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(done_bytes / el / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{reps} x one layer of the workload (write 32768 tokens, decode 32 heads "
+                      f"over 32768 tokens), float64 attention, OpenMP on {cores} threads, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores."""
+    import oracle
+    oracle.build()
+    st = workloads.structure(CFG)
+    lay = workloads.make_layer(CFG, 0, st=st)
+    cores = oracle.max_threads()
+    n_tok, heads = 4096, range(4)  # bounded per-step sample
+    for _ in range(max(args.warmup, 1)):
+        oracle_sample_step(lay, st, n_tok, heads)
+    t = time.perf_counter()
+    tot = 0
+    for _ in range(args.steps):
+        tot += oracle_sample_step(lay, st, n_tok, heads)
+    el = time.perf_counter() - t
+    v = round(tot / el / 1e9, 4)
+    sample = (f"per step: write 4096 tokens of one layer and decode 4 query heads over the "
+              f"32768-token cache (float64 oracle, OpenMP on {cores} threads)")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": max(args.warmup, 1),
+            "ms_per_step": round(el * 1e3 / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": WORKLOAD,
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

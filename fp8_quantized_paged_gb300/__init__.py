@@ -1,0 +1,180 @@
+"""Python binding of libkvq (FP8 paged KV cache for GB300).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+``_build/libkvq.so``, reached through the C ABI declared in
+``include/kvq.h``.  The functions carry the C names.  Tensors are torch CUDA
+tensors (torch provides device memory and streams); pointers, sizes and the
+current stream are passed to the library, a negative status raises
+``KvqError``.  There is no fallback: importing this package without the
+built library raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
+
+KVQ_FMT_BF16, KVQ_FMT_E4M3, KVQ_FMT_E5M2 = 0, 1, 2
+KVQ_SCALE_PER_TENSOR, KVQ_SCALE_PER_HEAD = 0, 1
+KVQ_OK, KVQ_ERR_NULL, KVQ_ERR_SHAPE, KVQ_ERR_ALIGN = 0, -1, -2, -3
+KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA, KVQ_ERR_ARG = -4, -5, -6, -7
+KVQ_DEV_BAD_SLOT, KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
+KVQ_DEV_INTERNAL = 16
+KVQ_Q_FP8 = 1
+BLOCK_SIZE = 16
+
+# exported symbol -> (restype, argtypes)
+_vp, _i32, _i64, _u32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint, ctypes.c_size_t
+SIGNATURES = {
+    "kvq_write": (_i32, [_vp, _vp, _i64, _vp, _i64, _i32, _i32, _vp, _vp, _i64, _i32, _vp, _i32,
+                         _vp, _i32, _i32, _i32, _vp, _vp]),
+    "kvq_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "kvq_decode_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
+                               _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _u32, _vp, _sz,
+                               _vp, _vp, _vp]),
+    "kvq_dequant_cache": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
+    "kvq_parse_dtype": (_i32, [ctypes.c_char_p]),
+    "kvq_layer_fmt": (_i32, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_char_p), _i32]),
+    "kvq_status_string": (ctypes.c_char_p, [_i32]),
+    "kvq_version": (_i32, []),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libkvq is not built ({LIB_PATH} missing); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kvq_status_string(status)} ({status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != KVQ_OK:
+        raise KvqError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _len(t):
+    return 0 if t is None else int(t.numel())
+
+
+# --------------------------------------------------------------------------
+# compute entry points (torch CUDA tensors)
+# --------------------------------------------------------------------------
+
+def kvq_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, scale_granularity, fmt,
+              dev_status=None, stream=None, token_stride=None) -> None:
+    """Quantize-and-scatter: k, v bf16 [N][Hkv][dh] (token stride may exceed Hkv*dh);
+    caches [num_blocks][Hkv][16][dh] uint8 (FP8) or bf16."""
+    n, hkv, dh = k.shape
+    stride = k.stride(0) if token_stride is None else token_stride
+    if v.stride(0) != stride or k.stride(1) != dh or k.stride(2) != 1 or v.stride(1) != dh:
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_write")
+    nb, hkv2, bs, dh2 = k_cache.shape
+    if (hkv2, dh2) != (hkv, dh) or v_cache.shape != k_cache.shape or tuple(v.shape) != (n, hkv, dh):
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_write")
+    st = _lib.kvq_write(_ptr(k), _ptr(v), stride, _ptr(slot_mapping), n, hkv, dh, _ptr(k_cache),
+                        _ptr(v_cache), nb, bs, _ptr(k_scale), _len(k_scale), _ptr(v_scale),
+                        _len(v_scale), scale_granularity, fmt, _ptr(dev_status), _stream(stream))
+    _check(st, "kvq_write")
+
+
+def kvq_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, num_sms=0) -> int:
+    return int(_lib.kvq_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              num_sms))
+
+
+def kvq_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, q_scale, k_scale, v_scale,
+                    scale_granularity, fmt, sliding_window, workspace, out, dev_status=None,
+                    stream=None, flags=0) -> None:
+    """Decode attention: q bf16 [B][Hq][dh] -> out bf16 [B][Hq][dh]."""
+    B, hq, dh = q.shape
+    nb, hkv, bs, dh2 = k_cache.shape
+    if dh2 != dh or tuple(out.shape) != (B, hq, dh) or block_tables.shape[0] != B:
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_decode_attn")
+    st = _lib.kvq_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                              block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, dh, nb, bs,
+                              _ptr(q_scale), _len(q_scale), _ptr(k_scale), _len(k_scale),
+                              _ptr(v_scale), _len(v_scale), scale_granularity, fmt,
+                              sliding_window, flags, _ptr(workspace), workspace.numel(), _ptr(out),
+                              _ptr(dev_status), _stream(stream))
+    _check(st, "kvq_decode_attn")
+
+
+def kvq_dequant_cache(src, dst_bf16, scale, scale_granularity, fmt, stream=None) -> None:
+    nb, hkv, bs, dh = src.shape
+    if tuple(dst_bf16.shape) != tuple(src.shape):
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_dequant_cache")
+    st = _lib.kvq_dequant_cache(_ptr(src), _ptr(dst_bf16), nb, hkv, bs, dh, _ptr(scale),
+                                _len(scale), scale_granularity, fmt, _stream(stream))
+    _check(st, "kvq_dequant_cache")
+
+
+# --------------------------------------------------------------------------
+# host helpers
+# --------------------------------------------------------------------------
+
+def kvq_parse_dtype(s: str) -> int:
+    return int(_lib.kvq_parse_dtype(None if s is None else s.encode()))
+
+
+def kvq_layer_fmt(fmt: int, layer_idx: int, is_sliding: bool, skip) -> int:
+    arr = (ctypes.c_char_p * max(len(skip), 1))(*[x.encode() for x in skip])
+    return int(_lib.kvq_layer_fmt(fmt, layer_idx, 1 if is_sliding else 0, arr, len(skip)))
+
+
+def kvq_status_string(status: int) -> str:
+    return _lib.kvq_status_string(status).decode()
+
+
+def kvq_version() -> int:
+    return int(_lib.kvq_version())
+
+
+# --------------------------------------------------------------------------
+# allocation helpers (torch memory; no compute)
+# --------------------------------------------------------------------------
+
+def new_cache(num_blocks, num_kv_heads, head_dim, fmt, device="cuda"):
+    import torch
+    dt = torch.bfloat16 if fmt == KVQ_FMT_BF16 else torch.uint8
+    return torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE, head_dim), dtype=dt, device=device)
+
+
+def new_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, device="cuda"):
+    import torch
+    n = kvq_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)
+    if n == 0:
+        raise KvqError(KVQ_ERR_ARG, "kvq_decode_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)

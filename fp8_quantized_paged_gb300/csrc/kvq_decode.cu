@@ -1,0 +1,926 @@
+// kvq_decode.cu -- paged GQA decode attention with the dequantization fused in.
+//
+// "10.4 KV Cache quantization: INT8, KIVI 2-bit, FP8 KV", section 10.4.2:
+// P = softmax(Q K^T / sqrt(dh) + mask), O = P V^, computed on the efficient
+// path that reads the compressed KV, restores it in registers and feeds QK,
+// PV and an online softmax directly; section 10.4.5: K^ = cast_float(K_fp8)
+// * sK.  The scale sK is folded into the logit scale and sV is applied once to
+// the normalised output, so the inner loop works on the raw codes.
+//
+// Work decomposition (one GPU, persistent grid)
+//   A unit of work is one KV-head page: block_size = 16 tokens of K and of V
+//   for one (sequence b, KV head g).  Units are numbered sequence by
+//   sequence, head by head, page by page; CTA c of P takes the contiguous
+//   range [floor(c W / P), floor((c+1) W / P)) of the W units, so every CTA
+//   streams the same number of bytes whatever the length mix.  A range cut
+//   through a (b, g) segment leaves partial softmax states (m, l, o) that the
+//   reduce kernel merges; a segment held by one CTA is written directly.
+//
+// Inside a CTA
+//   warp 4 (producer): one lane issues TMA tile loads of the K page and the V
+//   page of each unit into a ring of shared-memory stages (128-byte swizzle,
+//   mbarrier completion); the block ids of the next 32 units are fetched by
+//   the 32 lanes ahead of use.
+//   warps 0-3 (consumers): take the pages of the current segment round-robin.
+//   Per page: the K tile is an m16n8k16 A operand (16 tokens x 16 dims),
+//   converted FP8 -> f16 in registers (exact), against the G <= 8 query heads
+//   of the group as the B operand; the logits feed a warp online softmax; P
+//   (split into f16 hi + lo parts, ~22-bit weights) and the V tile (converted
+//   the same way, transposed with byte permutes) give O^T += V^T P^T.  The
+//   bf16 cache mode feeds the bf16 tiles to bf16 MMAs unchanged.
+//   Segment end: the four warps' states merge in shared memory.
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "kvq_common.cuh"
+#include "kvq_host.h"
+
+namespace kvq {
+
+constexpr int kBS = 16;  // tokens per page (block_size)
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kCtasPerSM = 2;
+constexpr int kMaxSeqs = 4096;
+constexpr int kMaxGroup = 8;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazily rescale O
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+template <int FMT, int DH>
+struct Cfg {
+  static constexpr int kElem = (FMT == KVQ_FMT_BF16) ? 2 : 1;
+  static constexpr int kRow = DH * kElem;         // bytes of one token row
+  static constexpr int kPage = kBS * kRow;        // bytes of one tensor's page
+  static constexpr int kSlot = 2 * kPage;         // K page + V page
+  // A multiple of the consumer-warp count: position pos of the CTA's page
+  // stream goes to warp pos % 4 and slot pos % kStages, so every slot is
+  // used by one warp only, in order, and a parity wait can never alias a
+  // phase two behind.
+  static constexpr int kStages =
+      kConsumerWarps * ((48 * 1024) / (kConsumerWarps * kSlot) > 0 ? (48 * 1024) / (kConsumerWarps * kSlot) : 1);
+  static constexpr uint32_t kSwz = (kRow >= 128) ? 7u : 3u;  // 128B or 64B swizzle
+};
+
+// Dynamic shared memory of the decode kernel (offsets from a 1024-aligned base).
+template <int FMT, int DH>
+struct SmemLayout {
+  using C = Cfg<FMT, DH>;
+  static constexpr int S = C::kStages;
+  static constexpr size_t ring = 0;
+  static constexpr size_t bars = ring + static_cast<size_t>(S) * C::kSlot;  // full[S], empty[S]
+  static constexpr size_t flags = bars + 2 * S * sizeof(uint64_t);  // bad[S], abort, issued, tot[8]
+  static constexpr size_t comb = (flags + (S + 2 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
+  static constexpr size_t comb_floats = 2 * kConsumerWarps * kMaxGroup + kConsumerWarps * kMaxGroup * DH;
+  static constexpr size_t seq = comb + comb_floats * sizeof(float);
+  static size_t total(int B) { return seq + (2 * static_cast<size_t>(B) + 1) * sizeof(int32_t) + 1024; }
+};
+
+struct DecodeParams {
+  const uint16_t* q;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  int max_blocks;
+  int B, Hq, Hkv, G;
+  int window;
+  int64_t num_blocks;
+  const float* ks;
+  const float* vs;
+  int per_head;
+  int P;
+  float logit_scale;  // log2(e) / sqrt(dh)
+  int32_t* ws_seq_off;
+  float* ws_ml;
+  float* ws_o;
+  uint16_t* out;
+  uint32_t* status;
+  int64_t rows;     // rows of the cache tensor maps (num_blocks * Hkv * 16)
+  int64_t n_slots;  // partial slots in the workspace
+};
+
+// Workspace: [B+1] int32 unit offsets, then per partial slot (m, l) pairs and
+// o vectors for the G heads of a group.  Partial slot of the piece of segment
+// sigma = b * Hkv + g held by CTA c is c + sigma (unique: ranges are ordered).
+struct WsLayout {
+  size_t seq_off, ml, o, total;
+};
+
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static WsLayout ws_layout(int B, int G, int Hkv, int DH, int P) {
+  WsLayout w;
+  const size_t slots = static_cast<size_t>(P) + static_cast<size_t>(B) * Hkv;
+  w.seq_off = 0;
+  w.ml = round256(sizeof(int32_t) * (static_cast<size_t>(B) + 1));
+  w.o = w.ml + round256(slots * G * 2 * sizeof(float));
+  w.total = w.o + round256(slots * G * DH * sizeof(float));
+  return w;
+}
+
+KVQ_DEVI uint32_t swz(uint32_t logical, uint32_t mask) {
+  return logical ^ (((logical >> 7) & mask) << 4);
+}
+
+// Byte b of token row r inside one staged page.  Rows of at most 128 bytes are
+// stored row after row; a 256-byte bf16 row (dh = 128) is staged as two
+// 16-row sub-tiles of 128-byte half rows, one TMA box each.
+template <int ROW>
+KVQ_DEVI uint32_t page_off(int r, int b) {
+  if (ROW > 128) return static_cast<uint32_t>((b >> 7) * (16 * 128) + r * 128 + (b & 127));
+  return static_cast<uint32_t>(r * ROW + b);
+}
+
+KVQ_DEVI uint4 lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr));
+  return r;
+}
+
+KVQ_DEVI uint2 lds64(uint32_t addr) {
+  uint2 r;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
+  return r;
+}
+
+KVQ_DEVI void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
+
+// Valid length of sequence b (same rule everywhere): out-of-range -> 0.
+KVQ_DEVI int seq_len_checked(const DecodeParams& p, int b) {
+  const int L = __ldg(p.seq_lens + b);
+  return (L < 0 || L > p.max_blocks * kBS) ? 0 : L;
+}
+
+KVQ_DEVI int window_lo(const DecodeParams& p, int L) {
+  return (p.window > 0 && L > p.window) ? L - p.window : 0;
+}
+
+// Last b with seq_off[b] <= u (seq_off non-decreasing, seq_off[B] > u).
+KVQ_DEVI int find_seq(const int32_t* seq_off, int B, int64_t u) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (seq_off[mid] <= u)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Exclusive scan of per-sequence unit counts into seq_off[0..B], and the
+// first page of every sequence's attended window into first_page[0..B).
+KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* first_page,
+                         int32_t* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (p.B + kThreads - 1) / kThreads;
+  const int b0 = tid * per, b1 = min(p.B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int raw = __ldg(p.seq_lens + b);
+    if ((raw < 0 || raw > p.max_blocks * kBS) && blockIdx.x == 0)
+      flag_status(p.status, KVQ_DEV_BAD_SEQLEN);
+    const int L = (raw < 0 || raw > p.max_blocks * kBS) ? 0 : raw;
+    const int fp = window_lo(p, L) / kBS;
+    const int pages = L > 0 ? (L + kBS - 1) / kBS - fp : 0;
+    first_page[b] = fp;
+    seq_off[b] = local;
+    local += pages * p.Hkv;
+  }
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += warp_tot[w];
+  const int excl = base + incl - local;
+  for (int b = b0; b < b1; ++b) seq_off[b] += excl;
+  if (tid == kThreads - 1) seq_off[p.B] = base + incl;
+  __syncthreads();
+}
+
+// Bounded mbarrier wait that also gives up when another warp has aborted.
+KVQ_DEVI bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u && *abort_flag) return false;
+  }
+  return false;
+}
+
+// --------------------------------------------------------------------------
+// One page of one consumer warp
+// --------------------------------------------------------------------------
+
+struct SoftmaxState {
+  float m[2];  // running max (log2 units) of heads 2t, 2t+1; warp-uniform per t
+  float l[2];  // per-lane partial denominators
+};
+
+// Online softmax update of one 16-token page; x holds log2-domain logits of
+// (token g, head 2t), (token g, head 2t+1), (token g+8, head 2t),
+// (token g+8, head 2t+1).  Returns the probabilities in pr; rescales o.
+template <int MT>
+KVQ_DEVI void softmax_page(float (&x)[4], float (&pr)[4], SoftmaxState& st, float (&o)[MT][4]) {
+  const float ninf = -INFINITY;
+  float lm0 = fmaxf(x[0], x[2]), lm1 = fmaxf(x[1], x[3]);
+  const bool need = (lm0 > st.m[0] + kRescaleThreshold) || (lm1 > st.m[1] + kRescaleThreshold);
+  if (__any_sync(kFull, need)) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      lm0 = fmaxf(lm0, __shfl_xor_sync(kFull, lm0, off));
+      lm1 = fmaxf(lm1, __shfl_xor_sync(kFull, lm1, off));
+    }
+    const float n0 = fmaxf(st.m[0], lm0), n1 = fmaxf(st.m[1], lm1);
+    const float a0 = (n0 == ninf) ? 1.f : fast_exp2(st.m[0] - n0);
+    const float a1 = (n1 == ninf) ? 1.f : fast_exp2(st.m[1] - n1);
+    st.l[0] *= a0;
+    st.l[1] *= a1;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      o[mt][0] *= a0;
+      o[mt][2] *= a0;
+      o[mt][1] *= a1;
+      o[mt][3] *= a1;
+    }
+    st.m[0] = n0;
+    st.m[1] = n1;
+  }
+  pr[0] = (x[0] == ninf) ? 0.f : fast_exp2(x[0] - st.m[0]);
+  pr[1] = (x[1] == ninf) ? 0.f : fast_exp2(x[1] - st.m[1]);
+  pr[2] = (x[2] == ninf) ? 0.f : fast_exp2(x[2] - st.m[0]);
+  pr[3] = (x[3] == ninf) ? 0.f : fast_exp2(x[3] - st.m[1]);
+  st.l[0] += pr[0] + pr[2];
+  st.l[1] += pr[1] + pr[3];
+}
+
+// P^T as the B operand of the PV MMA (k = token, n = head), split into a high
+// and a low 16-bit part.  PV uses the token order k -> {2t: 2t, 2t+1: 2t+8,
+// 2t+8: 2t+1, 2t+9: 2t+9} so that a lane's two k values of a register come
+// from one source lane's (token g', token g'+8) pair.
+template <bool BF16P>
+KVQ_DEVI void p_fragments(const float (&pr)[4], int g, int t, int G, uint32_t (&bh)[2],
+                          uint32_t (&bl)[2]) {
+  uint32_t h0, h1, l0, l1;
+  if (BF16P) {
+    h0 = f32x2_to_bf16x2(pr[0], pr[2]);
+    h1 = f32x2_to_bf16x2(pr[1], pr[3]);
+    l0 = f32x2_to_bf16x2(pr[0] - bf16lo_to_f32(h0), pr[2] - bf16hi_to_f32(h0));
+    l1 = f32x2_to_bf16x2(pr[1] - bf16lo_to_f32(h1), pr[3] - bf16hi_to_f32(h1));
+  } else {
+    h0 = f32x2_to_f16x2(pr[0], pr[2]);
+    h1 = f32x2_to_f16x2(pr[1], pr[3]);
+    l0 = f32x2_to_f16x2(pr[0] - f16lo_to_f32(h0), pr[2] - f16hi_to_f32(h0));
+    l1 = f32x2_to_f16x2(pr[1] - f16lo_to_f32(h1), pr[3] - f16hi_to_f32(h1));
+  }
+  const int srcA = (2 * t) * 4 + (g >> 1), srcB = (2 * t + 1) * 4 + (g >> 1);
+  const bool odd = g & 1;
+  const uint32_t ha0 = __shfl_sync(kFull, h0, srcA), ha1 = __shfl_sync(kFull, h1, srcA);
+  const uint32_t hb0 = __shfl_sync(kFull, h0, srcB), hb1 = __shfl_sync(kFull, h1, srcB);
+  const uint32_t la0 = __shfl_sync(kFull, l0, srcA), la1 = __shfl_sync(kFull, l1, srcA);
+  const uint32_t lb0 = __shfl_sync(kFull, l0, srcB), lb1 = __shfl_sync(kFull, l1, srcB);
+  const bool live = g < G;
+  bh[0] = live ? (odd ? ha1 : ha0) : 0u;
+  bh[1] = live ? (odd ? hb1 : hb0) : 0u;
+  bl[0] = live ? (odd ? la1 : la0) : 0u;
+  bl[1] = live ? (odd ? lb1 : lb0) : 0u;
+}
+
+KVQ_DEVI bool token_valid(int tok, int lo, int L, bool bad) { return !bad && tok >= lo && tok < L; }
+
+KVQ_DEVI void mask_logits(float (&x)[4], int tok0, int g, int lo, int L, bool bad) {
+  const int ta = tok0 + g, tb = tok0 + g + 8;
+  if (bad || ta < lo || ta >= L) x[0] = x[1] = -INFINITY;
+  if (bad || tb < lo || tb >= L) x[2] = x[3] = -INFINITY;
+}
+
+// FP8 page (E4M3 / E5M2).
+template <int FMT, int DH>
+KVQ_DEVI void page_fp8(uint32_t kp, uint32_t vp, int g, int t, int G,
+                       const uint32_t (&qb)[DH / 16][2], float (&o)[DH / 16][4], SoftmaxState& st,
+                       float lscale, int tok0, int lo, int L, bool bad) {
+  using C = Cfg<FMT, DH>;
+  constexpr int KW = DH / 16;  // 32-bit words of one K row a lane reads
+  uint32_t k0[KW], k1[KW];
+#pragma unroll
+  for (int c = 0; c < KW / 4; ++c) {
+    const uint32_t off = static_cast<uint32_t>(t * (DH / 4) + c * 16);
+    const uint4 a = lds128(kp + swz(g * C::kRow + off, C::kSwz));
+    const uint4 b = lds128(kp + swz((g + 8) * C::kRow + off, C::kSwz));
+    k0[4 * c] = a.x; k0[4 * c + 1] = a.y; k0[4 * c + 2] = a.z; k0[4 * c + 3] = a.w;
+    k1[4 * c] = b.x; k1[4 * c + 1] = b.y; k1[4 * c + 2] = b.z; k1[4 * c + 3] = b.w;
+  }
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < KW; ++kk) {
+    uint32_t a[4];
+    a[0] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(k0[kk] & 0xFFFFu));
+    a[1] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(k1[kk] & 0xFFFFu));
+    a[2] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(k0[kk] >> 16));
+    a[3] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(k1[kk] >> 16));
+    mma_f16(s, a, qb[kk][0], qb[kk][1]);
+  }
+  float x[4] = {s[0] * lscale, s[1] * lscale, s[2] * lscale, s[3] * lscale};
+  mask_logits(x, tok0, g, lo, L, bad);
+  float pr[4];
+  softmax_page<DH / 16>(x, pr, st, o);
+  uint32_t bh[2], bl[2];
+  p_fragments<false>(pr, g, t, G, bh, bl);
+
+  constexpr int VW = DH / 32;  // 32-bit words of one V row a lane reads
+  uint32_t A[VW], B[VW], Cc[VW], D[VW];
+  const int rows[4] = {2 * t, 2 * t + 8, 2 * t + 1, 2 * t + 9};
+  uint32_t* dst[4] = {A, B, Cc, D};
+  const bool edge = bad || tok0 < lo || tok0 + kBS > L;  // warp-uniform
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t addr = vp + swz(rows[r] * C::kRow + g * (DH / 8), C::kSwz);
+    if (VW == 4) {
+      const uint4 v = lds128(addr);
+      dst[r][0] = v.x; dst[r][1] = v.y; dst[r][2] = v.z; dst[r][3] = v.w;
+    } else {
+      const uint2 v = lds64(addr);
+      dst[r][0] = v.x; dst[r][1] = v.y;
+    }
+    if (edge && !token_valid(tok0 + rows[r], lo, L, bad)) {
+#pragma unroll
+      for (int w = 0; w < VW; ++w) dst[r][w] = 0u;
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < VW; ++w) {
+    const uint32_t x0 = prmt(A[w], B[w], 0x5140u), y0 = prmt(A[w], B[w], 0x7362u);
+    const uint32_t z0 = prmt(Cc[w], D[w], 0x5140u), u0 = prmt(Cc[w], D[w], 0x7362u);
+    uint32_t a[4];
+    a[0] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(x0 & 0xFFFFu));
+    a[1] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(x0 >> 16));
+    a[2] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(z0 & 0xFFFFu));
+    a[3] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(z0 >> 16));
+    mma_f16(o[2 * w], a, bh[0], bh[1]);
+    mma_f16(o[2 * w], a, bl[0], bl[1]);
+    a[0] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(y0 & 0xFFFFu));
+    a[1] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(y0 >> 16));
+    a[2] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(u0 & 0xFFFFu));
+    a[3] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(u0 >> 16));
+    mma_f16(o[2 * w + 1], a, bh[0], bh[1]);
+    mma_f16(o[2 * w + 1], a, bl[0], bl[1]);
+  }
+}
+
+// bf16 page (layers skipped from quantization).
+template <int DH>
+KVQ_DEVI void page_bf16(uint32_t kp, uint32_t vp, int g, int t, int G,
+                        const uint32_t (&qb)[DH / 16][2], float (&o)[DH / 16][4],
+                        SoftmaxState& st, float lscale, int tok0, int lo, int L, bool bad) {
+  using C = Cfg<KVQ_FMT_BF16, DH>;
+  constexpr int KW = DH / 8;  // words of one K row a lane reads (2 bf16 each)
+  uint32_t k0[KW], k1[KW];
+#pragma unroll
+  for (int c = 0; c < KW / 4; ++c) {
+    const int off = t * (DH / 2) + c * 16;
+    const uint4 a = lds128(kp + swz(page_off<C::kRow>(g, off), C::kSwz));
+    const uint4 b = lds128(kp + swz(page_off<C::kRow>(g + 8, off), C::kSwz));
+    k0[4 * c] = a.x; k0[4 * c + 1] = a.y; k0[4 * c + 2] = a.z; k0[4 * c + 3] = a.w;
+    k1[4 * c] = b.x; k1[4 * c + 1] = b.y; k1[4 * c + 2] = b.z; k1[4 * c + 3] = b.w;
+  }
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < DH / 16; ++kk) {
+    const uint32_t a[4] = {k0[2 * kk], k1[2 * kk], k0[2 * kk + 1], k1[2 * kk + 1]};
+    mma_bf16(s, a, qb[kk][0], qb[kk][1]);
+  }
+  float x[4] = {s[0] * lscale, s[1] * lscale, s[2] * lscale, s[3] * lscale};
+  mask_logits(x, tok0, g, lo, L, bad);
+  float pr[4];
+  softmax_page<DH / 16>(x, pr, st, o);
+  uint32_t bh[2], bl[2];
+  p_fragments<true>(pr, g, t, G, bh, bl);
+
+  constexpr int VW = DH / 16;  // words of one V row a lane reads
+  uint32_t V[4][VW];
+  const int rows[4] = {2 * t, 2 * t + 8, 2 * t + 1, 2 * t + 9};
+  const bool edge = bad || tok0 < lo || tok0 + kBS > L;  // warp-uniform
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+#pragma unroll
+    for (int c = 0; c < VW / 4; ++c) {
+      const uint4 v = lds128(vp + swz(page_off<C::kRow>(rows[r], g * (DH / 4) + c * 16), C::kSwz));
+      V[r][4 * c] = v.x; V[r][4 * c + 1] = v.y; V[r][4 * c + 2] = v.z; V[r][4 * c + 3] = v.w;
+    }
+    if (edge && !token_valid(tok0 + rows[r], lo, L, bad)) {
+#pragma unroll
+      for (int w = 0; w < VW; ++w) V[r][w] = 0u;
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < VW; ++w) {
+    const uint32_t a[4] = {prmt(V[0][w], V[1][w], 0x5410u), prmt(V[0][w], V[1][w], 0x7632u),
+                           prmt(V[2][w], V[3][w], 0x5410u), prmt(V[2][w], V[3][w], 0x7632u)};
+    mma_bf16(o[w], a, bh[0], bh[1]);
+    mma_bf16(o[w], a, bl[0], bl[1]);
+  }
+}
+
+// Q of head g (lane row) of the group, dims t*(DH/4) + 4kk + {0..3}, as the
+// B operand of the QK MMA: f16 for the FP8 caches (exact for |q| in the f16
+// normal range), the bf16 bits for the bf16 cache.
+template <int FMT, int DH>
+KVQ_DEVI void load_q(const DecodeParams& p, int b, int gkv, int g, int t,
+                     uint32_t (&qb)[DH / 16][2]) {
+  if (g >= p.G) {
+#pragma unroll
+    for (int kk = 0; kk < DH / 16; ++kk) qb[kk][0] = qb[kk][1] = 0u;
+    return;
+  }
+  const int64_t qrow = static_cast<int64_t>(b) * p.Hq + gkv * p.G + g;
+  if (!guard(b >= 0 && b < p.B && qrow >= 0 && qrow < static_cast<int64_t>(p.B) * p.Hq, p.status, 2)) {
+#pragma unroll
+    for (int kk = 0; kk < DH / 16; ++kk) qb[kk][0] = qb[kk][1] = 0u;
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * DH + t * (DH / 4));
+  uint32_t w[DH / 8];
+#pragma unroll
+  for (int i = 0; i < DH / 32; ++i) {
+    const uint4 v = __ldg(src + i);
+    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+  }
+#pragma unroll
+  for (int kk = 0; kk < DH / 16; ++kk) {
+    if (FMT == KVQ_FMT_BF16) {
+      qb[kk][0] = w[2 * kk];
+      qb[kk][1] = w[2 * kk + 1];
+    } else {
+      qb[kk][0] = f32x2_to_f16x2(bf16lo_to_f32(w[2 * kk]), bf16hi_to_f32(w[2 * kk]));
+      qb[kk][1] = f32x2_to_f16x2(bf16lo_to_f32(w[2 * kk + 1]), bf16hi_to_f32(w[2 * kk + 1]));
+    }
+  }
+}
+
+KVQ_DEVI uint16_t to_bf16(float x) { return static_cast<uint16_t>(f32x2_to_bf16x2(x, 0.f)); }
+
+// --------------------------------------------------------------------------
+// Decode kernel
+// --------------------------------------------------------------------------
+
+template <int FMT, int DH>
+__global__ void __launch_bounds__(kThreads, kCtasPerSM)
+    decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv) {
+  using C = Cfg<FMT, DH>;
+  constexpr int S = C::kStages;
+  constexpr int MT = DH / 16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  using SL = SmemLayout<FMT, DH>;
+  uint8_t* ring = smem + SL::ring;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::bars);
+  uint64_t* empty = full + S;
+  uint32_t* bad_s = reinterpret_cast<uint32_t*>(smem + SL::flags);
+  volatile uint32_t* abort_flag = bad_s + S;
+  int32_t* issued_s = reinterpret_cast<int32_t*>(bad_s + S + 1);
+  int32_t* warp_tot = issued_s + 1;                        // [8]
+  float* cm = reinterpret_cast<float*>(smem + SL::comb);   // [4][8] running max
+  float* cl = cm + kConsumerWarps * kMaxGroup;             // [4][8] denominators
+  float* co = cl + kConsumerWarps * kMaxGroup;             // [4][8][DH] unnormalised O
+  int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq);  // [B+1]
+  int32_t* first_page = seq_off + p.B + 1;                        // [B]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_flag = 0u;
+    *issued_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  build_plan(p, seq_off, first_page, warp_tot);  // contains __syncthreads
+
+  const int64_t W = seq_off[p.B];
+  if (blockIdx.x == 0)
+    for (int b = tid; b <= p.B; b += kThreads) p.ws_seq_off[b] = seq_off[b];
+  // Effective partition size: never more CTAs than units, so every CTA of the
+  // partition owns at least one unit (the reduce relies on it); the others idle.
+  const int64_t Pe = W < p.P ? W : p.P;
+  const int64_t c = blockIdx.x;
+  const int64_t u0 = c < Pe ? c * W / Pe : 0;
+  const int64_t u1 = c < Pe ? (c + 1) * W / Pe : 0;
+  const int64_t total = u1 - u0;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    int nxt_blk = 0, nxt_g = 0;
+    auto fetch = [&](int64_t i, int& blk, int& g) {
+      blk = 0;
+      g = 0;
+      if (i < total) {
+        const int64_t u = u0 + i;
+        const int b = find_seq(seq_off, p.B, u);
+        const int pages = (seq_off[b + 1] - seq_off[b]) / p.Hkv;
+        const int r = static_cast<int>(u - seq_off[b]);
+        g = r / pages;
+        const int pg = r - g * pages;
+        const int col = first_page[b] + pg;
+        if (guard(b >= 0 && b < p.B && col >= 0 && col < p.max_blocks && g >= 0 && g < p.Hkv,
+                  p.status, 0))
+          blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + col);
+        else
+          blk = -1;
+      }
+    };
+    fetch(lane, nxt_blk, nxt_g);
+    bool stop = false;
+    int64_t issued = 0;
+    for (int64_t base = 0; base < total && !stop; base += 32) {
+      const int cur_blk = nxt_blk, cur_g = nxt_g;
+      if (base + 32 < total) fetch(base + 32 + lane, nxt_blk, nxt_g);
+      const int cnt = static_cast<int>(total - base < 32 ? total - base : 32);
+      for (int i = 0; i < cnt; ++i) {
+        const int blk = __shfl_sync(kFull, cur_blk, i);
+        const int g = __shfl_sync(kFull, cur_g, i);
+        if (lane == 0 && !stop) {
+          const int64_t pos = base + i;
+          const int slot = static_cast<int>(pos % S);
+          const uint32_t par = static_cast<uint32_t>((pos / S) & 1) ^ 1u;
+          if (!wait_or_abort(&empty[slot], par, abort_flag)) {
+            *abort_flag = 1u;
+            flag_status(p.status, KVQ_DEV_WAIT_TIMEOUT);
+            stop = true;
+          } else {
+            const bool bad = blk < 0 || blk >= p.num_blocks;
+            if (bad) flag_status(p.status, KVQ_DEV_BAD_BLOCK);
+            bad_s[slot] = bad ? 1u : 0u;
+            int32_t row = ((bad ? 0 : blk) * p.Hkv + g) * kBS;
+            if (!guard(row >= 0 && row + kBS <= p.rows && slot >= 0 && slot < S, p.status, 1)) {
+              row = 0;
+              bad_s[slot % S] = 1u;
+            }
+            uint8_t* dstK = ring + slot * C::kSlot;
+            mbar_arrive_expect_tx(&full[slot], C::kSlot);
+            if (C::kRow > 128) {  // two 128-byte column boxes per page
+              tma_load_2d(dstK, &tmk, 0, row, &full[slot]);
+              tma_load_2d(dstK + C::kPage / 2, &tmk, 64, row, &full[slot]);
+              tma_load_2d(dstK + C::kPage, &tmv, 0, row, &full[slot]);
+              tma_load_2d(dstK + C::kPage + C::kPage / 2, &tmv, 64, row, &full[slot]);
+            } else {
+              tma_load_2d(dstK, &tmk, 0, row, &full[slot]);
+              tma_load_2d(dstK + C::kPage, &tmv, 0, row, &full[slot]);
+            }
+            issued = pos + 1;
+          }
+        }
+        stop = __shfl_sync(kFull, stop ? 1 : 0, 0) != 0;
+      }
+    }
+    if (lane == 0) *issued_s = static_cast<int32_t>(issued);
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int g = lane >> 2, t = lane & 3;
+    const int ctid = tid;  // 0 .. 127
+    uint32_t qb[MT][2];
+    float o[MT][4];
+    int64_t pos_base = 0;
+    bool aborted = false;
+    for (int64_t u = u0; u < u1;) {
+      const int b = find_seq(seq_off, p.B, u);
+      const int seg_units = seq_off[b + 1] - seq_off[b];
+      const int pages = seg_units / p.Hkv;
+      if (!guard(pages > 0 && u >= seq_off[b] && u < seq_off[b + 1], p.status, 10)) break;
+      const int r = static_cast<int>(u - seq_off[b]);
+      const int gkv = r / pages;
+      const int p0 = r - gkv * pages;
+      const int n = static_cast<int>((u1 - u) < (pages - p0) ? (u1 - u) : (pages - p0));
+      const int L = seq_len_checked(p, b);
+      const int lo = window_lo(p, L);
+      const int fp = first_page[b];
+      const float sk = (FMT == KVQ_FMT_BF16) ? 1.f : __ldg(p.ks + (p.per_head ? gkv : 0));
+      const float sv = (FMT == KVQ_FMT_BF16) ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
+      const float lscale = sk * p.logit_scale;
+      load_q<FMT, DH>(p, b, gkv, g, t, qb);
+      SoftmaxState st;
+      st.m[0] = st.m[1] = -INFINITY;
+      st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+      static_assert(S % kConsumerWarps == 0, "slots must split evenly among the consumer warps");
+      const int j0 = (warp - static_cast<int>(pos_base % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+      for (int j = j0; j < n; j += kConsumerWarps) {
+        const int64_t pos = pos_base + j;
+        const int slot = static_cast<int>(pos % S);
+        const uint32_t par = static_cast<uint32_t>((pos / S) & 1);
+        if (!aborted && !wait_or_abort(&full[slot], par, abort_flag)) {
+          aborted = true;
+          if (lane == 0) {
+            *abort_flag = 1u;
+            flag_status(p.status, KVQ_DEV_WAIT_TIMEOUT);
+          }
+        }
+        aborted = __shfl_sync(kFull, aborted ? 1 : 0, 0) != 0;
+        if (!aborted) {
+          const uint32_t kp = smem_u32(ring + slot * C::kSlot);
+          const int tok0 = (fp + p0 + j) * kBS;
+          const bool bad = bad_s[slot] != 0u;
+          if (FMT == KVQ_FMT_BF16)
+            page_bf16<DH>(kp, kp + C::kPage, g, t, p.G, qb, o, st, lscale, tok0, lo, L, bad);
+          else
+            page_fp8<FMT, DH>(kp, kp + C::kPage, g, t, p.G, qb, o, st, lscale, tok0, lo, L, bad);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
+
+      // ---- merge the four warps' states of this segment piece
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        st.l[0] += __shfl_xor_sync(kFull, st.l[0], off);
+        st.l[1] += __shfl_xor_sync(kFull, st.l[1], off);
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int h = 2 * t + c;
+        if (h < p.G) {
+          if (g == 0) {
+            cm[warp * kMaxGroup + h] = st.m[c];
+            cl[warp * kMaxGroup + h] = st.l[c];
+          }
+          float* dst = co + (warp * kMaxGroup + h) * DH + g * (DH / 8);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+            *reinterpret_cast<float2*>(dst + 2 * mt) = make_float2(o[mt][c], o[mt][2 + c]);
+        }
+      }
+      consumer_bar();
+      const bool single = (p0 == 0 && n == pages);
+      const int64_t slot_idx = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(b) * p.Hkv + gkv;
+      for (int idx = ctid; idx < p.G * DH; idx += kConsumerWarps * 32) {
+        const int h = idx / DH, d = idx - h * DH;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * kMaxGroup + h]);
+        float acc = 0.f, ls = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = cm[w * kMaxGroup + h];
+            const float sc = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+            acc += co[(w * kMaxGroup + h) * DH + d] * sc;
+            ls += cl[w * kMaxGroup + h] * sc;
+          }
+        }
+        if (single) {
+          const float val = ls > 0.f ? acc / ls * sv : 0.f;
+          const int64_t oi = (static_cast<int64_t>(b) * p.Hq + gkv * p.G + h) * DH + d;
+          if (guard(oi >= 0 && oi < static_cast<int64_t>(p.B) * p.Hq * DH, p.status, 3))
+            p.out[oi] = to_bf16(val);
+        } else if (guard(slot_idx >= 0 && slot_idx < p.n_slots, p.status, 4)) {
+          p.ws_o[(slot_idx * p.G + h) * DH + d] = acc;
+          if (d == 0) {
+            p.ws_ml[(slot_idx * p.G + h) * 2] = M;
+            p.ws_ml[(slot_idx * p.G + h) * 2 + 1] = ls;
+          }
+        }
+      }
+      consumer_bar();
+      pos_base += n;
+      u += n;
+    }
+  }
+  __syncthreads();
+  // After an abort, wait (bounded) for copies still in flight before exit.
+  if (*abort_flag && tid == 0) {
+    const int64_t issued = *issued_s;
+    for (int64_t pos = issued > S ? issued - S : 0; pos < issued; ++pos)
+      mbar_wait(&full[pos % S], static_cast<uint32_t>((pos / S) & 1));
+  }
+}
+
+// Merge of the partial states of segments split across CTAs.
+template <int DH>
+__global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p) {
+  const int b = blockIdx.x / p.Hkv, gkv = blockIdx.x - b * p.Hkv;
+  const int64_t W = p.ws_seq_off[p.B];
+  const int64_t so = p.ws_seq_off[b];
+  const int pages = (p.ws_seq_off[b + 1] - p.ws_seq_off[b]) / p.Hkv;
+  uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + gkv * p.G) * DH;
+  if (pages == 0) {
+    for (int idx = threadIdx.x; idx < p.G * DH; idx += blockDim.x) out[idx] = 0;
+    return;
+  }
+  const int64_t us = so + static_cast<int64_t>(gkv) * pages, ue = us + pages;
+  // CTAs c < Pe own [floor(c W / Pe), floor((c+1) W / Pe)), all non-empty;
+  // the CTA holding unit u is ceil((u+1) Pe / W) - 1.
+  const int64_t Pe = W < p.P ? W : p.P;
+  const int64_t c_lo = ((us + 1) * Pe + W - 1) / W - 1;
+  const int64_t c_hi = (ue * Pe + W - 1) / W - 1;
+  if (c_lo == c_hi) return;  // one CTA held the whole segment and wrote it
+  const float sv = (p.vs == nullptr) ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
+  const int64_t sigma = static_cast<int64_t>(b) * p.Hkv + gkv;
+  if (!guard(c_lo >= 0 && c_hi < Pe && c_lo <= c_hi && c_hi + sigma < p.n_slots, p.status, 5))
+    return;
+  for (int idx = threadIdx.x; idx < p.G * DH; idx += blockDim.x) {
+    const int h = idx / DH, d = idx - h * DH;
+    float M = -INFINITY;
+    for (int64_t c = c_lo; c <= c_hi; ++c) M = fmaxf(M, p.ws_ml[((c + sigma) * p.G + h) * 2]);
+    float acc = 0.f, ls = 0.f;
+    if (M != -INFINITY) {
+      for (int64_t c = c_lo; c <= c_hi; ++c) {
+        const int64_t s = (c + sigma) * p.G + h;
+        const float m = p.ws_ml[s * 2];
+        const float sc = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+        acc += p.ws_o[s * DH + d] * sc;
+        ls += p.ws_ml[s * 2 + 1] * sc;
+      }
+    }
+    out[h * DH + d] = to_bf16(ls > 0.f ? acc / ls * sv : 0.f);
+  }
+}
+
+// --------------------------------------------------------------------------
+// Host side
+// --------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tensor map of one cache tensor viewed as 2D: rows of head_dim elements
+// (num_blocks * Hkv * 16 rows).  One box is 16 rows by at most 128 bytes,
+// swizzled so that the decode kernel's fragment reads are free of bank
+// conflicts; a 256-byte bf16 row takes two boxes (x = 0 and x = 64).
+static bool make_cache_map(CUtensorMap* m, const void* base, int fmt, int dh, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const int elem = fmt == KVQ_FMT_BF16 ? 2 : 1;
+  const int row_bytes = dh * elem;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(dh), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes > 128 ? 128 / elem : dh), kBS};
+  const cuuint32_t es[2] = {1, 1};
+  const CUtensorMapSwizzle sw =
+      row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r =
+      enc(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+          const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int FMT, int DH>
+static size_t smem_bytes(int B) {
+  return SmemLayout<FMT, DH>::total(B);
+}
+
+template <int FMT, int DH>
+static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                  cudaStream_t s) {
+  const size_t smem = smem_bytes<FMT, DH>(p.B);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    const size_t maxsmem = smem_bytes<FMT, DH>(kMaxSeqs);
+    if (cudaFuncSetAttribute(decode_kernel<FMT, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(maxsmem)) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  decode_kernel<FMT, DH><<<p.P, kThreads, smem, s>>>(p, tk, tv);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  reduce_kernel<DH><<<p.B * p.Hkv, 128, 0, s>>>(p);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int num_sms) {
+  if (num_seqs <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads)
+    return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
+  if (num_sms <= 0) num_sms = device_sm_count();
+  if (num_sms <= 0) return 0;
+  const int G = num_q_heads / num_kv_heads;
+  return ws_layout(num_seqs, G, num_kv_heads, head_dim, kCtasPerSM * num_sms).total;
+}
+
+extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int64_t num_blocks,
+                               int block_size, const float* q_scale, int q_scale_len,
+                               const float* k_scale, int k_scale_len, const float* v_scale,
+                               int v_scale_len, int scale_granularity, int fmt,
+                               int sliding_window, unsigned flags, void* workspace,
+                               size_t workspace_bytes, void* out, uint32_t* dev_status,
+                               kvq_stream_t stream) {
+  if (fmt < KVQ_FMT_BF16 || fmt > KVQ_FMT_E5M2) return KVQ_ERR_ARG;
+  if (scale_granularity != KVQ_SCALE_PER_TENSOR && scale_granularity != KVQ_SCALE_PER_HEAD)
+    return KVQ_ERR_ARG;
+  if (flags & KVQ_Q_FP8) return KVQ_ERR_UNSUPPORTED;
+  if (flags & ~KVQ_Q_FP8) return KVQ_ERR_ARG;
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0 || sliding_window < 0)
+    return KVQ_ERR_ARG;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace || !out)
+    return KVQ_ERR_NULL;
+  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (block_size != kBS) return KVQ_ERR_UNSUPPORTED;
+  if (num_q_heads % num_kv_heads) return KVQ_ERR_SHAPE;
+  const int G = num_q_heads / num_kv_heads;
+  if (G > kMaxGroup) return KVQ_ERR_UNSUPPORTED;
+  if (num_seqs > kMaxSeqs) return KVQ_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * num_kv_heads >= (int64_t(1) << 31))
+    return KVQ_ERR_UNSUPPORTED;
+  if (num_blocks * num_kv_heads * kBS >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return KVQ_ERR_ALIGN;
+  if (fmt != KVQ_FMT_BF16) {
+    if (!k_scale || !v_scale) return KVQ_ERR_NULL;
+    const int want = scale_granularity == KVQ_SCALE_PER_HEAD ? num_kv_heads : 1;
+    if (k_scale_len != want || v_scale_len != want) return KVQ_ERR_SHAPE;
+  }
+  if (q_scale) {
+    const int want = scale_granularity == KVQ_SCALE_PER_HEAD ? num_q_heads : 1;
+    if (q_scale_len != want) return KVQ_ERR_SHAPE;
+  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return KVQ_ERR_CUDA;
+  const int64_t max_units = static_cast<int64_t>(num_seqs) * max_blocks_per_seq * num_kv_heads;
+  const int P = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(kCtasPerSM) * sms, max_units));
+  const WsLayout wl = ws_layout(num_seqs, G, num_kv_heads, head_dim, kCtasPerSM * sms);
+  if (workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
+
+  DecodeParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.max_blocks = max_blocks_per_seq;
+  p.B = num_seqs;
+  p.Hq = num_q_heads;
+  p.Hkv = num_kv_heads;
+  p.G = G;
+  p.window = sliding_window;
+  p.num_blocks = num_blocks;
+  p.ks = fmt == KVQ_FMT_BF16 ? nullptr : k_scale;
+  p.vs = fmt == KVQ_FMT_BF16 ? nullptr : v_scale;
+  p.per_head = scale_granularity == KVQ_SCALE_PER_HEAD;
+  p.P = P;
+  p.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws_seq_off = reinterpret_cast<int32_t*>(ws + wl.seq_off);
+  p.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
+  p.ws_o = reinterpret_cast<float*>(ws + wl.o);
+  p.out = static_cast<uint16_t*>(out);
+  p.status = dev_status;
+  p.rows = num_blocks * num_kv_heads * kBS;
+  p.n_slots = static_cast<int64_t>(kCtasPerSM) * sms + static_cast<int64_t>(num_seqs) * num_kv_heads;
+
+  CUtensorMap tk, tv;
+  const uint64_t rows = static_cast<uint64_t>(num_blocks) * num_kv_heads * kBS;
+  if (!make_cache_map(&tk, k_cache, fmt, head_dim, rows) ||
+      !make_cache_map(&tv, v_cache, fmt, head_dim, rows))
+    return KVQ_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (fmt) {
+    case KVQ_FMT_E4M3:
+      return head_dim == 128 ? launch<KVQ_FMT_E4M3, 128>(p, tk, tv, s)
+                             : launch<KVQ_FMT_E4M3, 64>(p, tk, tv, s);
+    case KVQ_FMT_E5M2:
+      return head_dim == 128 ? launch<KVQ_FMT_E5M2, 128>(p, tk, tv, s)
+                             : launch<KVQ_FMT_E5M2, 64>(p, tk, tv, s);
+    default:
+      return head_dim == 128 ? launch<KVQ_FMT_BF16, 128>(p, tk, tv, s)
+                             : launch<KVQ_FMT_BF16, 64>(p, tk, tv, s);
+  }
+}

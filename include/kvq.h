@@ -1,0 +1,224 @@
+/*
+ * kvq.h -- C ABI of libkvq: FP8 paged KV cache for NVIDIA GB300 (sm_103a).
+ *
+ * Two operations make the hot path of a quantized-KV-cache decoder:
+ *
+ *   kvq_write        quantize bf16 K/V with cast_fp8(x / s) and scatter the
+ *                    codes into a paged cache ("10.4 KV Cache quantization:
+ *                    INT8, KIVI 2-bit, FP8 KV", section 10.4.5; the INT8
+ *                    analogue of the write is section 10.4.2).
+ *   kvq_decode_attn  decode attention straight off that cache with the
+ *                    dequantization fused in: P = softmax(Q K^T / sqrt(dh)),
+ *                    O = P V^, K^ = cast_float(K_fp8) * sK, V^ likewise
+ *                    (section 10.4.2 "efficient path", section 10.4.5).
+ *
+ * plus the unfused ablation (kvq_dequant_cache, section 10.4.2 "inefficient
+ * path": a separate dequant kernel that materialises a bf16 cache) and the
+ * host helpers that mirror the configuration surface described in the
+ * "vLLM FP8 quantized KV cache guide" (kv_cache_dtype strings, per-tensor
+ * and per-attention-head scales, skip layers).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All pointers passed to the compute calls are DEVICE pointers on the
+ *   current CUDA device, except where a parameter says "host".  The caller
+ *   owns every buffer (inputs, caches, scales, workspace, outputs, status).
+ *   The library keeps no state between calls and allocates no device memory.
+ * - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *   stream).  Calls do not synchronize and never read device memory on the
+ *   host: scale values are only read on the device.
+ * - Return value: KVQ_OK (0), or a negative kvq_status.  Host-detectable
+ *   errors are returned BEFORE anything is enqueued.  KVQ_ERR_CUDA reports a
+ *   launch error (cudaGetLastError after the launch).
+ * - Device-detected bad indices (a slot past the cache, a block id outside
+ *   [0, num_blocks), a sequence length outside [0, max_blocks_per_seq *
+ *   block_size]) never trap: the offending work item is skipped (its tokens
+ *   are masked out of attention, or not written) and a KVQ_DEV_* bit is OR-ed
+ *   into *dev_status when dev_status is not NULL.  The caller reads the word
+ *   after synchronizing.  Bounded waits inside the kernels that run out set
+ *   KVQ_DEV_WAIT_TIMEOUT and the kernel returns early.
+ * - Cache layout, per layer and per tensor (K and V separately):
+ *     [num_blocks][num_kv_heads][block_size][head_dim]
+ *   elements are uint8 FP8 codes (fmt E4M3 / E5M2) or bf16 (fmt BF16, the
+ *   layout used for layers skipped from quantization).  A token at slot s
+ *   lives in block s / block_size at offset s % block_size.
+ * - Supported shapes: head_dim in {64, 128}; block_size == 16;
+ *   num_q_heads % num_kv_heads == 0 with num_q_heads / num_kv_heads <= 8.
+ *   All device pointers must be 16-byte aligned.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* kvq_stream_t;
+
+/* Cache element format (the kv_cache_dtype of the layer). */
+typedef enum {
+  KVQ_FMT_BF16 = 0, /* not quantized: bf16 cache ("auto" for a bf16 model)  */
+  KVQ_FMT_E4M3 = 1, /* FP8 E4M3 (OCP, max 448, no inf); "fp8" is an alias   */
+  KVQ_FMT_E5M2 = 2  /* FP8 E5M2 (OCP, max 57344)                            */
+} kvq_fmt;
+
+/* Scale granularity: per tensor (shape [1]) or per attention head
+ * (k/v scale shape [num_kv_heads], q scale shape [num_q_heads]). */
+typedef enum { KVQ_SCALE_PER_TENSOR = 0, KVQ_SCALE_PER_HEAD = 1 } kvq_gran;
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_NULL = -1,        /* a required pointer is NULL                         */
+  KVQ_ERR_SHAPE = -2,       /* inconsistent sizes, or a scale length off its shape */
+  KVQ_ERR_ALIGN = -3,       /* a pointer or stride is not 16-byte aligned         */
+  KVQ_ERR_UNSUPPORTED = -4, /* head_dim, block_size, group size, fmt or flag      */
+  KVQ_ERR_WORKSPACE = -5,   /* workspace smaller than kvq_decode_workspace_size   */
+  KVQ_ERR_CUDA = -6,        /* CUDA runtime error at launch                       */
+  KVQ_ERR_ARG = -7          /* other invalid argument (negative count, bad enum)  */
+} kvq_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define KVQ_DEV_BAD_SLOT 1u     /* slot >= num_blocks * block_size: token not written */
+#define KVQ_DEV_BAD_BLOCK 2u    /* block id outside [0, num_blocks): page masked out  */
+#define KVQ_DEV_BAD_SEQLEN 4u   /* seq_len < 0 or > max_blocks_per_seq * block_size   */
+#define KVQ_DEV_WAIT_TIMEOUT 8u /* a bounded pipeline wait ran out; output is invalid */
+#define KVQ_DEV_INTERNAL 16u    /* an internal index guard failed (bits 16..31 name it); */
+                                /* the access was skipped and the output is invalid      */
+
+/* Flags of kvq_decode_attn. */
+#define KVQ_Q_FP8 1u /* reserved: FP8-domain attention with Q quantized; not built */
+
+/*
+ * kvq_write -- quantize and scatter K and V into the paged cache.
+ *
+ * For every token t with slot = slot_mapping[t] >= 0, every KV head h and
+ * every d < head_dim:
+ *   k_cache[slot / bs][h][slot % bs][d] = cast_fp8(float(k[t][h][d]) / sK[h])
+ * and likewise for V with sV.  The quotient is the IEEE binary32 quotient
+ * (round to nearest even); cast_fp8 rounds to nearest even and saturates
+ * finite overflow and +-inf to +-max ("10.4 KV Cache quantization",
+ * section 10.4.5: cast_fp8(K / sK) is stored).  With fmt == KVQ_FMT_BF16 the
+ * bf16 bits are copied unchanged and the scales are ignored (may be NULL).
+ *
+ *   k, v            bf16 [num_tokens][num_kv_heads][head_dim], consecutive
+ *                   tokens `token_stride` elements apart (token_stride >=
+ *                   num_kv_heads * head_dim, a multiple of 8).
+ *   slot_mapping    int64 [num_tokens]; negative = padding, skipped.
+ *                   Slots must be distinct (duplicates race).
+ *   k_cache,v_cache the layer's caches, layout above, num_blocks blocks.
+ *   k_scale,v_scale fp32 device arrays of k_scale_len / v_scale_len floats:
+ *                   1 for KVQ_SCALE_PER_TENSOR, num_kv_heads for
+ *                   KVQ_SCALE_PER_HEAD; values finite and > 0.
+ *   dev_status      optional (NULL allowed); receives KVQ_DEV_BAD_SLOT.
+ * num_tokens == 0 is a no-op.
+ */
+KVQ_API int kvq_write(const void* k, const void* v, int64_t token_stride, const int64_t* slot_mapping,
+              int64_t num_tokens, int num_kv_heads, int head_dim, void* k_cache, void* v_cache,
+              int64_t num_blocks, int block_size, const float* k_scale, int k_scale_len,
+              const float* v_scale, int v_scale_len, int scale_granularity, int fmt,
+              uint32_t* dev_status, kvq_stream_t stream);
+
+/*
+ * kvq_decode_workspace_size -- bytes of device workspace kvq_decode_attn
+ * needs for these sizes.  num_sms <= 0 queries the current device (the value
+ * depends on the device's SM count).  Returns 0 for invalid sizes.
+ */
+KVQ_API size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int num_sms);
+
+/*
+ * kvq_decode_attn -- grouped-query decode attention over the paged cache,
+ * dequantization fused ("10.4 KV Cache quantization", section 10.4.2:
+ * P = softmax(Q K^T / sqrt(dh) + mask), O = P V^; section 10.4.5:
+ * K^ = cast_float(K_fp8) * sK).
+ *
+ * Sequence b attends to its tokens [lo_b, L_b), L_b = seq_lens[b] (the
+ * token being decoded included, so write it first on the same stream) and
+ * lo_b = L_b - sliding_window when 0 < sliding_window < L_b, else 0.  Query
+ * head h reads KV head h / (num_q_heads / num_kv_heads).  Token t of
+ * sequence b lives in block block_tables[b][t / block_size].
+ *
+ *   q               bf16 [num_seqs][num_q_heads][head_dim].
+ *   block_tables    int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                   ceil(L_b / block_size) are never read.
+ *   seq_lens        int32 [num_seqs]; 0 gives a zero output row.
+ *   q_scale         optional; accepted and shape-checked (q_scale_len 1 or
+ *                   num_q_heads) but not applied: the stored-FP8 path keeps
+ *                   Q in bf16 (see KVQ_Q_FP8).
+ *   k_scale,v_scale as for kvq_write (ignored and may be NULL for BF16).
+ *   sliding_window  0 = none.
+ *   flags           0 (KVQ_Q_FP8 returns KVQ_ERR_UNSUPPORTED).
+ *   workspace       device scratch of at least
+ *                   kvq_decode_workspace_size(num_seqs, ...) bytes, 256-byte
+ *                   aligned.  Contents need no initialisation and are
+ *                   overwritten; one workspace must not be shared by calls
+ *                   that may run concurrently.
+ *   out             bf16 [num_seqs][num_q_heads][head_dim] (fp32
+ *                   accumulation, round to nearest even).
+ *   dev_status      optional; KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN,
+ *                   KVQ_DEV_WAIT_TIMEOUT.
+ * Limits: num_seqs <= 4096; num_seqs * max_blocks_per_seq * num_kv_heads
+ * < 2^31.
+ */
+KVQ_API int kvq_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                    int64_t num_blocks, int block_size, const float* q_scale, int q_scale_len,
+                    const float* k_scale, int k_scale_len, const float* v_scale, int v_scale_len,
+                    int scale_granularity, int fmt, int sliding_window, unsigned flags,
+                    void* workspace, size_t workspace_bytes, void* out, uint32_t* dev_status,
+                    kvq_stream_t stream);
+
+/*
+ * kvq_dequant_cache -- the unfused path's separate dequant kernel
+ * ("10.4 KV Cache quantization", section 10.4.2: read the quantized KV,
+ * dequantize in an independent kernel, write a 16-bit KV back to HBM).
+ * dst_bf16[i] = bf16(fp32(cast_float(src[i]) * s_h)) over the whole cache
+ * [num_blocks][num_kv_heads][block_size][head_dim]; the product is rounded to
+ * binary32 (exact whenever s_h is a power of two), then to bf16 (nearest
+ * even).  kvq_decode_attn with fmt KVQ_FMT_BF16 then reads the result.
+ * fmt must be E4M3 or E5M2; scale as for kvq_write.
+ */
+KVQ_API int kvq_dequant_cache(const void* src, void* dst_bf16, int64_t num_blocks, int num_kv_heads,
+                      int block_size, int head_dim, const float* scale, int scale_len,
+                      int scale_granularity, int fmt, kvq_stream_t stream);
+
+/*
+ * Host helpers (no device work).
+ *
+ * kvq_parse_dtype: kv_cache_dtype string -> kvq_fmt ("vLLM FP8 quantized KV
+ * cache guide", choosing kv_cache_dtype): "fp8" and "fp8_e4m3" -> E4M3,
+ * "fp8_e5m2" -> E5M2, "auto" / "bfloat16" / "bf16" -> BF16 (this library's
+ * model dtype).  Anything else -> KVQ_ERR_UNSUPPORTED; NULL -> KVQ_ERR_NULL.
+ *
+ * kvq_layer_fmt: the skip-layer rule of the same guide ("per-layer
+ * exemption of quantization-sensitive layers"): a layer keeps the model
+ * dtype (returns KVQ_FMT_BF16) when it is a sliding-window layer
+ * (is_sliding != 0) and the skip list holds "sliding_window", or when the
+ * decimal string of layer_idx is in the skip list; otherwise returns fmt.
+ * skip is a host array of n_skip C strings.  Errors: KVQ_ERR_NULL,
+ * KVQ_ERR_ARG (bad fmt / negative index or count).
+ *
+ * kvq_status_string: static text for a kvq_status.
+ * kvq_version: 10000 * major + 100 * minor + patch.
+ */
+KVQ_API int kvq_parse_dtype(const char* s);
+KVQ_API int kvq_layer_fmt(int fmt, int layer_idx, int is_sliding, const char* const* skip, int n_skip);
+KVQ_API const char* kvq_status_string(int status);
+KVQ_API int kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

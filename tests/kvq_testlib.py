@@ -1,0 +1,117 @@
+"""Helpers shared by the GPU parity tests: move the seeded workload inputs to
+the device, run the library through its binding, and compare with the CPU
+oracle on the same inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+# Attention tolerance, elementwise: |gpu - ref| <= ABS + REL * |ref|, with ref
+# the float64 oracle over the same dequantized cache and gpu the bf16 output.
+ABS_TOL, REL_TOL = 2e-3, 1e-2
+
+
+def to_dev(a, dev="cuda"):
+    """numpy -> device tensor; uint16 arrays hold bf16 bit patterns."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+def to_np(t):
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def bf16_out_to_f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_attention(got, ref, what=""):
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - ref)
+    bound = ABS_TOL + REL_TOL * np.abs(ref)
+    bad = ~(err <= bound)
+    assert not bad.any(), (
+        f"{what}: {int(bad.sum())} of {err.size} elements out of tolerance; "
+        f"max abs err {np.nanmax(err):.3e}, worst ratio {np.nanmax(err / bound):.2f}")
+    return float(err.max()) if err.size else 0.0
+
+
+class DeviceLayer:
+    """One workload layer resident on the GPU, with its paged caches."""
+
+    def __init__(self, lay: workloads.Layer, dev="cuda", fill=0):
+        import fp8_quantized_paged_gb300 as kvq
+        self.kvq = kvq
+        self.lay = lay
+        st = lay.st
+        self.dev = dev
+        self.q = to_dev(lay.q, dev)
+        self.k = to_dev(lay.k, dev)
+        self.v = to_dev(lay.v, dev)
+        self.slots = to_dev(st.slot_mapping, dev)
+        self.bt = to_dev(st.block_tables, dev)
+        self.sl = to_dev(st.seq_lens, dev)
+        self.qs = to_dev(lay.q_scale, dev)
+        self.ks = to_dev(lay.k_scale, dev)
+        self.vs = to_dev(lay.v_scale, dev)
+        self.kc = kvq.new_cache(st.num_blocks, lay.Hkv, lay.dh, lay.fmt, dev)
+        self.vc = kvq.new_cache(st.num_blocks, lay.Hkv, lay.dh, lay.fmt, dev)
+        self.kc.view(torch.uint8).fill_(fill)
+        self.vc.view(torch.uint8).fill_(fill)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = kvq.new_workspace(lay.B, lay.Hq, lay.Hkv, lay.dh, dev)
+        self.ws.fill_(0xFF)  # NaN bytes: a read of a slot nobody wrote shows up
+        self.out = torch.empty((lay.B, lay.Hq, lay.dh), dtype=torch.bfloat16, device=dev)
+
+    def write(self, token_idx=None):
+        lay = self.lay
+        if token_idx is None:
+            k, v, s = self.k, self.v, self.slots
+        else:
+            idx = torch.as_tensor(np.asarray(token_idx, np.int64), device=self.dev)
+            k, v, s = self.k[idx], self.v[idx], self.slots[idx]
+        self.kvq.kvq_write(k, v, s, self.kc, self.vc, self.ks, self.vs, lay.gran, lay.fmt,
+                           dev_status=self.status)
+
+    def decode(self, window=None, seq_lens=None, block_tables=None):
+        lay = self.lay
+        self.kvq.kvq_decode_attn(self.q, self.kc, self.vc,
+                                 self.bt if block_tables is None else block_tables,
+                                 self.sl if seq_lens is None else seq_lens, self.qs, self.ks,
+                                 self.vs, lay.gran, lay.fmt,
+                                 lay.window if window is None else window, self.ws, self.out,
+                                 dev_status=self.status)
+        return self.out
+
+    def status_word(self):
+        torch.cuda.synchronize()
+        return int(self.status.item())
+
+
+def oracle_caches(lay: workloads.Layer, token_idx=None, fill=0):
+    st = lay.st
+    K = oracle.new_cache(st.num_blocks, lay.Hkv, lay.bs, lay.dh, lay.fmt, fill)
+    V = oracle.new_cache(st.num_blocks, lay.Hkv, lay.bs, lay.dh, lay.fmt, fill)
+    if token_idx is None:
+        k, v, s = lay.k, lay.v, st.slot_mapping
+    else:
+        k, v, s = lay.k[token_idx], lay.v[token_idx], st.slot_mapping[token_idx]
+    bad = oracle.write(k, v, s, K, V, lay.k_scale, lay.v_scale, lay.gran, lay.fmt)
+    assert bad == 0
+    return K, V
+
+
+def oracle_decode(lay, K, V, pairs=None, window=None, seq_lens=None, block_tables=None):
+    st = lay.st
+    return oracle.decode_attn(lay.q, K, V, st.block_tables if block_tables is None else block_tables,
+                              st.seq_lens if seq_lens is None else seq_lens, lay.k_scale,
+                              lay.v_scale, lay.gran, lay.fmt,
+                              lay.window if window is None else window, pairs=pairs)

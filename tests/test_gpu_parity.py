@@ -1,0 +1,321 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Cache bytes must be bit-exact; attention outputs must satisfy
+|gpu - ref| <= 2e-3 + 1e-2 |ref| elementwise against the float64 oracle over
+the same dequantized cache.  Inputs are the seeded workloads of
+``workloads`` (the tiny case, the Llama-3.1-8B-shaped decode layer, per-head
+scales in E4M3 and E5M2, one long-context layer, a FP8 and a bf16 layer of the
+mixed skip-layer batch) plus hand-made edge cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from kvq_testlib import (DeviceLayer, bf16_out_to_f64, check_attention, oracle_caches,
+                         oracle_decode, to_dev, to_np)
+
+pytestmark = pytest.mark.gpu
+
+CASES = [  # (config, layer, fmt for config 3)
+    (1, 0, workloads.E4M3),
+    (2, 0, workloads.E4M3),
+    (3, 0, workloads.E4M3),
+    (3, 0, workloads.E5M2),
+    (4, 0, workloads.E4M3),
+    (5, 2, workloads.E4M3),
+    (5, 3, workloads.E4M3),  # bf16 + sliding window 4096
+]
+IDS = ["tiny", "llama8b_layer", "perhead_e4m3", "perhead_e5m2", "longctx_layer0",
+       "mixed_fp8_layer2", "mixed_bf16_window_layer3"]
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import fp8_quantized_paged_gb300 as m
+    return m
+
+
+def _pairs_for(lay):
+    n = lay.B * lay.Hq
+    if n * int(lay.st.seq_lens.max()) <= 32 * 1024 * 1024:
+        return None  # every (sequence, head) pair
+    return workloads.sample_pairs(lay.B, lay.Hq, 192, seed=lay.cfg * 100 + lay.layer)
+
+
+@pytest.mark.parametrize("cfg,layer,fmt3", CASES, ids=IDS)
+def test_write_and_decode(kvq, cfg, layer, fmt3):
+    lay = workloads.make_layer(cfg, layer, fmt3)
+    d = DeviceLayer(lay)
+    if cfg == 2:
+        new = np.flatnonzero(lay.new_token_mask)
+        old = np.flatnonzero(~lay.new_token_mask)
+        d.write(old)   # prefill
+        d.write(new)   # the decode step's own tokens
+    else:
+        d.write()
+    out = d.decode()
+    assert d.status_word() == 0
+    K, V = oracle_caches(lay)
+    np.testing.assert_array_equal(to_np(d.kc), K)
+    np.testing.assert_array_equal(to_np(d.vc), V)
+    pairs = _pairs_for(lay)
+    ref = oracle_decode(lay, K, V, pairs=pairs)
+    got = bf16_out_to_f64(out)
+    if pairs is not None:
+        got = got[pairs[:, 0], pairs[:, 1]]
+    check_attention(got, ref, f"config {cfg} layer {layer}")
+    # deterministic: a second call gives the same bits
+    first = to_np(out).copy()
+    d.decode()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(d.out), first)
+
+
+# ---------------------------------------------------------------- write edge cases
+
+def _custom_layer(lens, Hq=8, Hkv=2, dh=64, fmt=workloads.E4M3, gran=workloads.PER_HEAD,
+                  seed=0, std=1.0, window=0, spare=2):
+    r = np.random.default_rng(seed)
+    st = workloads._structure(np.array(lens), r, extra_blocks=spare)
+    N = len(st.slot_mapping)
+    f = lambda *s: workloads.f32_to_bf16_bits((r.standard_normal(s) * std).astype(np.float32))  # noqa
+    q, k, v = f(len(lens), Hq, dh), f(N, Hkv, dh), f(N, Hkv, dh)
+    nsc = Hkv if gran == workloads.PER_HEAD else 1
+    ks = (r.uniform(0.5, 2.0, nsc) * std / 100).astype(np.float32)
+    vs = (r.uniform(0.5, 2.0, nsc) * std / 100).astype(np.float32)
+    if fmt == workloads.BF16:
+        ks = vs = np.ones(nsc, np.float32)
+    qs = np.ones(Hq if gran == workloads.PER_HEAD else 1, np.float32)
+    return workloads.Layer(0, 0, len(lens), Hq, Hkv, dh, 16, fmt, gran, window, st, q, k, v, qs,
+                           ks, vs)
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2])
+def test_write_special_values(kvq, fmt):
+    """Signed zeros, subnormal FP8 results, midpoints, saturation and +-inf."""
+    lay = _custom_layer([40, 9], fmt=fmt, gran=workloads.PER_TENSOR, seed=3)
+    s = np.float32(0.01)
+    lay.k_scale[:] = s
+    lay.v_scale[:] = s
+    mx = 448.0 if fmt == workloads.E4M3 else 57344.0
+    specials = np.array([0.0, -0.0, 1e-30, -1e-30, 2.0 ** -9 * 0.01, 2.0 ** -10 * 0.01,
+                         2.0 ** -16 * 0.01, mx * 0.01, mx * 0.0105, mx * 0.02, 1e30, -1e30,
+                         np.inf, -np.inf, 3.0, -2.75], np.float32)
+    bits = workloads.f32_to_bf16_bits(specials)
+    flat = lay.k.reshape(-1)
+    flat[: len(bits) * 40: 1] = np.resize(bits, len(bits) * 40)
+    lay.v.reshape(-1)[::7] = bits[np.arange(lay.v.size // 7 + (lay.v.size % 7 > 0)) % len(bits)]
+    d = DeviceLayer(lay)
+    d.write()
+    assert d.status_word() == 0
+    K, V = oracle_caches(lay)
+    np.testing.assert_array_equal(to_np(d.kc), K)
+    np.testing.assert_array_equal(to_np(d.vc), V)
+
+
+def test_write_nan_gives_a_nan_code(kvq):
+    lay = _custom_layer([16], gran=workloads.PER_TENSOR, seed=4)
+    lay.k[0, 0, :5] = workloads.f32_to_bf16_bits(np.array([np.nan] * 5, np.float32))
+    lay.k[0, 0, 5] = 0xFFC0  # negative quiet NaN
+    d = DeviceLayer(lay)
+    d.write()
+    codes = to_np(d.kc)[lay.st.block_tables[0, 0], 0, 0, :6]
+    assert np.all(np.isnan(oracle.decode(workloads.E4M3, codes)))
+
+
+def test_write_padding_bad_slot_and_fill(kvq):
+    lay = _custom_layer([30, 20], seed=5)
+    slots = lay.st.slot_mapping.copy()
+    slots[3] = -1                                   # padding token: skipped
+    slots[7] = lay.st.num_blocks * 16 + 5           # past the cache: flagged
+    lay.st.slot_mapping = slots
+    d = DeviceLayer(lay, fill=0x33)
+    d.write()
+    assert d.status_word() == kvq.KVQ_DEV_BAD_SLOT
+    st = lay.st
+    K = oracle.new_cache(st.num_blocks, lay.Hkv, 16, lay.dh, lay.fmt, 0x33)
+    V = oracle.new_cache(st.num_blocks, lay.Hkv, 16, lay.dh, lay.fmt, 0x33)
+    assert oracle.write(lay.k, lay.v, slots, K, V, lay.k_scale, lay.v_scale, lay.gran,
+                        lay.fmt) == 1
+    np.testing.assert_array_equal(to_np(d.kc), K)
+    np.testing.assert_array_equal(to_np(d.vc), V)
+
+
+def test_write_token_stride(kvq):
+    """K and V read as slices of a fused per-token [q | k | v] row."""
+    lay = _custom_layer([33, 17], Hq=8, Hkv=2, dh=128, seed=6)
+    N = lay.k.shape[0]
+    fused = np.zeros((N, (8 + 2 + 2) * 128), np.uint16)
+    fused[:, 8 * 128:10 * 128] = lay.k.reshape(N, -1)
+    fused[:, 10 * 128:] = lay.v.reshape(N, -1)
+    d = DeviceLayer(lay)
+    fz = to_dev(fused).view(N, 12, 128)
+    kvq.kvq_write(fz[:, 8:10], fz[:, 10:12], d.slots, d.kc, d.vc, d.ks, d.vs, lay.gran,
+                  lay.fmt, dev_status=d.status)
+    K, V = oracle_caches(lay)
+    np.testing.assert_array_equal(to_np(d.kc), K)
+    np.testing.assert_array_equal(to_np(d.vc), V)
+
+
+# ---------------------------------------------------------------- decode edge cases
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2, workloads.BF16])
+@pytest.mark.parametrize("dh", [64, 128])
+def test_decode_ragged_lengths(kvq, fmt, dh):
+    lens = [1, 15, 16, 17, 33, 0, 250, 5, 64, 1000]
+    lay = _custom_layer(lens, Hq=16, Hkv=4, dh=dh, fmt=fmt, seed=7 + dh)
+    d = DeviceLayer(lay)
+    d.write()
+    out = d.decode()
+    assert d.status_word() == 0
+    K, V = oracle_caches(lay)
+    ref = oracle_decode(lay, K, V)
+    got = bf16_out_to_f64(out)
+    check_attention(got, ref, "ragged")
+    assert np.all(got[5] == 0)  # empty sequence -> zero row
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_decode_group_sizes(kvq, G):
+    lay = _custom_layer([70, 300, 16], Hq=2 * G, Hkv=2, dh=128, seed=20 + G)
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    check_attention(bf16_out_to_f64(d.decode()), oracle_decode(lay, K, V), f"G={G}")
+
+
+@pytest.mark.parametrize("window", [1, 7, 16, 100, 512, 5000])
+def test_decode_sliding_window(kvq, window):
+    lay = _custom_layer([600, 16, 1, 129], Hq=8, Hkv=2, dh=128, fmt=workloads.BF16, seed=30,
+                        window=window)
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    check_attention(bf16_out_to_f64(d.decode()), oracle_decode(lay, K, V), f"window={window}")
+    # FP8 layers accept a window too
+    lay8 = _custom_layer([600, 40], Hq=8, Hkv=2, dh=128, seed=31, window=window)
+    d8 = DeviceLayer(lay8)
+    d8.write()
+    K8, V8 = oracle_caches(lay8)
+    check_attention(bf16_out_to_f64(d8.decode()), oracle_decode(lay8, K8, V8), "fp8 window")
+
+
+def test_decode_uniform_v_and_one_token(kvq):
+    lay = _custom_layer([300, 1, 45], Hq=8, Hkv=2, dh=128, seed=40)
+    lay.v[:] = lay.v[0]  # every token carries the same V row
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    vhat = oracle.decode(lay.fmt, V[lay.st.block_tables[0, 0], :, 0, :]) * lay.v_scale[:, None]
+    got = bf16_out_to_f64(d.decode())
+    for h in range(8):
+        check_attention(got[:, h, :], np.broadcast_to(vhat[h // 4], (3, 128)), "uniform V")
+
+
+def test_decode_large_logits(kvq):
+    """Logit spread far beyond the lazy-rescale threshold (K std 30)."""
+    lay = _custom_layer([2000, 700], Hq=8, Hkv=2, dh=128, seed=41, std=30.0)
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    check_attention(bf16_out_to_f64(d.decode()), oracle_decode(lay, K, V), "large logits")
+
+
+def test_decode_bad_block_and_seq_len(kvq):
+    lay = _custom_layer([64, 40, 20], Hq=8, Hkv=2, dh=128, seed=42)
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    ref = oracle_decode(lay, K, V)
+    bt = lay.st.block_tables.copy()
+    bt[1, 1] = lay.st.num_blocks + 3  # sequence 1, tokens 16..31
+    sl = lay.st.seq_lens.copy()
+    sl[2] = bt.shape[1] * 16 + 1      # longer than its block table
+    out = bf16_out_to_f64(d.decode(block_tables=to_dev(bt), seq_lens=to_dev(sl)))
+    assert d.status_word() == kvq.KVQ_DEV_BAD_BLOCK | kvq.KVQ_DEV_BAD_SEQLEN
+    check_attention(out[0], ref[0], "untouched sequence")
+    assert np.all(out[2] == 0)
+    # sequence 1 equals attention over its tokens outside the bad page
+    keep = [t for t in range(40) if not 16 <= t < 32]
+    sub = workloads.Layer(0, 0, 1, 8, 2, 128, 16, lay.fmt, lay.gran, 0,
+                          workloads._structure(np.array([len(keep)]), np.random.default_rng(0)),
+                          lay.q[1:2], None, None, lay.q_scale, lay.k_scale, lay.v_scale)
+    pos = np.array(keep)
+    blk = lay.st.block_tables[1, pos // 16] * 16 + pos % 16
+    K2 = oracle.new_cache(sub.st.num_blocks, 2, 16, 128, lay.fmt)
+    V2 = oracle.new_cache(sub.st.num_blocks, 2, 16, 128, lay.fmt)
+    slot2 = sub.st.slot_mapping
+    for i, s_old in enumerate(blk):
+        b_new, o_new = divmod(int(slot2[i]), 16)
+        b_old, o_old = divmod(int(s_old), 16)
+        K2[b_new, :, o_new] = K[b_old, :, o_old]
+        V2[b_new, :, o_new] = V[b_old, :, o_old]
+    ref1 = oracle.decode_attn(sub.q, K2, V2, sub.st.block_tables, sub.st.seq_lens, lay.k_scale,
+                              lay.v_scale, lay.gran, lay.fmt)
+    check_attention(out[1], ref1[0], "bad page masked")
+
+
+def test_decode_single_piece_segments(kvq):
+    """Tiny grids where one CTA holds a whole (sequence, head) segment and the
+    decode kernel writes the output itself (no reduce)."""
+    for lens in ([16], [16, 16], [5], [3, 16, 9]):
+        lay = _custom_layer(lens, Hq=8, Hkv=2, dh=128, seed=50 + len(lens))
+        d = DeviceLayer(lay)
+        d.write()
+        K, V = oracle_caches(lay)
+        check_attention(bf16_out_to_f64(d.decode()), oracle_decode(lay, K, V), f"lens={lens}")
+
+
+def test_workspace_too_small(kvq):
+    lay = _custom_layer([20], seed=60)
+    d = DeviceLayer(lay)
+    d.write()
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_decode_attn(d.q, d.kc, d.vc, d.bt, d.sl, None, d.ks, d.vs, lay.gran, lay.fmt, 0,
+                            small, d.out)
+    assert e.value.status == kvq.KVQ_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------- unfused ablation
+
+@pytest.mark.parametrize("cfg,fmt3", [(2, workloads.E4M3), (3, workloads.E5M2)])
+def test_dequant_then_bf16_decode(kvq, cfg, fmt3):
+    lay = workloads.make_layer(cfg, 0, fmt3)
+    d = DeviceLayer(lay)
+    d.write()
+    kb = torch.empty(d.kc.shape, dtype=torch.bfloat16, device="cuda")
+    vb = torch.empty(d.vc.shape, dtype=torch.bfloat16, device="cuda")
+    kvq.kvq_dequant_cache(d.kc, kb, d.ks, lay.gran, lay.fmt)
+    kvq.kvq_dequant_cache(d.vc, vb, d.vs, lay.gran, lay.fmt)
+    K, V = oracle_caches(lay)
+    Kb = oracle.dequant(K, lay.k_scale, lay.gran, lay.fmt)
+    Vb = oracle.dequant(V, lay.v_scale, lay.gran, lay.fmt)
+    np.testing.assert_array_equal(to_np(kb), Kb)
+    np.testing.assert_array_equal(to_np(vb), Vb)
+    kvq.kvq_decode_attn(d.q, kb, vb, d.bt, d.sl, None, None, None, 0, kvq.KVQ_FMT_BF16, 0, d.ws,
+                        d.out)
+    pairs = workloads.sample_pairs(lay.B, lay.Hq, 128, seed=cfg)
+    ref = oracle.decode_attn(lay.q, Kb, Vb, lay.st.block_tables, lay.st.seq_lens, None, None, 0,
+                             oracle.BF16, pairs=pairs)
+    got = bf16_out_to_f64(d.out)[pairs[:, 0], pairs[:, 1]]
+    check_attention(got, ref, "unfused bf16 path")
+
+
+@pytest.mark.parametrize("lens", [[70, 33, 1], [500, 300], [16] * 7, [1] * 40])
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.BF16])
+def test_decode_fewer_units_than_ctas(kvq, lens, fmt):
+    """Batches with fewer KV pages than the persistent grid has CTAs: segments
+    split over consecutive CTAs and the reduce must read only written slots
+    (the workspace starts as NaN bytes)."""
+    lay = _custom_layer(lens, Hq=8, Hkv=2, dh=128, fmt=fmt, seed=70 + len(lens))
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    for _ in range(3):
+        got = bf16_out_to_f64(d.decode())
+        assert d.status_word() == 0
+        check_attention(got, oracle_decode(lay, K, V), f"lens={lens}")
+        d.ws.fill_(0xFF)
