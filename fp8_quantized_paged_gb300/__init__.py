@@ -23,6 +23,7 @@ KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA, KVQ_ERR_ARG = -4, -5, -6, 
 KVQ_DEV_BAD_SLOT, KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
 KVQ_DEV_INTERNAL = 16
 KVQ_Q_FP8 = 1
+KVQ_STATIC_SCRATCH_BYTES = 16 << 20
 BLOCK_SIZE = 16
 
 # exported symbol -> (restype, argtypes)
@@ -34,6 +35,9 @@ SIGNATURES = {
     "kvq_decode_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
                                _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _u32, _vp, _sz,
                                _vp, _vp, _vp]),
+    "kvq_decode_attn_static": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i64,
+                                      _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                      _u32, _vp, _vp, _vp]),
     "kvq_dequant_cache": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
     "kvq_parse_dtype": (_i32, [ctypes.c_char_p]),
     "kvq_layer_fmt": (_i32, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_char_p), _i32]),
@@ -130,6 +134,24 @@ def kvq_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, q_scale, k_scal
                               sliding_window, flags, _ptr(workspace), workspace.numel(), _ptr(out),
                               _ptr(dev_status), _stream(stream))
     _check(st, "kvq_decode_attn")
+
+
+def kvq_decode_attn_static(q, k_cache, v_cache, block_tables, seq_lens, q_scale, k_scale,
+                           v_scale, scale_granularity, fmt, sliding_window, out, dev_status=None,
+                           stream=None, flags=0) -> None:
+    """kvq_decode_attn with the library's own static scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    B, hq, dh = q.shape
+    nb, hkv, bs, dh2 = k_cache.shape
+    if dh2 != dh or tuple(out.shape) != (B, hq, dh) or block_tables.shape[0] != B:
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_decode_attn_static")
+    st = _lib.kvq_decode_attn_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                     block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, dh, nb,
+                                     bs, _ptr(q_scale), _len(q_scale), _ptr(k_scale),
+                                     _len(k_scale), _ptr(v_scale), _len(v_scale),
+                                     scale_granularity, fmt, sliding_window, flags, _ptr(out),
+                                     _ptr(dev_status), _stream(stream))
+    _check(st, "kvq_decode_attn_static")
 
 
 def kvq_dequant_cache(src, dst_bf16, scale, scale_granularity, fmt, stream=None) -> None:

@@ -180,6 +180,43 @@ KVQ_API int kvq_decode_attn(const void* q, const void* k_cache, const void* v_ca
                     kvq_stream_t stream);
 
 /*
+ * kvq_decode_attn_static -- kvq_decode_attn without a caller-provided
+ * workspace.  The pages this library is written from have no counterpart of
+ * this entry point; it exists for callers that cannot allocate device
+ * memory: a plugin handed only input and output pointers by its host
+ * program, with no allocator to call, or a serving loop whose device-memory
+ * plan is fixed at start-up and which may not call cudaMalloc (it can block
+ * until the device is idle) on the decode path.
+ *
+ * Same arguments, semantics and errors as kvq_decode_attn, minus workspace
+ * and workspace_bytes; the caller still passes every input and the output.
+ * The scratch is one array of KVQ_STATIC_SCRATCH_BYTES bytes compiled into
+ * the library's device image: every GPU on which the library's device code
+ * is loaded holds it until the process exits.  Sizes whose workspace
+ * (kvq_decode_workspace_size) exceeds it return KVQ_ERR_WORKSPACE before
+ * anything is enqueued.  Nothing is allocated: no cudaMalloc, cudaFree or
+ * allocating library routine is called.
+ *
+ * The first call on a device, made with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and keeps it; make that
+ * first call before any stream capture.  All calls on a device share the
+ * one array, which keeps the last call's contents (the kernels overwrite
+ * whatever they read, so nothing needs clearing).  Calls that may overlap
+ * on the GPU (different streams, or different host threads) race on it:
+ * serialize them, or give each its own workspace through kvq_decode_attn.
+ */
+#define KVQ_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+KVQ_API int kvq_decode_attn_static(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int64_t num_blocks,
+                                   int block_size, const float* q_scale, int q_scale_len,
+                                   const float* k_scale, int k_scale_len, const float* v_scale,
+                                   int v_scale_len, int scale_granularity, int fmt,
+                                   int sliding_window, unsigned flags, void* out,
+                                   uint32_t* dev_status, kvq_stream_t stream);
+
+/*
  * kvq_dequant_cache -- the unfused path's separate dequant kernel
  * ("10.4 KV Cache quantization", section 10.4.2: read the quantized KV,
  * dequantize in an independent kernel, write a 16-bit KV back to HBM).
