@@ -153,7 +153,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -229,29 +229,42 @@ def run_gpu(args, rank, world, local_rank):
     E4, PH = kvq.KVQ_FMT_E4M3, kvq.KVQ_SCALE_PER_HEAD
     launches_per_step = LAYERS * 3  # write kernel; decode + reduce kernels
 
-    ev_w = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(LAYERS)]
-    ev_d = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(LAYERS)]
-    acc = {"write_ms": 0.0, "decode_ms": 0.0}
-
-    def step(timed):
-        for i, x in enumerate(L):
-            if timed:
-                ev_w[i][0].record(stream)
+    def writes():
+        for x in L:
             kvq.kvq_write(x["k"], x["v"], slots, x["kc"], x["vc"], x["ks"], x["vs"], PH, E4,
                           dev_status=status)
-            if timed:
-                ev_w[i][1].record(stream)
-        for i, x in enumerate(L):
-            if timed:
-                ev_d[i][0].record(stream)
+
+    def decodes():
+        for x in L:
             kvq.kvq_decode_attn(x["q"], x["kc"], x["vc"], bt, sl, None, x["ks"], x["vs"], PH, E4,
                                 0, ws, x["out"], dev_status=status)
-            if timed:
-                ev_d[i][1].record(stream)
-        if timed:
-            torch.cuda.synchronize()
-            acc["write_ms"] += sum(a.elapsed_time(b) for a, b in ev_w)
-            acc["decode_ms"] += sum(a.elapsed_time(b) for a, b in ev_d)
+
+    # eager warm-up (first calls configure the kernels), then one CUDA graph
+    # for the 32 writes and one for the 32 decodes: the step replays both.
+    for _ in range(max(args.warmup, 3)):
+        writes()
+        decodes()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    g_write, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_write):
+        writes()
+    with torch.cuda.graph(g_decode):
+        decodes()
+    stream = torch.cuda.current_stream()
+
+    def step(_timed=False):
+        g_write.replay()
+        g_decode.replay()
+
+    def timed_replays(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
 
     def barrier():
         if world > 1:
@@ -262,28 +275,21 @@ def run_gpu(args, rank, world, local_rank):
         return max_over_ranks(x, world, dev)
 
     for _ in range(max(args.warmup, 3)):
-        step(False)
+        step()
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
-    # ---- device-resident timed region (per-call events inside, whole-step events around)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- device-resident timed region: whole steps, then each graph alone
     barrier()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        t0.record(stream)
-        for _ in range(args.steps):
-            step(False)
-        t1.record(stream)
-        torch.cuda.synchronize()
-        total_ms = t0.elapsed_time(t1)
-        # per-call split, measured in separate timed passes (events add gaps)
-        for _ in range(args.steps):
-            step(True)
+        total_ms = timed_replays(step, args.steps)
+        write_total = timed_replays(g_write.replay, args.steps)
+        decode_total = timed_replays(g_decode.replay, args.steps)
     barrier()
-    total_ms = rank_max(total_ms)
-    ms_step = total_ms / args.steps
-    write_ms = rank_max(acc["write_ms"] / args.steps)
-    decode_ms = rank_max(acc["decode_ms"] / args.steps)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    ms_step = rank_max(total_ms) / args.steps
+    write_ms = rank_max(write_total) / args.steps
+    decode_ms = rank_max(decode_total) / args.steps
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barrier,
@@ -328,6 +334,8 @@ def run_gpu(args, rank, world, local_rank):
         "roofline_decode": roof("kvq_decode_attn", d_ach, decode_bytes(SEQ)),
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
+        "timing": "CUDA graphs (32 writes, 32 decodes) replayed; events on the replay stream; "
+                  "per-kernel figures from replaying each graph alone",
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -458,6 +466,42 @@ def run_reference(args):
 # ---------------------------------------------------------------- main
 
 
+def run_ncu_case(case: str):
+    """A few launches of one kernel on a case larger than L2, for ncu captures:
+    'decode' and 'write' run one FP8 layer of the mixed skip-layer batch
+    (128 sequences, about 0.9 GB of FP8 cache), 'decode_long' one layer of the
+    long-context workload (64 MiB of cache)."""
+    import torch
+
+    import fp8_quantized_paged_gb300 as kvq
+    cfg, layer = (4, 0) if case == "decode_long" else (5, 2)
+    lay = workloads.make_layer(cfg, layer)
+    st = lay.st
+    dev = torch.device("cuda:0")
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    k, v, q = up(lay.k), up(lay.v), up(lay.q)
+    slots, bt, sl = up(st.slot_mapping), up(st.block_tables), up(st.seq_lens)
+    ks, vs = up(lay.k_scale), up(lay.v_scale)
+    kc = kvq.new_cache(st.num_blocks, lay.Hkv, lay.dh, lay.fmt, dev)
+    vc = kvq.new_cache(st.num_blocks, lay.Hkv, lay.dh, lay.fmt, dev)
+    ws = kvq.new_workspace(lay.B, lay.Hq, lay.Hkv, lay.dh, dev)
+    out = torch.empty((lay.B, lay.Hq, lay.dh), dtype=torch.bfloat16, device=dev)
+    n_write = 3 if case == "write" else 1
+    for _ in range(n_write):
+        kvq.kvq_write(k, v, slots, kc, vc, ks, vs, lay.gran, lay.fmt)
+    for _ in range(3 if case.startswith("decode") else 0):
+        kvq.kvq_decode_attn(q, kc, vc, bt, sl, None, ks, vs, lay.gran, lay.fmt, lay.window, ws, out)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_case": case, "workload": cfg, "layer": layer,
+                      "kv_tokens": int(st.seq_lens.sum()), "decode_bytes": int(st.seq_lens.sum()) * 2048}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,7 +511,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", choices=["decode", "write", "decode_long"], default=None,
+                    help="run a few launches of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -68,6 +68,19 @@ KVQ_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test for completion of the phase of the given parity.
+KVQ_DEVI bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase of the given parity; false when it ran out.
 KVQ_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kMaxPolls; ++i)
@@ -129,6 +142,21 @@ KVQ_DEVI uint32_t fp8x2_to_f16x2(uint16_t two) {
   else
     asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(two));
   return r;
+}
+
+// Four FP8 codes of one word to two f16x2 (bytes 0,1 -> lo; bytes 2,3 -> hi).
+template <int FMT>
+KVQ_DEVI void fp8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if (FMT == KVQ_FMT_E4M3)
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  else
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, a;\n\tcvt.rn.f16x2.e5m2x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // Two binary32 values to two FP8 codes, round to nearest even, saturating

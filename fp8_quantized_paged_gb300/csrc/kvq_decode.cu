@@ -41,12 +41,24 @@
 
 namespace kvq {
 
+#ifndef KVQ_CONSUMER_WARPS
+#define KVQ_CONSUMER_WARPS 4
+#endif
+#ifndef KVQ_CTAS_PER_SM
+#define KVQ_CTAS_PER_SM 2
+#endif
+#ifndef KVQ_RING_KB
+#define KVQ_RING_KB 80
+#endif
+
 constexpr int kBS = 16;  // tokens per page (block_size)
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = KVQ_CONSUMER_WARPS;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kCtasPerSM = 2;
+constexpr int kCtasPerSM = KVQ_CTAS_PER_SM;
+constexpr int kRingBytes = KVQ_RING_KB * 1024;
 constexpr int kMaxSeqs = 4096;
 constexpr int kMaxGroup = 8;
+constexpr int kMaxKvHeads = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazily rescale O
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
@@ -61,22 +73,38 @@ struct Cfg {
   // used by one warp only, in order, and a parity wait can never alias a
   // phase two behind.
   static constexpr int kStages =
-      kConsumerWarps * ((48 * 1024) / (kConsumerWarps * kSlot) > 0 ? (48 * 1024) / (kConsumerWarps * kSlot) : 1);
+      kConsumerWarps * (kRingBytes / (kConsumerWarps * kSlot) > 0 ? kRingBytes / (kConsumerWarps * kSlot) : 1);
   static constexpr uint32_t kSwz = (kRow >= 128) ? 7u : 3u;  // 128B or 64B swizzle
+  // Pages a consumer warp works on at once.  Two (independent MMA chains)
+  // measured slower: each warp then holds two ring slots before it starts.
+  static constexpr int kPagesPerStep = 1;
 };
 
-// Dynamic shared memory of the decode kernel (offsets from a 1024-aligned base).
+// Dynamic shared memory of the decode kernel (offsets from a 1024-aligned
+// base): the ring and barriers at fixed offsets, then the warps' merge
+// scratch for the group's G heads, the plan ([B+1] unit offsets, [B] checked
+// lengths) and the k/v scales.
 template <int FMT, int DH>
 struct SmemLayout {
   using C = Cfg<FMT, DH>;
   static constexpr int S = C::kStages;
   static constexpr size_t ring = 0;
   static constexpr size_t bars = ring + static_cast<size_t>(S) * C::kSlot;  // full[S], empty[S]
-  static constexpr size_t flags = bars + 2 * S * sizeof(uint64_t);  // bad[S], abort, issued, tot[8]
-  static constexpr size_t comb = (flags + (S + 2 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
-  static constexpr size_t comb_floats = 2 * kConsumerWarps * kMaxGroup + kConsumerWarps * kMaxGroup * DH;
-  static constexpr size_t seq = comb + comb_floats * sizeof(float);
-  static size_t total(int B) { return seq + (2 * static_cast<size_t>(B) + 1) * sizeof(int32_t) + 1024; }
+  // bad[S], abort, spare, tot[8], last[S]
+  static constexpr size_t flags = bars + 2 * S * sizeof(uint64_t);
+  static constexpr size_t comb = (flags + (2 * S + 2 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
+  __host__ __device__ static size_t comb_floats(int G) {
+    return static_cast<size_t>(kConsumerWarps) * G * (DH + 2);
+  }
+  __host__ __device__ static size_t seq(int G) {
+    return comb + ((comb_floats(G) * sizeof(float) + 15) & ~size_t(15));
+  }
+  __host__ __device__ static size_t scales(int G, int B) {
+    return seq(G) + (2 * static_cast<size_t>(B) + 1) * sizeof(int32_t);
+  }
+  __host__ __device__ static size_t total(int G, int B, int Hkv) {
+    return scales(G, B) + 2 * static_cast<size_t>(Hkv) * sizeof(float) + 1024;
+  }
 };
 
 struct DecodeParams {
@@ -149,11 +177,6 @@ KVQ_DEVI uint2 lds64(uint32_t addr) {
 
 KVQ_DEVI void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
 
-// Valid length of sequence b (same rule everywhere): out-of-range -> 0.
-KVQ_DEVI int seq_len_checked(const DecodeParams& p, int b) {
-  const int L = __ldg(p.seq_lens + b);
-  return (L < 0 || L > p.max_blocks * kBS) ? 0 : L;
-}
 
 KVQ_DEVI int window_lo(const DecodeParams& p, int L) {
   return (p.window > 0 && L > p.window) ? L - p.window : 0;
@@ -172,11 +195,19 @@ KVQ_DEVI int find_seq(const int32_t* seq_off, int B, int64_t u) {
   return lo;
 }
 
-// Exclusive scan of per-sequence unit counts into seq_off[0..B], and the
-// first page of every sequence's attended window into first_page[0..B).
-KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* first_page,
-                         int32_t* warp_tot) {
+// Exclusive scan of per-sequence unit counts into seq_off[0..B], the checked
+// length of every sequence into len_s[0..B), and the k/v scales of the KV
+// heads into sk_s / sv_s (per-tensor scales replicated).
+KVQ_DEVI int first_page_of(const DecodeParams& p, int L) { return window_lo(p, L) / kBS; }
+
+template <bool SCALED>
+KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s, float* sk_s,
+                         float* sv_s, int32_t* warp_tot) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int h = tid; h < p.Hkv; h += kThreads) {
+    sk_s[h] = SCALED ? __ldg(p.ks + (p.per_head ? h : 0)) : 1.f;
+    sv_s[h] = SCALED ? __ldg(p.vs + (p.per_head ? h : 0)) : 1.f;
+  }
   const int per = (p.B + kThreads - 1) / kThreads;
   const int b0 = tid * per, b1 = min(p.B, b0 + per);
   int local = 0;
@@ -185,9 +216,8 @@ KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* first
     if ((raw < 0 || raw > p.max_blocks * kBS) && blockIdx.x == 0)
       flag_status(p.status, KVQ_DEV_BAD_SEQLEN);
     const int L = (raw < 0 || raw > p.max_blocks * kBS) ? 0 : raw;
-    const int fp = window_lo(p, L) / kBS;
-    const int pages = L > 0 ? (L + kBS - 1) / kBS - fp : 0;
-    first_page[b] = fp;
+    const int pages = L > 0 ? (L + kBS - 1) / kBS - first_page_of(p, L) : 0;
+    len_s[b] = L;
     seq_off[b] = local;
     local += pages * p.Hkv;
   }
@@ -225,13 +255,21 @@ struct SoftmaxState {
   float l[2];  // per-lane partial denominators
 };
 
-// Online softmax update of one 16-token page; x holds log2-domain logits of
-// (token g, head 2t), (token g, head 2t+1), (token g+8, head 2t),
-// (token g+8, head 2t+1).  Returns the probabilities in pr; rescales o.
-template <int MT>
-KVQ_DEVI void softmax_page(float (&x)[4], float (&pr)[4], SoftmaxState& st, float (&o)[MT][4]) {
+// Online softmax update of NP 16-token pages.  x[4i .. 4i+3] hold page i's
+// log2-domain logits of (token g, head 2t), (token g, head 2t+1),
+// (token g+8, head 2t), (token g+8, head 2t+1).  Returns the probabilities
+// in pr; rescales o (lazily: only when the running max grows by more than
+// kRescaleThreshold, so p <= 2^8 and the exact max is rarely reduced).
+template <int NP, int MT>
+KVQ_DEVI void softmax_pages(const float (&x)[4 * NP], float (&pr)[4 * NP], SoftmaxState& st,
+                            float (&o)[MT][4]) {
   const float ninf = -INFINITY;
-  float lm0 = fmaxf(x[0], x[2]), lm1 = fmaxf(x[1], x[3]);
+  float lm0 = ninf, lm1 = ninf;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    lm0 = fmaxf(lm0, fmaxf(x[4 * i], x[4 * i + 2]));
+    lm1 = fmaxf(lm1, fmaxf(x[4 * i + 1], x[4 * i + 3]));
+  }
   const bool need = (lm0 > st.m[0] + kRescaleThreshold) || (lm1 > st.m[1] + kRescaleThreshold);
   if (__any_sync(kFull, need)) {
 #pragma unroll
@@ -254,12 +292,16 @@ KVQ_DEVI void softmax_page(float (&x)[4], float (&pr)[4], SoftmaxState& st, floa
     st.m[0] = n0;
     st.m[1] = n1;
   }
-  pr[0] = (x[0] == ninf) ? 0.f : fast_exp2(x[0] - st.m[0]);
-  pr[1] = (x[1] == ninf) ? 0.f : fast_exp2(x[1] - st.m[1]);
-  pr[2] = (x[2] == ninf) ? 0.f : fast_exp2(x[2] - st.m[0]);
-  pr[3] = (x[3] == ninf) ? 0.f : fast_exp2(x[3] - st.m[1]);
-  st.l[0] += pr[0] + pr[2];
-  st.l[1] += pr[1] + pr[3];
+#pragma unroll
+  for (int i = 0; i < 4 * NP; ++i) {
+    const float m = (i & 1) ? st.m[1] : st.m[0];
+    pr[i] = (x[i] == ninf) ? 0.f : fast_exp2(x[i] - m);
+  }
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    st.l[0] += pr[4 * i] + pr[4 * i + 2];
+    st.l[1] += pr[4 * i + 1] + pr[4 * i + 3];
+  }
 }
 
 // P^T as the B operand of the PV MMA (k = token, n = head), split into a high
@@ -267,7 +309,7 @@ KVQ_DEVI void softmax_page(float (&x)[4], float (&pr)[4], SoftmaxState& st, floa
 // 2t+8: 2t+1, 2t+9: 2t+9} so that a lane's two k values of a register come
 // from one source lane's (token g', token g'+8) pair.
 template <bool BF16P>
-KVQ_DEVI void p_fragments(const float (&pr)[4], int g, int t, int G, uint32_t (&bh)[2],
+KVQ_DEVI void p_fragments(const float* pr, int g, int t, int G, uint32_t (&bh)[2],
                           uint32_t (&bl)[2]) {
   uint32_t h0, h1, l0, l1;
   if (BF16P) {
@@ -296,163 +338,154 @@ KVQ_DEVI void p_fragments(const float (&pr)[4], int g, int t, int G, uint32_t (&
 
 KVQ_DEVI bool token_valid(int tok, int lo, int L, bool bad) { return !bad && tok >= lo && tok < L; }
 
-KVQ_DEVI void mask_logits(float (&x)[4], int tok0, int g, int lo, int L, bool bad) {
-  const int ta = tok0 + g, tb = tok0 + g + 8;
-  if (bad || ta < lo || ta >= L) x[0] = x[1] = -INFINITY;
-  if (bad || tb < lo || tb >= L) x[2] = x[3] = -INFINITY;
-}
 
-// FP8 page (E4M3 / E5M2).
+// Register image of one staged page: the lane's K fragment words (token rows
+// g and g+8) and V fragment words (tokens 2t, 2t+8, 2t+1, 2t+9).  Reading the
+// page into registers first lets the ring slot go back to the producer
+// before the math, so slots are held only while their data is in flight.
 template <int FMT, int DH>
-KVQ_DEVI void page_fp8(uint32_t kp, uint32_t vp, int g, int t, int G,
-                       const uint32_t (&qb)[DH / 16][2], float (&o)[DH / 16][4], SoftmaxState& st,
-                       float lscale, int tok0, int lo, int L, bool bad) {
+struct PageRegs {
   using C = Cfg<FMT, DH>;
-  constexpr int KW = DH / 16;  // 32-bit words of one K row a lane reads
-  uint32_t k0[KW], k1[KW];
-#pragma unroll
-  for (int c = 0; c < KW / 4; ++c) {
-    const uint32_t off = static_cast<uint32_t>(t * (DH / 4) + c * 16);
-    const uint4 a = lds128(kp + swz(g * C::kRow + off, C::kSwz));
-    const uint4 b = lds128(kp + swz((g + 8) * C::kRow + off, C::kSwz));
-    k0[4 * c] = a.x; k0[4 * c + 1] = a.y; k0[4 * c + 2] = a.z; k0[4 * c + 3] = a.w;
-    k1[4 * c] = b.x; k1[4 * c + 1] = b.y; k1[4 * c + 2] = b.z; k1[4 * c + 3] = b.w;
-  }
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int kk = 0; kk < KW; ++kk) {
-    uint32_t a[4];
-    a[0] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(k0[kk] & 0xFFFFu));
-    a[1] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(k1[kk] & 0xFFFFu));
-    a[2] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(k0[kk] >> 16));
-    a[3] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(k1[kk] >> 16));
-    mma_f16(s, a, qb[kk][0], qb[kk][1]);
-  }
-  float x[4] = {s[0] * lscale, s[1] * lscale, s[2] * lscale, s[3] * lscale};
-  mask_logits(x, tok0, g, lo, L, bad);
-  float pr[4];
-  softmax_page<DH / 16>(x, pr, st, o);
-  uint32_t bh[2], bl[2];
-  p_fragments<false>(pr, g, t, G, bh, bl);
+  static constexpr int KB = C::kRow / 4;  // bytes of one K row a lane reads
+  static constexpr int VB = C::kRow / 8;  // bytes of one V row a lane reads
+  uint32_t k0[KB / 4], k1[KB / 4];
+  uint32_t v[4][VB / 4];
+};
 
-  constexpr int VW = DH / 32;  // 32-bit words of one V row a lane reads
-  uint32_t A[VW], B[VW], Cc[VW], D[VW];
-  const int rows[4] = {2 * t, 2 * t + 8, 2 * t + 1, 2 * t + 9};
-  uint32_t* dst[4] = {A, B, Cc, D};
-  const bool edge = bad || tok0 < lo || tok0 + kBS > L;  // warp-uniform
+template <int FMT, int DH>
+KVQ_DEVI void load_page(uint32_t kp, uint32_t vp, int g, int t, int tok0, int lo, int L,
+                        bool bad, PageRegs<FMT, DH>& r) {
+  using C = Cfg<FMT, DH>;
+  using R = PageRegs<FMT, DH>;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const uint32_t addr = vp + swz(rows[r] * C::kRow + g * (DH / 8), C::kSwz);
-    if (VW == 4) {
-      const uint4 v = lds128(addr);
-      dst[r][0] = v.x; dst[r][1] = v.y; dst[r][2] = v.z; dst[r][3] = v.w;
-    } else {
-      const uint2 v = lds64(addr);
-      dst[r][0] = v.x; dst[r][1] = v.y;
-    }
-    if (edge && !token_valid(tok0 + rows[r], lo, L, bad)) {
-#pragma unroll
-      for (int w = 0; w < VW; ++w) dst[r][w] = 0u;
-    }
-  }
-#pragma unroll
-  for (int w = 0; w < VW; ++w) {
-    const uint32_t x0 = prmt(A[w], B[w], 0x5140u), y0 = prmt(A[w], B[w], 0x7362u);
-    const uint32_t z0 = prmt(Cc[w], D[w], 0x5140u), u0 = prmt(Cc[w], D[w], 0x7362u);
-    uint32_t a[4];
-    a[0] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(x0 & 0xFFFFu));
-    a[1] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(x0 >> 16));
-    a[2] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(z0 & 0xFFFFu));
-    a[3] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(z0 >> 16));
-    mma_f16(o[2 * w], a, bh[0], bh[1]);
-    mma_f16(o[2 * w], a, bl[0], bl[1]);
-    a[0] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(y0 & 0xFFFFu));
-    a[1] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(y0 >> 16));
-    a[2] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(u0 & 0xFFFFu));
-    a[3] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(u0 >> 16));
-    mma_f16(o[2 * w + 1], a, bh[0], bh[1]);
-    mma_f16(o[2 * w + 1], a, bl[0], bl[1]);
-  }
-}
-
-// bf16 page (layers skipped from quantization).
-template <int DH>
-KVQ_DEVI void page_bf16(uint32_t kp, uint32_t vp, int g, int t, int G,
-                        const uint32_t (&qb)[DH / 16][2], float (&o)[DH / 16][4],
-                        SoftmaxState& st, float lscale, int tok0, int lo, int L, bool bad) {
-  using C = Cfg<KVQ_FMT_BF16, DH>;
-  constexpr int KW = DH / 8;  // words of one K row a lane reads (2 bf16 each)
-  uint32_t k0[KW], k1[KW];
-#pragma unroll
-  for (int c = 0; c < KW / 4; ++c) {
-    const int off = t * (DH / 2) + c * 16;
+  for (int c = 0; c < R::KB / 16; ++c) {
+    const int off = t * R::KB + c * 16;
     const uint4 a = lds128(kp + swz(page_off<C::kRow>(g, off), C::kSwz));
     const uint4 b = lds128(kp + swz(page_off<C::kRow>(g + 8, off), C::kSwz));
-    k0[4 * c] = a.x; k0[4 * c + 1] = a.y; k0[4 * c + 2] = a.z; k0[4 * c + 3] = a.w;
-    k1[4 * c] = b.x; k1[4 * c + 1] = b.y; k1[4 * c + 2] = b.z; k1[4 * c + 3] = b.w;
+    r.k0[4 * c] = a.x; r.k0[4 * c + 1] = a.y; r.k0[4 * c + 2] = a.z; r.k0[4 * c + 3] = a.w;
+    r.k1[4 * c] = b.x; r.k1[4 * c + 1] = b.y; r.k1[4 * c + 2] = b.z; r.k1[4 * c + 3] = b.w;
   }
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int kk = 0; kk < DH / 16; ++kk) {
-    const uint32_t a[4] = {k0[2 * kk], k1[2 * kk], k0[2 * kk + 1], k1[2 * kk + 1]};
-    mma_bf16(s, a, qb[kk][0], qb[kk][1]);
-  }
-  float x[4] = {s[0] * lscale, s[1] * lscale, s[2] * lscale, s[3] * lscale};
-  mask_logits(x, tok0, g, lo, L, bad);
-  float pr[4];
-  softmax_page<DH / 16>(x, pr, st, o);
-  uint32_t bh[2], bl[2];
-  p_fragments<true>(pr, g, t, G, bh, bl);
-
-  constexpr int VW = DH / 16;  // words of one V row a lane reads
-  uint32_t V[4][VW];
   const int rows[4] = {2 * t, 2 * t + 8, 2 * t + 1, 2 * t + 9};
   const bool edge = bad || tok0 < lo || tok0 + kBS > L;  // warp-uniform
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
+  for (int q = 0; q < 4; ++q) {
+    if (R::VB >= 16) {
 #pragma unroll
-    for (int c = 0; c < VW / 4; ++c) {
-      const uint4 v = lds128(vp + swz(page_off<C::kRow>(rows[r], g * (DH / 4) + c * 16), C::kSwz));
-      V[r][4 * c] = v.x; V[r][4 * c + 1] = v.y; V[r][4 * c + 2] = v.z; V[r][4 * c + 3] = v.w;
+      for (int c = 0; c < R::VB / 16; ++c) {
+        const uint4 v = lds128(vp + swz(page_off<C::kRow>(rows[q], g * R::VB + c * 16), C::kSwz));
+        r.v[q][4 * c] = v.x; r.v[q][4 * c + 1] = v.y; r.v[q][4 * c + 2] = v.z; r.v[q][4 * c + 3] = v.w;
+      }
+    } else {
+      const uint2 v = lds64(vp + swz(page_off<C::kRow>(rows[q], g * R::VB), C::kSwz));
+      r.v[q][0] = v.x;
+      r.v[q][1] = v.y;
     }
-    if (edge && !token_valid(tok0 + rows[r], lo, L, bad)) {
+    // a masked token's V row may hold anything (p = 0 would not clear a NaN)
+    if (edge && !token_valid(tok0 + rows[q], lo, L, bad)) {
 #pragma unroll
-      for (int w = 0; w < VW; ++w) V[r][w] = 0u;
+      for (int w = 0; w < R::VB / 4; ++w) r.v[q][w] = 0u;
     }
-  }
-#pragma unroll
-  for (int w = 0; w < VW; ++w) {
-    const uint32_t a[4] = {prmt(V[0][w], V[1][w], 0x5410u), prmt(V[0][w], V[1][w], 0x7632u),
-                           prmt(V[2][w], V[3][w], 0x5410u), prmt(V[2][w], V[3][w], 0x7632u)};
-    mma_bf16(o[w], a, bh[0], bh[1]);
-    mma_bf16(o[w], a, bl[0], bl[1]);
   }
 }
 
-// Q of head g (lane row) of the group, dims t*(DH/4) + 4kk + {0..3}, as the
-// B operand of the QK MMA: f16 for the FP8 caches (exact for |q| in the f16
-// normal range), the bf16 bits for the bf16 cache.
-template <int FMT, int DH>
-KVQ_DEVI void load_q(const DecodeParams& p, int b, int gkv, int g, int t,
-                     uint32_t (&qb)[DH / 16][2]) {
-  if (g >= p.G) {
+// QK^T, online softmax and PV of NP pages held in registers (the pages'
+// MMA chains are independent, which hides their latency).
+//   QK: the K tile is the m16n8k16 A operand (16 tokens x 16 dims; FP8 codes
+//   converted to f16 exactly, or bf16 as is), the group's query heads the B
+//   operand; lane (g, t) covers dims t*(DH/4) + 4kk + {0..3} of step kk.
+//   PV: O^T += V^T P^T with m-tile mt, row r -> dim g*(DH/8) + 2mt + r/8.
+template <int FMT, int DH, int NP>
+KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[NP],
+                            const bool (&bad)[NP], int g, int t, int G,
+                            const uint32_t (&qb)[DH / 16][2], float (&o)[DH / 16][4],
+                            SoftmaxState& st, float lscale, int lo, int L) {
+  using R = PageRegs<FMT, DH>;
+  constexpr bool BF = FMT == KVQ_FMT_BF16;
+  float s[NP][4];
 #pragma unroll
-    for (int kk = 0; kk < DH / 16; ++kk) qb[kk][0] = qb[kk][1] = 0u;
-    return;
+  for (int i = 0; i < NP; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < DH / 16; ++kk) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      uint32_t a[4];
+      if (BF) {
+        a[0] = r[i].k0[2 * kk]; a[1] = r[i].k1[2 * kk];
+        a[2] = r[i].k0[2 * kk + 1]; a[3] = r[i].k1[2 * kk + 1];
+        mma_bf16(s[i], a, qb[kk][0], qb[kk][1]);
+      } else {
+        fp8x4_to_f16x2x2<FMT>(r[i].k0[kk], a[0], a[2]);
+        fp8x4_to_f16x2x2<FMT>(r[i].k1[kk], a[1], a[3]);
+        mma_f16(s[i], a, qb[kk][0], qb[kk][1]);
+      }
+    }
   }
+  float x[4 * NP];
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int ta = tok0[i] + g, tb = ta + 8;
+    const bool va = token_valid(ta, lo, L, bad[i]), vb = token_valid(tb, lo, L, bad[i]);
+    x[4 * i] = va ? s[i][0] * lscale : -INFINITY;
+    x[4 * i + 1] = va ? s[i][1] * lscale : -INFINITY;
+    x[4 * i + 2] = vb ? s[i][2] * lscale : -INFINITY;
+    x[4 * i + 3] = vb ? s[i][3] * lscale : -INFINITY;
+  }
+  float pr[4 * NP];
+  softmax_pages<NP, DH / 16>(x, pr, st, o);
+  uint32_t bh[NP][2], bl[NP][2];
+#pragma unroll
+  for (int i = 0; i < NP; ++i) p_fragments<BF>(pr + 4 * i, g, t, G, bh[i], bl[i]);
+
+#pragma unroll
+  for (int w = 0; w < R::VB / 4; ++w) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const uint32_t* v0 = r[i].v[0];
+      const uint32_t* v1 = r[i].v[1];
+      const uint32_t* v2 = r[i].v[2];
+      const uint32_t* v3 = r[i].v[3];
+      if (BF) {  // word w = dims g*(DH/8) + 2w, +1 -> m-tile w, rows g (lo) and g+8 (hi)
+        const uint32_t a[4] = {prmt(v0[w], v1[w], 0x5410u), prmt(v0[w], v1[w], 0x7632u),
+                               prmt(v2[w], v3[w], 0x5410u), prmt(v2[w], v3[w], 0x7632u)};
+        mma_bf16(o[w], a, bh[i][0], bh[i][1]);
+        mma_bf16(o[w], a, bl[i][0], bl[i][1]);
+      } else {  // word w = dims g*(DH/8) + 4w .. +3 -> m-tiles 2w, 2w+1
+        const uint32_t x0 = prmt(v0[w], v1[w], 0x5140u), y0 = prmt(v0[w], v1[w], 0x7362u);
+        const uint32_t z0 = prmt(v2[w], v3[w], 0x5140u), u0 = prmt(v2[w], v3[w], 0x7362u);
+        uint32_t a[4], c[4];
+        fp8x4_to_f16x2x2<FMT>(x0, a[0], a[1]);
+        fp8x4_to_f16x2x2<FMT>(z0, a[2], a[3]);
+        fp8x4_to_f16x2x2<FMT>(y0, c[0], c[1]);
+        fp8x4_to_f16x2x2<FMT>(u0, c[2], c[3]);
+        mma_f16(o[2 * w], a, bh[i][0], bh[i][1]);
+        mma_f16(o[2 * w + 1], c, bh[i][0], bh[i][1]);
+        mma_f16(o[2 * w], a, bl[i][0], bl[i][1]);
+        mma_f16(o[2 * w + 1], c, bl[i][0], bl[i][1]);
+      }
+    }
+  }
+}
+
+// Q of head g (lane row) of the group, dims t*(DH/4) + 4kk + {0..3}: the
+// raw bf16 words (issued a piece ahead), then the B operand of the QK MMA:
+// f16 for the FP8 caches (exact for |q| in the f16 normal range), the bf16
+// bits for the bf16 cache.  Rows past the group (g >= G) are zero.
+template <int DH>
+KVQ_DEVI void load_q_raw(const DecodeParams& p, int b, int gkv, int g, int t,
+                         uint32_t (&w)[DH / 8]) {
   const int64_t qrow = static_cast<int64_t>(b) * p.Hq + gkv * p.G + g;
-  if (!guard(b >= 0 && b < p.B && qrow >= 0 && qrow < static_cast<int64_t>(p.B) * p.Hq, p.status, 2)) {
-#pragma unroll
-    for (int kk = 0; kk < DH / 16; ++kk) qb[kk][0] = qb[kk][1] = 0u;
-    return;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * DH + t * (DH / 4));
-  uint32_t w[DH / 8];
+  const bool ok = g < p.G && guard(b >= 0 && b < p.B && qrow < static_cast<int64_t>(p.B) * p.Hq,
+                                   p.status, 2);
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + (ok ? qrow : 0) * DH + t * (DH / 4));
 #pragma unroll
   for (int i = 0; i < DH / 32; ++i) {
-    const uint4 v = __ldg(src + i);
+    const uint4 v = ok ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
     w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
   }
+}
+
+template <int FMT, int DH>
+KVQ_DEVI void q_fragments(const uint32_t (&w)[DH / 8], uint32_t (&qb)[DH / 16][2]) {
 #pragma unroll
   for (int kk = 0; kk < DH / 16; ++kk) {
     if (FMT == KVQ_FMT_BF16) {
@@ -487,13 +520,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   uint64_t* empty = full + S;
   uint32_t* bad_s = reinterpret_cast<uint32_t*>(smem + SL::flags);
   volatile uint32_t* abort_flag = bad_s + S;
-  int32_t* issued_s = reinterpret_cast<int32_t*>(bad_s + S + 1);
-  int32_t* warp_tot = issued_s + 1;                        // [8]
-  float* cm = reinterpret_cast<float*>(smem + SL::comb);   // [4][8] running max
-  float* cl = cm + kConsumerWarps * kMaxGroup;             // [4][8] denominators
-  float* co = cl + kConsumerWarps * kMaxGroup;             // [4][8][DH] unnormalised O
-  int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq);  // [B+1]
-  int32_t* first_page = seq_off + p.B + 1;                        // [B]
+  int32_t* warp_tot = reinterpret_cast<int32_t*>(bad_s + S + 2);  // [8]
+  int32_t* last_s = warp_tot + 8;  // [S] last position issued into each slot
+  float* cm = reinterpret_cast<float*>(smem + SL::comb);   // [warps][G] running max
+  float* cl = cm + kConsumerWarps * p.G;                   // [warps][G] denominators
+  float* co = cl + kConsumerWarps * p.G;                   // [warps][G][DH] unnormalised O
+  int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq(p.G));  // [B+1]
+  int32_t* len_s = seq_off + p.B + 1;                                  // [B]
+  float* sk_s = reinterpret_cast<float*>(smem + SL::scales(p.G, p.B)); // [Hkv]
+  float* sv_s = sk_s + p.Hkv;                                          // [Hkv]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -502,14 +537,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       mbar_init(&empty[s], 1);
     }
     *abort_flag = 0u;
-    *issued_s = 0;
+    for (int s = 0; s < S; ++s) last_s[s] = -1;
     fence_mbar_init();
   }
   if (warp == kConsumerWarps && lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
-  build_plan(p, seq_off, first_page, warp_tot);  // contains __syncthreads
+  build_plan<FMT != KVQ_FMT_BF16>(p, seq_off, len_s, sk_s, sv_s, warp_tot);  // has __syncthreads
 
   const int64_t W = seq_off[p.B];
   if (blockIdx.x == 0)
@@ -524,94 +559,131 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    int nxt_blk = 0, nxt_g = 0;
-    auto fetch = [&](int64_t i, int& blk, int& g) {
-      blk = 0;
-      g = 0;
-      if (i < total) {
-        const int64_t u = u0 + i;
-        const int b = find_seq(seq_off, p.B, u);
-        const int pages = (seq_off[b + 1] - seq_off[b]) / p.Hkv;
-        const int r = static_cast<int>(u - seq_off[b]);
-        g = r / pages;
-        const int pg = r - g * pages;
-        const int col = first_page[b] + pg;
-        if (guard(b >= 0 && b < p.B && col >= 0 && col < p.max_blocks && g >= 0 && g < p.Hkv,
-                  p.status, 0))
-          blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + col);
-        else
-          blk = -1;
-      }
+    // Lane j owns ring slots j and j + 32 and issues their positions
+    // slot, slot + S, slot + 2S, ... of the CTA's page stream.  Each lane
+    // polls its own empty barriers without blocking, so up to S pages are
+    // requested at once, and looks up the block id of a slot's next position
+    // right after an issue, one ring turn ahead.
+    constexpr int SPL = (S + 31) / 32;  // slots per lane
+    static_assert(SPL <= 2, "at most 64 ring slots");
+    auto lookup = [&](int64_t i, int& blk_out, int& g_out) {
+      const int64_t u = u0 + i;
+      const int b = find_seq(seq_off, p.B, u);
+      const int pages = (seq_off[b + 1] - seq_off[b]) / p.Hkv;
+      const int r = static_cast<int>(u - seq_off[b]);
+      g_out = r / pages;
+      const int pg = r - g_out * pages;
+      const int col = first_page_of(p, len_s[b]) + pg;
+      if (guard(b >= 0 && b < p.B && col >= 0 && col < p.max_blocks && g_out >= 0 &&
+                    g_out < p.Hkv,
+                p.status, 0))
+        blk_out = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + col);
+      else
+        blk_out = -1;
     };
-    fetch(lane, nxt_blk, nxt_g);
-    bool stop = false;
-    int64_t issued = 0;
-    for (int64_t base = 0; base < total && !stop; base += 32) {
-      const int cur_blk = nxt_blk, cur_g = nxt_g;
-      if (base + 32 < total) fetch(base + 32 + lane, nxt_blk, nxt_g);
-      const int cnt = static_cast<int>(total - base < 32 ? total - base : 32);
-      for (int i = 0; i < cnt; ++i) {
-        const int blk = __shfl_sync(kFull, cur_blk, i);
-        const int g = __shfl_sync(kFull, cur_g, i);
-        if (lane == 0 && !stop) {
-          const int64_t pos = base + i;
-          const int slot = static_cast<int>(pos % S);
-          const uint32_t par = static_cast<uint32_t>((pos / S) & 1) ^ 1u;
-          if (!wait_or_abort(&empty[slot], par, abort_flag)) {
+    int64_t q[SPL];
+    int blk[SPL], gg[SPL];
+    uint32_t par[SPL];
+    bool done[SPL];
+#pragma unroll
+    for (int k = 0; k < SPL; ++k) {
+      q[k] = lane + 32 * k;
+      par[k] = 1u;  // the first wait on a fresh empty barrier passes
+      done[k] = lane + 32 * k >= S || q[k] >= total;
+      blk[k] = gg[k] = 0;
+      if (!done[k]) lookup(q[k], blk[k], gg[k]);
+    }
+    uint32_t idle = 0;
+    while (true) {
+      bool live = false, progressed = false;
+#pragma unroll
+      for (int k = 0; k < SPL; ++k) {
+        if (done[k]) continue;
+        live = true;
+        const int slot = lane + 32 * k;
+        if (!mbar_test_wait(&empty[slot], par[k])) continue;
+        const bool bad = blk[k] < 0 || blk[k] >= p.num_blocks;
+        if (bad) flag_status(p.status, KVQ_DEV_BAD_BLOCK);
+        int32_t row = ((bad ? 0 : blk[k]) * p.Hkv + gg[k]) * kBS;
+        bool skip = bad;
+        if (!guard(row >= 0 && row + kBS <= p.rows, p.status, 1)) {
+          row = 0;
+          skip = true;
+        }
+        bad_s[slot] = skip ? 1u : 0u;
+        uint8_t* dstK = ring + slot * C::kSlot;
+        mbar_arrive_expect_tx(&full[slot], C::kSlot);
+        if (C::kRow > 128) {  // two 128-byte column boxes per page
+          tma_load_2d(dstK, &tmk, 0, row, &full[slot]);
+          tma_load_2d(dstK + C::kPage / 2, &tmk, 64, row, &full[slot]);
+          tma_load_2d(dstK + C::kPage, &tmv, 0, row, &full[slot]);
+          tma_load_2d(dstK + C::kPage + C::kPage / 2, &tmv, 64, row, &full[slot]);
+        } else {
+          tma_load_2d(dstK, &tmk, 0, row, &full[slot]);
+          tma_load_2d(dstK + C::kPage, &tmv, 0, row, &full[slot]);
+        }
+        last_s[slot] = static_cast<int32_t>(q[k]);
+        q[k] += S;
+        par[k] ^= 1u;
+        if (q[k] < total)
+          lookup(q[k], blk[k], gg[k]);
+        else
+          done[k] = true;
+        progressed = true;
+      }
+      if (!__any_sync(kFull, live)) break;
+      if (__any_sync(kFull, progressed)) {
+        idle = 0;
+      } else {
+        if (*abort_flag) break;
+        if (++idle > kMaxPolls) {
+          if (lane == 0) {
             *abort_flag = 1u;
             flag_status(p.status, KVQ_DEV_WAIT_TIMEOUT);
-            stop = true;
-          } else {
-            const bool bad = blk < 0 || blk >= p.num_blocks;
-            if (bad) flag_status(p.status, KVQ_DEV_BAD_BLOCK);
-            bad_s[slot] = bad ? 1u : 0u;
-            int32_t row = ((bad ? 0 : blk) * p.Hkv + g) * kBS;
-            if (!guard(row >= 0 && row + kBS <= p.rows && slot >= 0 && slot < S, p.status, 1)) {
-              row = 0;
-              bad_s[slot % S] = 1u;
-            }
-            uint8_t* dstK = ring + slot * C::kSlot;
-            mbar_arrive_expect_tx(&full[slot], C::kSlot);
-            if (C::kRow > 128) {  // two 128-byte column boxes per page
-              tma_load_2d(dstK, &tmk, 0, row, &full[slot]);
-              tma_load_2d(dstK + C::kPage / 2, &tmk, 64, row, &full[slot]);
-              tma_load_2d(dstK + C::kPage, &tmv, 0, row, &full[slot]);
-              tma_load_2d(dstK + C::kPage + C::kPage / 2, &tmv, 64, row, &full[slot]);
-            } else {
-              tma_load_2d(dstK, &tmk, 0, row, &full[slot]);
-              tma_load_2d(dstK + C::kPage, &tmv, 0, row, &full[slot]);
-            }
-            issued = pos + 1;
           }
+          break;
         }
-        stop = __shfl_sync(kFull, stop ? 1 : 0, 0) != 0;
+        __nanosleep(20);
       }
     }
-    if (lane == 0) *issued_s = static_cast<int32_t>(issued);
   } else {
     // ------------------------------------------------------------ consumers
     const int g = lane >> 2, t = lane & 3;
     const int ctid = tid;  // 0 .. 127
     uint32_t qb[MT][2];
+    uint32_t qraw[DH / 8];  // raw Q words of the current piece, loaded a piece ahead
     float o[MT][4];
-    int64_t pos_base = 0;
+    int pos_base = 0;
     bool aborted = false;
-    for (int64_t u = u0; u < u1;) {
-      const int b = find_seq(seq_off, p.B, u);
-      const int seg_units = seq_off[b + 1] - seq_off[b];
-      const int pages = seg_units / p.Hkv;
-      if (!guard(pages > 0 && u >= seq_off[b] && u < seq_off[b + 1], p.status, 10)) break;
+    // piece = the part of one (sequence, KV head) segment inside [u0, u1)
+    auto piece_at = [&](int64_t u, int& b, int& gkv, int& pages, int& p0) {
+      b = find_seq(seq_off, p.B, u);
+      pages = (seq_off[b + 1] - seq_off[b]) / p.Hkv;
       const int r = static_cast<int>(u - seq_off[b]);
-      const int gkv = r / pages;
-      const int p0 = r - gkv * pages;
+      gkv = pages > 0 ? r / pages : 0;
+      p0 = r - gkv * pages;
+    };
+    if (u0 < u1) {
+      int b, gkv, pages, p0;
+      piece_at(u0, b, gkv, pages, p0);
+      load_q_raw<DH>(p, b, gkv, g, t, qraw);
+    }
+    for (int64_t u = u0; u < u1;) {
+      int b, gkv, pages, p0;
+      piece_at(u, b, gkv, pages, p0);
+      if (!guard(pages > 0 && u >= seq_off[b] && u < seq_off[b + 1], p.status, 10)) break;
       const int n = static_cast<int>((u1 - u) < (pages - p0) ? (u1 - u) : (pages - p0));
-      const int L = seq_len_checked(p, b);
+      const int L = len_s[b];
       const int lo = window_lo(p, L);
-      const int fp = first_page[b];
-      const float sk = (FMT == KVQ_FMT_BF16) ? 1.f : __ldg(p.ks + (p.per_head ? gkv : 0));
-      const float sv = (FMT == KVQ_FMT_BF16) ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
-      const float lscale = sk * p.logit_scale;
-      load_q<FMT, DH>(p, b, gkv, g, t, qb);
+      const int fp = lo / kBS;
+      const float sv = sv_s[gkv];
+      const float lscale = sk_s[gkv] * p.logit_scale;
+      q_fragments<FMT, DH>(qraw, qb);
+      if (u + n < u1) {  // next piece's Q, in flight while this piece runs
+        int nb, ng, npg, np0;
+        piece_at(u + n, nb, ng, npg, np0);
+        load_q_raw<DH>(p, nb, ng, g, t, qraw);
+      }
       SoftmaxState st;
       st.m[0] = st.m[1] = -INFINITY;
       st.l[0] = st.l[1] = 0.f;
@@ -619,30 +691,65 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
       static_assert(S % kConsumerWarps == 0, "slots must split evenly among the consumer warps");
-      const int j0 = (warp - static_cast<int>(pos_base % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
-      for (int j = j0; j < n; j += kConsumerWarps) {
-        const int64_t pos = pos_base + j;
-        const int slot = static_cast<int>(pos % S);
-        const uint32_t par = static_cast<uint32_t>((pos / S) & 1);
-        if (!aborted && !wait_or_abort(&full[slot], par, abort_flag)) {
+      // This warp's positions in the piece are j0, j0 + 4, j0 + 8, ...; it
+      // takes them NP at a time (positions j, j + 4, ..., j + 4 (NP - 1)).
+      constexpr int NP = C::kPagesPerStep;
+      const int j0 = (warp - pos_base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+      int cur_slot = (pos_base + j0) % S;  // stage and phase parity of position pos_base + j0
+      uint32_t cur_par = static_cast<uint32_t>(((pos_base + j0) / S) & 1);
+      for (int j = j0; j < n; j += NP * kConsumerWarps) {
+        int slot[NP];
+        bool have[NP];
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          have[i] = j + i * kConsumerWarps < n;  // warp-uniform
+          slot[i] = cur_slot;
+          if (have[i] && ok && !aborted) ok = wait_or_abort(&full[cur_slot], cur_par, abort_flag);
+          cur_slot += kConsumerWarps;
+          if (cur_slot >= S) {
+            cur_slot -= S;
+            cur_par ^= 1u;
+          }
+        }
+        if (!__all_sync(kFull, ok) && !aborted) {
           aborted = true;
           if (lane == 0) {
             *abort_flag = 1u;
             flag_status(p.status, KVQ_DEV_WAIT_TIMEOUT);
           }
         }
-        aborted = __shfl_sync(kFull, aborted ? 1 : 0, 0) != 0;
         if (!aborted) {
-          const uint32_t kp = smem_u32(ring + slot * C::kSlot);
-          const int tok0 = (fp + p0 + j) * kBS;
-          const bool bad = bad_s[slot] != 0u;
-          if (FMT == KVQ_FMT_BF16)
-            page_bf16<DH>(kp, kp + C::kPage, g, t, p.G, qb, o, st, lscale, tok0, lo, L, bad);
-          else
-            page_fp8<FMT, DH>(kp, kp + C::kPage, g, t, p.G, qb, o, st, lscale, tok0, lo, L, bad);
+          PageRegs<FMT, DH> pr[NP];
+          int tok0[NP];
+          bool bad[NP];
+#pragma unroll
+          for (int i = 0; i < NP; ++i) {
+            tok0[i] = (fp + p0 + j + i * kConsumerWarps) * kBS;
+            if (have[i]) {
+              const uint32_t kp = smem_u32(ring + slot[i] * C::kSlot);
+              bad[i] = bad_s[slot[i]] != 0u;
+              load_page<FMT, DH>(kp, kp + C::kPage, g, t, tok0[i], lo, L, bad[i], pr[i]);
+            } else {  // past the piece's last page: an empty, masked page
+              bad[i] = true;
+              pr[i] = PageRegs<FMT, DH>{};
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {  // slots free: their data is in registers
+#pragma unroll
+            for (int i = 0; i < NP; ++i)
+              if (have[i]) mbar_arrive(&empty[slot[i]]);
+          }
+          compute_pages<FMT, DH, NP>(pr, tok0, bad, g, t, p.G, qb, o, st, lscale, lo, L);
+        } else {
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < NP; ++i)
+              if (have[i]) mbar_arrive(&empty[slot[i]]);
+          }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
       }
 
       // ---- merge the four warps' states of this segment piece
@@ -656,10 +763,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         const int h = 2 * t + c;
         if (h < p.G) {
           if (g == 0) {
-            cm[warp * kMaxGroup + h] = st.m[c];
-            cl[warp * kMaxGroup + h] = st.l[c];
+            cm[warp * p.G + h] = st.m[c];
+            cl[warp * p.G + h] = st.l[c];
           }
-          float* dst = co + (warp * kMaxGroup + h) * DH + g * (DH / 8);
+          float* dst = co + (warp * p.G + h) * DH + g * (DH / 8);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
             *reinterpret_cast<float2*>(dst + 2 * mt) = make_float2(o[mt][c], o[mt][2 + c]);
@@ -672,15 +779,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         const int h = idx / DH, d = idx - h * DH;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * kMaxGroup + h]);
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * p.G + h]);
         float acc = 0.f, ls = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
           for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = cm[w * kMaxGroup + h];
+            const float mw = cm[w * p.G + h];
             const float sc = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-            acc += co[(w * kMaxGroup + h) * DH + d] * sc;
-            ls += cl[w * kMaxGroup + h] * sc;
+            acc += co[(w * p.G + h) * DH + d] * sc;
+            ls += cl[w * p.G + h] * sc;
           }
         }
         if (single) {
@@ -704,22 +811,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   __syncthreads();
   // After an abort, wait (bounded) for copies still in flight before exit.
   if (*abort_flag && tid == 0) {
-    const int64_t issued = *issued_s;
-    for (int64_t pos = issued > S ? issued - S : 0; pos < issued; ++pos)
-      mbar_wait(&full[pos % S], static_cast<uint32_t>((pos / S) & 1));
+    for (int s = 0; s < S; ++s)
+      if (last_s[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>((last_s[s] / S) & 1));
   }
 }
 
-// Merge of the partial states of segments split across CTAs.
+// Merge of the partial states of segments split across CTAs: one CTA per
+// (sequence, KV head), one thread per (head, dim).  The per-piece weights
+// 2^(m - M) and the denominators are formed once in shared memory; the o
+// loads of the pieces are independent, so they pipeline.
 template <int DH>
-__global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(1024) reduce_kernel(const DecodeParams p) {
+  extern __shared__ float red_smem[];
   const int b = blockIdx.x / p.Hkv, gkv = blockIdx.x - b * p.Hkv;
+  const int tid = threadIdx.x, G = p.G;
   const int64_t W = p.ws_seq_off[p.B];
   const int64_t so = p.ws_seq_off[b];
   const int pages = (p.ws_seq_off[b + 1] - p.ws_seq_off[b]) / p.Hkv;
-  uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + gkv * p.G) * DH;
+  uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + gkv * G) * DH;
   if (pages == 0) {
-    for (int idx = threadIdx.x; idx < p.G * DH; idx += blockDim.x) out[idx] = 0;
+    for (int idx = tid; idx < G * DH; idx += blockDim.x) out[idx] = 0;
     return;
   }
   const int64_t us = so + static_cast<int64_t>(gkv) * pages, ue = us + pages;
@@ -729,25 +840,40 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p) {
   const int64_t c_lo = ((us + 1) * Pe + W - 1) / W - 1;
   const int64_t c_hi = (ue * Pe + W - 1) / W - 1;
   if (c_lo == c_hi) return;  // one CTA held the whole segment and wrote it
-  const float sv = (p.vs == nullptr) ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
   const int64_t sigma = static_cast<int64_t>(b) * p.Hkv + gkv;
   if (!guard(c_lo >= 0 && c_hi < Pe && c_lo <= c_hi && c_hi + sigma < p.n_slots, p.status, 5))
     return;
-  for (int idx = threadIdx.x; idx < p.G * DH; idx += blockDim.x) {
-    const int h = idx / DH, d = idx - h * DH;
+  const int n = static_cast<int>(c_hi - c_lo + 1);
+  float* wgt = red_smem;        // [n][G]: m, then the weight 2^(m - M)
+  float* Mh = wgt + n * G;      // [G]
+  float* Lh = Mh + G;           // [G]
+  const float* ml = p.ws_ml + ((c_lo + sigma) * G) * 2;
+  for (int i = tid; i < n * G; i += blockDim.x) wgt[i] = ml[2 * i];
+  if (tid < G) Lh[tid] = 0.f;
+  __syncthreads();
+  if (tid < G) {
     float M = -INFINITY;
-    for (int64_t c = c_lo; c <= c_hi; ++c) M = fmaxf(M, p.ws_ml[((c + sigma) * p.G + h) * 2]);
-    float acc = 0.f, ls = 0.f;
-    if (M != -INFINITY) {
-      for (int64_t c = c_lo; c <= c_hi; ++c) {
-        const int64_t s = (c + sigma) * p.G + h;
-        const float m = p.ws_ml[s * 2];
-        const float sc = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
-        acc += p.ws_o[s * DH + d] * sc;
-        ls += p.ws_ml[s * 2 + 1] * sc;
-      }
-    }
-    out[h * DH + d] = to_bf16(ls > 0.f ? acc / ls * sv : 0.f);
+    for (int c = 0; c < n; ++c) M = fmaxf(M, wgt[c * G + tid]);
+    Mh[tid] = M;
+  }
+  __syncthreads();
+  for (int i = tid; i < n * G; i += blockDim.x) {
+    const int h = i % G;
+    const float m = wgt[i], M = Mh[h];
+    const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
+    wgt[i] = w;
+    atomicAdd(&Lh[h], ml[2 * i + 1] * w);
+  }
+  __syncthreads();
+  const float sv = (p.vs == nullptr) ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
+  const float* ob = p.ws_o + (c_lo + sigma) * G * DH;
+  for (int idx = tid; idx < G * DH; idx += blockDim.x) {
+    const int h = idx / DH;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < n; ++c) acc += wgt[c * G + h] * ob[static_cast<int64_t>(c) * G * DH + idx];
+    const float ls = Lh[h];
+    out[idx] = to_bf16(ls > 0.f ? acc / ls * sv : 0.f);
   }
 }
 
@@ -792,19 +918,19 @@ static bool make_cache_map(CUtensorMap* m, const void* base, int fmt, int dh, ui
 }
 
 template <int FMT, int DH>
-static size_t smem_bytes(int B) {
-  return SmemLayout<FMT, DH>::total(B);
+static size_t smem_bytes(int G, int B, int Hkv) {
+  return SmemLayout<FMT, DH>::total(G, B, Hkv);
 }
 
 template <int FMT, int DH>
 static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                   cudaStream_t s) {
-  const size_t smem = smem_bytes<FMT, DH>(p.B);
+  const size_t smem = smem_bytes<FMT, DH>(p.G, p.B, p.Hkv);
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    const size_t maxsmem = smem_bytes<FMT, DH>(kMaxSeqs);
+    const size_t maxsmem = smem_bytes<FMT, DH>(kMaxGroup, kMaxSeqs, kMaxKvHeads);
     if (cudaFuncSetAttribute(decode_kernel<FMT, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(maxsmem)) != cudaSuccess)
       return KVQ_ERR_CUDA;
@@ -812,7 +938,9 @@ static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMa
   }
   decode_kernel<FMT, DH><<<p.P, kThreads, smem, s>>>(p, tk, tv);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-  reduce_kernel<DH><<<p.B * p.Hkv, 128, 0, s>>>(p);
+  const int red_threads = ((p.G * DH + 31) / 32) * 32;
+  const size_t red_smem = (static_cast<size_t>(p.P) * p.G + 2 * p.G) * sizeof(float);
+  reduce_kernel<DH><<<p.B * p.Hkv, red_threads, red_smem, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -855,7 +983,7 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   if (block_size != kBS) return KVQ_ERR_UNSUPPORTED;
   if (num_q_heads % num_kv_heads) return KVQ_ERR_SHAPE;
   const int G = num_q_heads / num_kv_heads;
-  if (G > kMaxGroup) return KVQ_ERR_UNSUPPORTED;
+  if (G > kMaxGroup || num_kv_heads > kMaxKvHeads) return KVQ_ERR_UNSUPPORTED;
   if (num_seqs > kMaxSeqs) return KVQ_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * num_kv_heads >= (int64_t(1) << 31))
     return KVQ_ERR_UNSUPPORTED;
