@@ -88,6 +88,14 @@ KVQ_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// ------------------------------------------------------------------ PDL
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream drains;
+// it must wait for that kernel's completion (and memory) before touching any
+// data another kernel may have written.
+KVQ_DEVI void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+KVQ_DEVI void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 
 KVQ_DEVI void tma_prefetch_desc(const CUtensorMap* map) {

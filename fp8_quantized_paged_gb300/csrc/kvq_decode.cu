@@ -59,6 +59,7 @@ constexpr int kRingBytes = KVQ_RING_KB * 1024;
 constexpr int kMaxSeqs = 4096;
 constexpr int kMaxGroup = 8;
 constexpr int kMaxKvHeads = 256;
+constexpr int kMaxSegments = 65536;  // num_seqs * num_kv_heads (counter table entries)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazily rescale O
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
@@ -120,7 +121,7 @@ struct DecodeParams {
   int per_head;
   int P;
   float logit_scale;  // log2(e) / sqrt(dh)
-  int32_t* ws_seq_off;
+  uint32_t* ws_cnt;  // [B * Hkv] arrivals of the pieces of each segment (zero between calls)
   float* ws_ml;
   float* ws_o;
   uint16_t* out;
@@ -129,11 +130,14 @@ struct DecodeParams {
   int64_t n_slots;  // partial slots in the workspace
 };
 
-// Workspace: [B+1] int32 unit offsets, then per partial slot (m, l) pairs and
-// o vectors for the G heads of a group.  Partial slot of the piece of segment
-// sigma = b * Hkv + g held by CTA c is c + sigma (unique: ranges are ordered).
+// Workspace: a table of kMaxSegments uint32 arrival counters, one per
+// (sequence, KV head) segment (zero before the first call, left zero by
+// every completed call), then per partial slot the (m, l) pairs
+// and o vectors for the G heads of a group.  The partial slot of the piece of
+// segment sigma = b * Hkv + g held by CTA c is c + sigma (unique: CTA ranges
+// are ordered).
 struct WsLayout {
-  size_t seq_off, ml, o, total;
+  size_t cnt, ml, o, total;
 };
 
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -141,8 +145,8 @@ static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 static WsLayout ws_layout(int B, int G, int Hkv, int DH, int P) {
   WsLayout w;
   const size_t slots = static_cast<size_t>(P) + static_cast<size_t>(B) * Hkv;
-  w.seq_off = 0;
-  w.ml = round256(sizeof(int32_t) * (static_cast<size_t>(B) + 1));
+  w.cnt = 0;  // a fixed-size table, so every batch shape reuses the same zeroed counters
+  w.ml = round256(sizeof(uint32_t) * static_cast<size_t>(kMaxSegments));
   w.o = w.ml + round256(slots * G * 2 * sizeof(float));
   w.total = w.o + round256(slots * G * DH * sizeof(float));
   return w;
@@ -500,6 +504,66 @@ KVQ_DEVI void q_fragments(const uint32_t (&w)[DH / 8], uint32_t (&qb)[DH / 16][2
 
 KVQ_DEVI uint16_t to_bf16(float x) { return static_cast<uint16_t>(f32x2_to_bf16x2(x, 0.f)); }
 
+// Merge of the partial states of a segment split across CTAs, run by the
+// consumer threads of the CTA that completed the segment's last piece.  The
+// per-piece weights 2^(m - M) and the denominators are formed once in shared
+// memory (reusing the warps' merge scratch); the o loads of the pieces are
+// independent, so they pipeline.
+//   M = max_c m_c,  l = sum_c l_c 2^(m_c - M),  O = sV sum_c o_c 2^(m_c - M) / l
+template <int DH>
+KVQ_DEVI void merge_segment(const DecodeParams& p, int b, int gkv, int64_t sigma, int64_t c_lo,
+                            int n, float sv, float* wgt, float* hl, int ctid) {
+  const int G = p.G;
+  constexpr int NT = kConsumerWarps * 32;
+  uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + gkv * G) * DH;
+  if (!guard(c_lo >= 0 && c_lo + n - 1 + sigma < p.n_slots && n * G <= kConsumerWarps * G * DH,
+             p.status, 5))
+    return;
+  float* Mh = hl;      // [G]
+  float* Lh = hl + G;  // [G]
+  const float* ml = p.ws_ml + ((c_lo + sigma) * G) * 2;
+  for (int i = ctid; i < n * G; i += NT) wgt[i] = __ldcg(ml + 2 * i);
+  if (ctid < G) Lh[ctid] = 0.f;
+  consumer_bar();
+  if (ctid < G) {
+    float M = -INFINITY;
+    for (int c = 0; c < n; ++c) M = fmaxf(M, wgt[c * G + ctid]);
+    Mh[ctid] = M;
+  }
+  consumer_bar();
+  for (int i = ctid; i < n * G; i += NT) {
+    const int h = i % G;
+    const float m = wgt[i], M = Mh[h];
+    const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
+    wgt[i] = w;
+    atomicAdd(&Lh[h], __ldcg(ml + 2 * i + 1) * w);
+  }
+  consumer_bar();
+  // one float4 of outputs per thread; 16 pieces' loads in flight
+  const float4* ob = reinterpret_cast<const float4*>(p.ws_o + (c_lo + sigma) * G * DH);
+  const int n4 = G * DH / 4;
+  for (int q4 = ctid; q4 < n4; q4 += NT) {
+    const int h = (4 * q4) / DH;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 16
+    for (int c = 0; c < n; ++c) {
+      const float w = wgt[c * G + h];
+      const float4 v = __ldcg(ob + static_cast<int64_t>(c) * n4 + q4);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    const float ls = Lh[h];
+    const float f = ls > 0.f ? sv / ls : 0.f;
+    uint2 packed;
+    packed.x = f32x2_to_bf16x2(acc.x * f, acc.y * f);
+    packed.y = f32x2_to_bf16x2(acc.z * f, acc.w * f);
+    *reinterpret_cast<uint2*>(out + 4 * q4) = packed;
+  }
+  consumer_bar();
+}
+
 // --------------------------------------------------------------------------
 // Decode kernel
 // --------------------------------------------------------------------------
@@ -520,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   uint64_t* empty = full + S;
   uint32_t* bad_s = reinterpret_cast<uint32_t*>(smem + SL::flags);
   volatile uint32_t* abort_flag = bad_s + S;
+  volatile uint32_t* merge_s = bad_s + S + 1;
   int32_t* warp_tot = reinterpret_cast<int32_t*>(bad_s + S + 2);  // [8]
   int32_t* last_s = warp_tot + 8;  // [S] last position issued into each slot
   float* cm = reinterpret_cast<float*>(smem + SL::comb);   // [warps][G] running max
@@ -544,11 +609,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
+  pdl_allow_next();
+  pdl_wait();  // inputs (caches, q, tables, lengths) may come from the previous kernel
   build_plan<FMT != KVQ_FMT_BF16>(p, seq_off, len_s, sk_s, sv_s, warp_tot);  // has __syncthreads
 
   const int64_t W = seq_off[p.B];
-  if (blockIdx.x == 0)
-    for (int b = tid; b <= p.B; b += kThreads) p.ws_seq_off[b] = seq_off[b];
+  // Sequences with nothing to attend to get a zero output row (CTAs share them).
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    if (seq_off[b + 1] != seq_off[b]) continue;
+    uint16_t* row = p.out + static_cast<int64_t>(b) * p.Hq * DH;
+    for (int i = tid; i < p.Hq * DH; i += kThreads) row[i] = 0;
+  }
   // Effective partition size: never more CTAs than units, so every CTA of the
   // partition owns at least one unit (the reduce relies on it); the others idle.
   const int64_t Pe = W < p.P ? W : p.P;
@@ -804,6 +875,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         }
       }
       consumer_bar();
+      if (!single) {
+        // Publish this piece; the CTA whose piece completes the segment merges
+        // all of its pieces and resets the segment's counter.
+        const int64_t sigma = static_cast<int64_t>(b) * p.Hkv + gkv;
+        const int64_t us = seq_off[b] + static_cast<int64_t>(gkv) * pages, ue = us + pages;
+        const int64_t c_lo = ((us + 1) * Pe + W - 1) / W - 1;  // CTA holding unit us
+        const int64_t c_hi = (ue * Pe + W - 1) / W - 1;        // CTA holding unit ue - 1
+        const int npieces = static_cast<int>(c_hi - c_lo + 1);
+        __threadfence();
+        consumer_bar();
+        if (ctid == 0) {
+          const uint32_t prev = atomicAdd(p.ws_cnt + sigma, 1u);
+          merge_s[0] = (prev + 1 == static_cast<uint32_t>(npieces)) ? 1u : 0u;
+        }
+        consumer_bar();
+        if (merge_s[0]) {
+          __threadfence();
+          merge_segment<DH>(p, b, gkv, sigma, c_lo, npieces, sv, co, cm, ctid);
+          if (ctid == 0) p.ws_cnt[sigma] = 0u;
+        }
+      }
       pos_base += n;
       u += n;
     }
@@ -813,67 +905,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   if (*abort_flag && tid == 0) {
     for (int s = 0; s < S; ++s)
       if (last_s[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>((last_s[s] / S) & 1));
-  }
-}
-
-// Merge of the partial states of segments split across CTAs: one CTA per
-// (sequence, KV head), one thread per (head, dim).  The per-piece weights
-// 2^(m - M) and the denominators are formed once in shared memory; the o
-// loads of the pieces are independent, so they pipeline.
-template <int DH>
-__global__ void __launch_bounds__(1024) reduce_kernel(const DecodeParams p) {
-  extern __shared__ float red_smem[];
-  const int b = blockIdx.x / p.Hkv, gkv = blockIdx.x - b * p.Hkv;
-  const int tid = threadIdx.x, G = p.G;
-  const int64_t W = p.ws_seq_off[p.B];
-  const int64_t so = p.ws_seq_off[b];
-  const int pages = (p.ws_seq_off[b + 1] - p.ws_seq_off[b]) / p.Hkv;
-  uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + gkv * G) * DH;
-  if (pages == 0) {
-    for (int idx = tid; idx < G * DH; idx += blockDim.x) out[idx] = 0;
-    return;
-  }
-  const int64_t us = so + static_cast<int64_t>(gkv) * pages, ue = us + pages;
-  // CTAs c < Pe own [floor(c W / Pe), floor((c+1) W / Pe)), all non-empty;
-  // the CTA holding unit u is ceil((u+1) Pe / W) - 1.
-  const int64_t Pe = W < p.P ? W : p.P;
-  const int64_t c_lo = ((us + 1) * Pe + W - 1) / W - 1;
-  const int64_t c_hi = (ue * Pe + W - 1) / W - 1;
-  if (c_lo == c_hi) return;  // one CTA held the whole segment and wrote it
-  const int64_t sigma = static_cast<int64_t>(b) * p.Hkv + gkv;
-  if (!guard(c_lo >= 0 && c_hi < Pe && c_lo <= c_hi && c_hi + sigma < p.n_slots, p.status, 5))
-    return;
-  const int n = static_cast<int>(c_hi - c_lo + 1);
-  float* wgt = red_smem;        // [n][G]: m, then the weight 2^(m - M)
-  float* Mh = wgt + n * G;      // [G]
-  float* Lh = Mh + G;           // [G]
-  const float* ml = p.ws_ml + ((c_lo + sigma) * G) * 2;
-  for (int i = tid; i < n * G; i += blockDim.x) wgt[i] = ml[2 * i];
-  if (tid < G) Lh[tid] = 0.f;
-  __syncthreads();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int c = 0; c < n; ++c) M = fmaxf(M, wgt[c * G + tid]);
-    Mh[tid] = M;
-  }
-  __syncthreads();
-  for (int i = tid; i < n * G; i += blockDim.x) {
-    const int h = i % G;
-    const float m = wgt[i], M = Mh[h];
-    const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
-    wgt[i] = w;
-    atomicAdd(&Lh[h], ml[2 * i + 1] * w);
-  }
-  __syncthreads();
-  const float sv = (p.vs == nullptr) ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
-  const float* ob = p.ws_o + (c_lo + sigma) * G * DH;
-  for (int idx = tid; idx < G * DH; idx += blockDim.x) {
-    const int h = idx / DH;
-    float acc = 0.f;
-#pragma unroll 8
-    for (int c = 0; c < n; ++c) acc += wgt[c * G + h] * ob[static_cast<int64_t>(c) * G * DH + idx];
-    const float ls = Lh[h];
-    out[idx] = to_bf16(ls > 0.f ? acc / ls * sv : 0.f);
   }
 }
 
@@ -936,11 +967,9 @@ static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMa
       return KVQ_ERR_CUDA;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  decode_kernel<FMT, DH><<<p.P, kThreads, smem, s>>>(p, tk, tv);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-  const int red_threads = ((p.G * DH + 31) / 32) * 32;
-  const size_t red_smem = (static_cast<size_t>(p.P) * p.G + 2 * p.G) * sizeof(float);
-  reduce_kernel<DH><<<p.B * p.Hkv, red_threads, red_smem, s>>>(p);
+  if (launch_pdl(decode_kernel<FMT, DH>, dim3(p.P), dim3(kThreads), smem, s, p, tk, tv) !=
+      cudaSuccess)
+    return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -984,7 +1013,7 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   if (num_q_heads % num_kv_heads) return KVQ_ERR_SHAPE;
   const int G = num_q_heads / num_kv_heads;
   if (G > kMaxGroup || num_kv_heads > kMaxKvHeads) return KVQ_ERR_UNSUPPORTED;
-  if (num_seqs > kMaxSeqs) return KVQ_ERR_UNSUPPORTED;
+  if (num_seqs > kMaxSeqs || num_seqs * num_kv_heads > kMaxSegments) return KVQ_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * num_kv_heads >= (int64_t(1) << 31))
     return KVQ_ERR_UNSUPPORTED;
   if (num_blocks * num_kv_heads * kBS >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
@@ -1026,7 +1055,7 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   p.P = P;
   p.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.ws_seq_off = reinterpret_cast<int32_t*>(ws + wl.seq_off);
+  p.ws_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt);
   p.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
   p.ws_o = reinterpret_cast<float*>(ws + wl.o);
   p.out = static_cast<uint16_t*>(out);

@@ -1,6 +1,7 @@
 // kvq_host.h -- host-side helpers shared by the entry points of libkvq.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace kvq {
@@ -9,5 +10,23 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // SM count of the current device (cached per device); 0 if no device.
 int device_sm_count();
+
+// Launch with programmatic stream serialization (the kernel must call
+// griddepcontrol.wait before reading data written by earlier kernels).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 }  // namespace kvq

@@ -57,6 +57,8 @@ KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, float s) {
 
 template <int FMT>
 __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
+  pdl_allow_next();
+  pdl_wait();  // k, v, slots may come from the previous kernel
   const int chunks = p.dh >> 4;
   const int64_t units = p.num_tokens * p.hkv * chunks;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -111,6 +113,8 @@ struct DequantParams {
 // product with the head's scale, RNE to bf16.
 template <int FMT>
 __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
+  pdl_allow_next();
+  pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < p.units;
        u += stride) {
@@ -192,11 +196,13 @@ extern "C" int kvq_write(const void* k, const void* v, int64_t token_stride,
   const int64_t units = num_tokens * num_kv_heads * (head_dim / 16);
   const int grid = grid_for(units, 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
   switch (fmt) {
-    case KVQ_FMT_E4M3: write_kernel<KVQ_FMT_E4M3><<<grid, 256, 0, s>>>(p); break;
-    case KVQ_FMT_E5M2: write_kernel<KVQ_FMT_E5M2><<<grid, 256, 0, s>>>(p); break;
-    default: write_kernel<KVQ_FMT_BF16><<<grid, 256, 0, s>>>(p); break;
+    case KVQ_FMT_E4M3: e = launch_pdl(write_kernel<KVQ_FMT_E4M3>, dim3(grid), dim3(256), 0, s, p); break;
+    case KVQ_FMT_E5M2: e = launch_pdl(write_kernel<KVQ_FMT_E5M2>, dim3(grid), dim3(256), 0, s, p); break;
+    default: e = launch_pdl(write_kernel<KVQ_FMT_BF16>, dim3(grid), dim3(256), 0, s, p); break;
   }
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -225,9 +231,10 @@ extern "C" int kvq_dequant_cache(const void* src, void* dst_bf16, int64_t num_bl
   p.per_head = scale_granularity == KVQ_SCALE_PER_HEAD;
   const int grid = grid_for(p.units, 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (fmt == KVQ_FMT_E4M3)
-    dequant_kernel<KVQ_FMT_E4M3><<<grid, 256, 0, s>>>(p);
-  else
-    dequant_kernel<KVQ_FMT_E5M2><<<grid, 256, 0, s>>>(p);
+  const cudaError_t e =
+      fmt == KVQ_FMT_E4M3
+          ? launch_pdl(dequant_kernel<KVQ_FMT_E4M3>, dim3(grid), dim3(256), 0, s, p)
+          : launch_pdl(dequant_kernel<KVQ_FMT_E5M2>, dim3(grid), dim3(256), 0, s, p);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -95,6 +95,11 @@ typedef enum {
 #define KVQ_DEV_INTERNAL 16u    /* an internal index guard failed (bits 16..31 name it); */
                                 /* the access was skipped and the output is invalid      */
 
+/* Bytes at the start of every decode workspace that must be zero before the
+ * first call: the arrival counters of kvq_decode_attn, one 32-bit word per
+ * (sequence, KV head), in a fixed-size table whatever the batch shape. */
+#define KVQ_WS_COUNTER_BYTES ((size_t)65536 * 4u)
+
 /* Flags of kvq_decode_attn. */
 #define KVQ_Q_FP8 1u /* reserved: FP8-domain attention with Q quantized; not built */
 
@@ -160,15 +165,20 @@ KVQ_API size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_
  *   flags           0 (KVQ_Q_FP8 returns KVQ_ERR_UNSUPPORTED).
  *   workspace       device scratch of at least
  *                   kvq_decode_workspace_size(num_seqs, ...) bytes, 256-byte
- *                   aligned.  Contents need no initialisation and are
- *                   overwritten; one workspace must not be shared by calls
- *                   that may run concurrently.
+ *                   aligned.  Its first KVQ_WS_COUNTER_BYTES bytes are
+ *                   per-(sequence, KV head) arrival counters: zero them
+ *                   once before the first call (for
+ *                   instance cudaMemsetAsync of the whole buffer); every
+ *                   completed call leaves them zero again (re-zero after a
+ *                   KVQ_DEV_WAIT_TIMEOUT).  The rest needs no initialisation.
+ *                   One workspace must not be shared by calls that may run
+ *                   concurrently.
  *   out             bf16 [num_seqs][num_q_heads][head_dim] (fp32
  *                   accumulation, round to nearest even).
  *   dev_status      optional; KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN,
  *                   KVQ_DEV_WAIT_TIMEOUT.
- * Limits: num_seqs <= 4096; num_seqs * max_blocks_per_seq * num_kv_heads
- * < 2^31.
+ * Limits: num_seqs <= 4096; num_seqs * num_kv_heads <= 65536;
+ * num_seqs * max_blocks_per_seq * num_kv_heads < 2^31.
  */
 KVQ_API int kvq_decode_attn(const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
@@ -200,10 +210,13 @@ KVQ_API int kvq_decode_attn(const void* q, const void* k_cache, const void* v_ca
  * The first call on a device, made with that device current, looks up the
  * array's device address (cudaGetSymbolAddress) and keeps it; make that
  * first call before any stream capture.  All calls on a device share the
- * one array, which keeps the last call's contents (the kernels overwrite
- * whatever they read, so nothing needs clearing).  Calls that may overlap
- * on the GPU (different streams, or different host threads) race on it:
- * serialize them, or give each its own workspace through kvq_decode_attn.
+ * one array, which keeps the last call's contents.  Its counters start at
+ * zero (device variables are zero-initialized when the library's device
+ * code is loaded) and every completed call leaves them zero, so nothing
+ * needs clearing unless a call reported KVQ_DEV_WAIT_TIMEOUT.  Calls that
+ * may overlap on the GPU (different streams, or different host threads)
+ * race on it: serialize them, or give each its own workspace through
+ * kvq_decode_attn.
  */
 #define KVQ_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 KVQ_API int kvq_decode_attn_static(const void* q, const void* k_cache, const void* v_cache,

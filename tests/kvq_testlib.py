@@ -68,8 +68,14 @@ class DeviceLayer:
         self.vc.view(torch.uint8).fill_(fill)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.ws = kvq.new_workspace(lay.B, lay.Hq, lay.Hkv, lay.dh, dev)
-        self.ws.fill_(0xFF)  # NaN bytes: a read of a slot nobody wrote shows up
+        self.poison_workspace()
         self.out = torch.empty((lay.B, lay.Hq, lay.dh), dtype=torch.bfloat16, device=dev)
+
+    def poison_workspace(self):
+        """NaN bytes everywhere but the counters (which must stay zero), so a
+        read of a partial slot nobody wrote shows up."""
+        self.ws.fill_(0xFF)
+        self.ws[: self.kvq.KVQ_WS_COUNTER_BYTES].zero_()
 
     def write(self, token_idx=None):
         lay = self.lay

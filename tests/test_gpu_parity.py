@@ -318,4 +318,4 @@ def test_decode_fewer_units_than_ctas(kvq, lens, fmt):
         got = bf16_out_to_f64(d.decode())
         assert d.status_word() == 0
         check_attention(got, oracle_decode(lay, K, V), f"lens={lens}")
-        d.ws.fill_(0xFF)
+        d.poison_workspace()
