@@ -36,25 +36,44 @@ struct WriteParams {
   int64_t cache_elems;  // elements of one cache tensor
 };
 
+// x / s, correctly rounded (IEEE binary32), for a scale s whose reciprocal
+// r = RN(1/s) and the residuals below stay normal (s in [2^-80, 2^80]): one
+// product and one fused residual correction (Markstein's iteration)
+// q0 = RN(x r), e = RN(x - q0 s), q = RN(q0 + e r).  Exhaustively checked
+// against IEEE division for every bf16 significand and every binary32 scale
+// significand.  e == 0 means q0 is exact (this also keeps the sign of zero);
+// |q0| >= 2^20 saturates every FP8 format, so q0 is kept there (and an
+// infinite or NaN x passes through).  Quotients too small for the residual to
+// stay normal encode to a signed FP8 zero either way.
+KVQ_DEVI float div_by_scale(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-q0, s, x);
+  return (e == 0.f || !(fabsf(q0) < 1048576.f)) ? q0 : __fmaf_rn(e, r, q0);
+}
+
+KVQ_DEVI bool scale_is_nice(float s) { return s >= 0x1p-80f && s <= 0x1p80f; }
+
 // Sixteen bf16 values (two uint4) -> sixteen FP8 codes: binary32 IEEE
 // quotient x / s (round to nearest even, no flush to zero), then the
 // saturating RNE conversion to FP8.
 template <int FMT>
-KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, float s) {
+KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, float s, float r, bool fast) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float x0 = __fdiv_rn(bf16lo_to_f32(w[2 * i]), s);
-    const float x1 = __fdiv_rn(bf16hi_to_f32(w[2 * i]), s);
-    const float x2 = __fdiv_rn(bf16lo_to_f32(w[2 * i + 1]), s);
-    const float x3 = __fdiv_rn(bf16hi_to_f32(w[2 * i + 1]), s);
-    o[i] = static_cast<uint32_t>(f32x2_to_fp8x2<FMT>(x0, x1)) |
-           (static_cast<uint32_t>(f32x2_to_fp8x2<FMT>(x2, x3)) << 16);
+    float x[4] = {bf16lo_to_f32(w[2 * i]), bf16hi_to_f32(w[2 * i]), bf16lo_to_f32(w[2 * i + 1]),
+                  bf16hi_to_f32(w[2 * i + 1])};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = fast ? div_by_scale(x[j], s, r) : __fdiv_rn(x[j], s);
+    o[i] = static_cast<uint32_t>(f32x2_to_fp8x2<FMT>(x[0], x[1])) |
+           (static_cast<uint32_t>(f32x2_to_fp8x2<FMT>(x[2], x[3])) << 16);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// One thread per 16-element chunk of one (token, KV head) row.  The K/V
+// loads do not depend on the slot, so they are issued before it is checked.
 template <int FMT>
 __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
   pdl_allow_next();
@@ -68,6 +87,12 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
     const int64_t th = u / chunks;
     const int h = static_cast<int>(th % p.hkv);
     const int64_t t = th / p.hkv;
+    const int64_t src = t * p.token_stride + static_cast<int64_t>(h) * p.dh + c * 16;
+    if (!guard(src >= 0 && src + 16 <= p.in_elems, p.status, 7)) continue;
+    const uint4* ksrc = reinterpret_cast<const uint4*>(p.k + src);
+    const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + src);
+    const uint4 ka = __ldcs(ksrc), kb = __ldcs(ksrc + 1);
+    const uint4 va = __ldcs(vsrc), vb = __ldcs(vsrc + 1);
     const int64_t slot = __ldg(p.slots + t);
     if (slot < 0) continue;  // padding token
     if (slot >= p.capacity) {
@@ -75,14 +100,8 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
       continue;
     }
     const int64_t blk = slot / p.bs, off = slot - blk * p.bs;
-    const int64_t src = t * p.token_stride + static_cast<int64_t>(h) * p.dh + c * 16;
     const int64_t dst = ((blk * p.hkv + h) * p.bs + off) * p.dh + c * 16;
-    if (!guard(src >= 0 && src + 16 <= p.in_elems, p.status, 7)) continue;
     if (!guard(dst >= 0 && dst + 16 <= p.cache_elems, p.status, 8)) continue;
-    const uint4* ksrc = reinterpret_cast<const uint4*>(p.k + src);
-    const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + src);
-    const uint4 ka = __ldcs(ksrc), kb = __ldcs(ksrc + 1);
-    const uint4 va = __ldcs(vsrc), vb = __ldcs(vsrc + 1);
     if (FMT == KVQ_FMT_BF16) {
       uint4* kd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.kc) + dst);
       uint4* vd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.vc) + dst);
@@ -93,8 +112,11 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
     } else {
       const float sk = __ldg(p.ks + (p.per_head ? h : 0));
       const float sv = __ldg(p.vs + (p.per_head ? h : 0));
-      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.kc) + dst) = quantize16<FMT>(ka, kb, sk);
-      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.vc) + dst) = quantize16<FMT>(va, vb, sv);
+      const bool fast = scale_is_nice(sk) && scale_is_nice(sv);
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.kc) + dst) =
+          quantize16<FMT>(ka, kb, sk, __frcp_rn(sk), fast);
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.vc) + dst) =
+          quantize16<FMT>(va, vb, sv, __frcp_rn(sv), fast);
     }
   }
 }
@@ -137,9 +159,11 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
   }
 }
 
+// One work unit per thread while the grid stays under 64 waves of the SMs;
+// beyond that the kernels loop (grid-stride).
 static int grid_for(int64_t units, int threads) {
   const int64_t need = (units + threads - 1) / threads;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8 * 64;
   return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
