@@ -340,6 +340,35 @@ KVQ_DEVI void p_fragments(const float* pr, int g, int t, int G, uint32_t (&bh)[2
   bl[1] = live ? (odd ? lb1 : lb0) : 0u;
 }
 
+// Packed variant for groups of at most 4 heads: the PV MMA's 8 columns hold
+// P_hi of heads 0..3 (columns 0..3) and P_lo of heads 0..3 (columns 4..7), so
+// one MMA per m-tile accumulates both parts (summed once per piece).  Q is
+// replicated into columns 4..7 of the QK MMA, so lane (g, t) with t >= 2 holds
+// the same probabilities as lane (g, t - 2) and supplies the lo parts: each
+// destination needs one source lane per token pair (2 shuffles each).
+template <bool BF16P>
+KVQ_DEVI void p_fragments_packed(const float* pr, int g, int t, int G, uint32_t (&b)[2]) {
+  const bool lo_src = t >= 2;
+  uint32_t pk0, pk1;
+  if (BF16P) {
+    const uint32_t h0 = f32x2_to_bf16x2(pr[0], pr[2]), h1 = f32x2_to_bf16x2(pr[1], pr[3]);
+    pk0 = lo_src ? f32x2_to_bf16x2(pr[0] - bf16lo_to_f32(h0), pr[2] - bf16hi_to_f32(h0)) : h0;
+    pk1 = lo_src ? f32x2_to_bf16x2(pr[1] - bf16lo_to_f32(h1), pr[3] - bf16hi_to_f32(h1)) : h1;
+  } else {
+    const uint32_t h0 = f32x2_to_f16x2(pr[0], pr[2]), h1 = f32x2_to_f16x2(pr[1], pr[3]);
+    pk0 = lo_src ? f32x2_to_f16x2(pr[0] - f16lo_to_f32(h0), pr[2] - f16hi_to_f32(h0)) : h0;
+    pk1 = lo_src ? f32x2_to_f16x2(pr[1] - f16lo_to_f32(h1), pr[3] - f16hi_to_f32(h1)) : h1;
+  }
+  const int hh = g & 3;                            // head of this lane's B column
+  const int src = ((hh >> 1) + ((g >> 2) << 1));   // source lane's t: hi (g < 4) or lo part
+  const int srcA = (2 * t) * 4 + src, srcB = (2 * t + 1) * 4 + src;
+  const uint32_t a0 = __shfl_sync(kFull, pk0, srcA), a1 = __shfl_sync(kFull, pk1, srcA);
+  const uint32_t b0 = __shfl_sync(kFull, pk0, srcB), b1 = __shfl_sync(kFull, pk1, srcB);
+  const bool live = hh < G, odd = hh & 1;
+  b[0] = live ? (odd ? a1 : a0) : 0u;
+  b[1] = live ? (odd ? b1 : b0) : 0u;
+}
+
 KVQ_DEVI bool token_valid(int tok, int lo, int L, bool bad) { return !bad && tok >= lo && tok < L; }
 
 
@@ -398,7 +427,7 @@ KVQ_DEVI void load_page(uint32_t kp, uint32_t vp, int g, int t, int tok0, int lo
 //   converted to f16 exactly, or bf16 as is), the group's query heads the B
 //   operand; lane (g, t) covers dims t*(DH/4) + 4kk + {0..3} of step kk.
 //   PV: O^T += V^T P^T with m-tile mt, row r -> dim g*(DH/8) + 2mt + r/8.
-template <int FMT, int DH, int NP>
+template <int FMT, int DH, int NP, bool PK>
 KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[NP],
                             const bool (&bad)[NP], int g, int t, int G,
                             const uint32_t (&qb)[DH / 16][2], float (&o)[DH / 16][4],
@@ -438,7 +467,12 @@ KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[
   softmax_pages<NP, DH / 16>(x, pr, st, o);
   uint32_t bh[NP][2], bl[NP][2];
 #pragma unroll
-  for (int i = 0; i < NP; ++i) p_fragments<BF>(pr + 4 * i, g, t, G, bh[i], bl[i]);
+  for (int i = 0; i < NP; ++i) {
+    if (PK)
+      p_fragments_packed<BF>(pr + 4 * i, g, t, G, bh[i]);
+    else
+      p_fragments<BF>(pr + 4 * i, g, t, G, bh[i], bl[i]);
+  }
 
 #pragma unroll
   for (int w = 0; w < R::VB / 4; ++w) {
@@ -452,7 +486,7 @@ KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[
         const uint32_t a[4] = {prmt(v0[w], v1[w], 0x5410u), prmt(v0[w], v1[w], 0x7632u),
                                prmt(v2[w], v3[w], 0x5410u), prmt(v2[w], v3[w], 0x7632u)};
         mma_bf16(o[w], a, bh[i][0], bh[i][1]);
-        mma_bf16(o[w], a, bl[i][0], bl[i][1]);
+        if (!PK) mma_bf16(o[w], a, bl[i][0], bl[i][1]);
       } else {  // word w = dims g*(DH/8) + 4w .. +3 -> m-tiles 2w, 2w+1
         const uint32_t x0 = prmt(v0[w], v1[w], 0x5140u), y0 = prmt(v0[w], v1[w], 0x7362u);
         const uint32_t z0 = prmt(v2[w], v3[w], 0x5140u), u0 = prmt(v2[w], v3[w], 0x7362u);
@@ -463,8 +497,10 @@ KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[
         fp8x4_to_f16x2x2<FMT>(u0, c[2], c[3]);
         mma_f16(o[2 * w], a, bh[i][0], bh[i][1]);
         mma_f16(o[2 * w + 1], c, bh[i][0], bh[i][1]);
-        mma_f16(o[2 * w], a, bl[i][0], bl[i][1]);
-        mma_f16(o[2 * w + 1], c, bl[i][0], bl[i][1]);
+        if (!PK) {
+          mma_f16(o[2 * w], a, bl[i][0], bl[i][1]);
+          mma_f16(o[2 * w + 1], c, bl[i][0], bl[i][1]);
+        }
       }
     }
   }
@@ -475,11 +511,11 @@ KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[
 // f16 for the FP8 caches (exact for |q| in the f16 normal range), the bf16
 // bits for the bf16 cache.  Rows past the group (g >= G) are zero.
 template <int DH>
-KVQ_DEVI void load_q_raw(const DecodeParams& p, int b, int gkv, int g, int t,
+KVQ_DEVI void load_q_raw(const DecodeParams& p, int b, int gkv, int hq, int t,
                          uint32_t (&w)[DH / 8]) {
-  const int64_t qrow = static_cast<int64_t>(b) * p.Hq + gkv * p.G + g;
-  const bool ok = g < p.G && guard(b >= 0 && b < p.B && qrow < static_cast<int64_t>(p.B) * p.Hq,
-                                   p.status, 2);
+  const int64_t qrow = static_cast<int64_t>(b) * p.Hq + gkv * p.G + hq;
+  const bool ok = hq < p.G && guard(b >= 0 && b < p.B && qrow < static_cast<int64_t>(p.B) * p.Hq,
+                                    p.status, 2);
   const uint4* src = reinterpret_cast<const uint4*>(p.q + (ok ? qrow : 0) * DH + t * (DH / 4));
 #pragma unroll
   for (int i = 0; i < DH / 32; ++i) {
@@ -568,7 +604,7 @@ KVQ_DEVI void merge_segment(const DecodeParams& p, int b, int gkv, int64_t sigma
 // Decode kernel
 // --------------------------------------------------------------------------
 
-template <int FMT, int DH>
+template <int FMT, int DH, bool PK>
 __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
@@ -721,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     // ------------------------------------------------------------ consumers
     const int g = lane >> 2, t = lane & 3;
     const int ctid = tid;  // 0 .. 127
+    const int qhead = PK ? (g & 3) : g;  // query head of this lane's QK column
     uint32_t qb[MT][2];
     uint32_t qraw[DH / 8];  // raw Q words of the current piece, loaded a piece ahead
     float o[MT][4];
@@ -737,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     if (u0 < u1) {
       int b, gkv, pages, p0;
       piece_at(u0, b, gkv, pages, p0);
-      load_q_raw<DH>(p, b, gkv, g, t, qraw);
+      load_q_raw<DH>(p, b, gkv, qhead, t, qraw);
     }
     for (int64_t u = u0; u < u1;) {
       int b, gkv, pages, p0;
@@ -753,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       if (u + n < u1) {  // next piece's Q, in flight while this piece runs
         int nb, ng, npg, np0;
         piece_at(u + n, nb, ng, npg, np0);
-        load_q_raw<DH>(p, nb, ng, g, t, qraw);
+        load_q_raw<DH>(p, nb, ng, qhead, t, qraw);
       }
       SoftmaxState st;
       st.m[0] = st.m[1] = -INFINITY;
@@ -812,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
             for (int i = 0; i < NP; ++i)
               if (have[i]) mbar_arrive(&empty[slot[i]]);
           }
-          compute_pages<FMT, DH, NP>(pr, tok0, bad, g, t, p.G, qb, o, st, lscale, lo, L);
+          compute_pages<FMT, DH, NP, PK>(pr, tok0, bad, g, t, p.G, qb, o, st, lscale, lo, L);
         } else {
           __syncwarp();
           if (lane == 0) {
@@ -824,6 +861,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       }
 
       // ---- merge the four warps' states of this segment piece
+      if (PK) {  // columns 4..7 hold the P_lo contributions of heads 0..3
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[mt][i] += __shfl_xor_sync(kFull, o[mt][i], 2);
+      }
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         st.l[0] += __shfl_xor_sync(kFull, st.l[0], off);
@@ -961,15 +1004,18 @@ static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMa
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    const size_t maxsmem = smem_bytes<FMT, DH>(kMaxGroup, kMaxSeqs, kMaxKvHeads);
-    if (cudaFuncSetAttribute(decode_kernel<FMT, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(maxsmem)) != cudaSuccess)
+    const int maxsmem = static_cast<int>(smem_bytes<FMT, DH>(kMaxGroup, kMaxSeqs, kMaxKvHeads));
+    if (cudaFuncSetAttribute(decode_kernel<FMT, DH, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, maxsmem) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_kernel<FMT, DH, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, maxsmem) != cudaSuccess)
       return KVQ_ERR_CUDA;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  if (launch_pdl(decode_kernel<FMT, DH>, dim3(p.P), dim3(kThreads), smem, s, p, tk, tv) !=
-      cudaSuccess)
-    return KVQ_ERR_CUDA;
+  const cudaError_t e =
+      p.G <= 4 ? launch_pdl(decode_kernel<FMT, DH, true>, dim3(p.P), dim3(kThreads), smem, s, p, tk, tv)
+               : launch_pdl(decode_kernel<FMT, DH, false>, dim3(p.P), dim3(kThreads), smem, s, p, tk, tv);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
