@@ -120,6 +120,19 @@ KVQ_DEVI void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t
       : "memory");
 }
 
+// Untiled bulk copy global -> shared, completion counted in bytes on bar.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+KVQ_DEVI void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses (and what it has
+// acquired from other threads) before its later async-proxy accesses.
+KVQ_DEVI void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 // ------------------------------------------------------------------ MMA (m16n8k16, fp32 accumulate)
 
 KVQ_DEVI void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {

@@ -13,8 +13,9 @@
 //   sequence, head by head, page by page; CTA c of P takes the contiguous
 //   range [floor(c W / P), floor((c+1) W / P)) of the W units, so every CTA
 //   streams the same number of bytes whatever the length mix.  A range cut
-//   through a (b, g) segment leaves partial softmax states (m, l, o) that the
-//   reduce kernel merges; a segment held by one CTA is written directly.
+//   through a (b, g) segment leaves partial softmax states (m, l, o) in the
+//   workspace; the CTA that completes a segment's last piece merges them.
+//   A segment held by one CTA is written directly.
 //
 // Inside a CTA
 //   warp 4 (producer): one lane issues TMA tile loads of the K page and the V
@@ -82,29 +83,33 @@ struct Cfg {
 };
 
 // Dynamic shared memory of the decode kernel (offsets from a 1024-aligned
-// base): the ring and barriers at fixed offsets, then the warps' merge
-// scratch for the group's G heads, the plan ([B+1] unit offsets, [B] checked
-// lengths) and the k/v scales.
+// base): the ring and barriers at fixed offsets, then the merge scratch (the
+// warps' states for the group's G heads, reused for the weights of up to P
+// pieces when a split segment is merged), the plan ([B+1] unit offsets, [B]
+// checked lengths) and the k/v scales.
 template <int FMT, int DH>
 struct SmemLayout {
   using C = Cfg<FMT, DH>;
   static constexpr int S = C::kStages;
   static constexpr size_t ring = 0;
-  static constexpr size_t bars = ring + static_cast<size_t>(S) * C::kSlot;  // full[S], empty[S]
-  // bad[S], abort, spare, tot[8], last[S]
-  static constexpr size_t flags = bars + 2 * S * sizeof(uint64_t);
-  static constexpr size_t comb = (flags + (2 * S + 2 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
-  __host__ __device__ static size_t comb_floats(int G) {
-    return static_cast<size_t>(kConsumerWarps) * G * (DH + 2);
+  // full[S], empty[S], and the barrier of the segment-merge bulk copy
+  static constexpr size_t bars = ring + static_cast<size_t>(S) * C::kSlot;
+  // bad[S], abort, merge decision, tot[8], last[S], merge copy issued
+  static constexpr size_t flags = bars + (2 * S + 1) * sizeof(uint64_t);
+  static constexpr size_t comb = (flags + (2 * S + 3 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
+  __host__ __device__ static size_t comb_floats(int G, int P) {
+    const size_t warps = static_cast<size_t>(kConsumerWarps) * G * (DH + 2);
+    const size_t pieces = (static_cast<size_t>(P) + 1) * G;
+    return warps > pieces ? warps : pieces;
   }
-  __host__ __device__ static size_t seq(int G) {
-    return comb + ((comb_floats(G) * sizeof(float) + 15) & ~size_t(15));
+  __host__ __device__ static size_t seq(int G, int P) {
+    return comb + ((comb_floats(G, P) * sizeof(float) + 15) & ~size_t(15));
   }
-  __host__ __device__ static size_t scales(int G, int B) {
-    return seq(G) + (2 * static_cast<size_t>(B) + 1) * sizeof(int32_t);
+  __host__ __device__ static size_t scales(int G, int P, int B) {
+    return seq(G, P) + (2 * static_cast<size_t>(B) + 1) * sizeof(int32_t);
   }
-  __host__ __device__ static size_t total(int G, int B, int Hkv) {
-    return scales(G, B) + 2 * static_cast<size_t>(Hkv) * sizeof(float) + 1024;
+  __host__ __device__ static size_t total(int G, int P, int B, int Hkv) {
+    return scales(G, P, B) + 2 * static_cast<size_t>(Hkv) * sizeof(float) + 1024;
   }
 };
 
@@ -179,7 +184,9 @@ KVQ_DEVI uint2 lds64(uint32_t addr) {
   return r;
 }
 
-KVQ_DEVI void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
+KVQ_DEVI void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
 
 
 KVQ_DEVI int window_lo(const DecodeParams& p, int L) {
@@ -538,64 +545,102 @@ KVQ_DEVI void q_fragments(const uint32_t (&w)[DH / 8], uint32_t (&qb)[DH / 16][2
   }
 }
 
-KVQ_DEVI uint16_t to_bf16(float x) { return static_cast<uint16_t>(f32x2_to_bf16x2(x, 0.f)); }
-
 // Merge of the partial states of a segment split across CTAs, run by the
-// consumer threads of the CTA that completed the segment's last piece.  The
-// per-piece weights 2^(m - M) and the denominators are formed once in shared
-// memory (reusing the warps' merge scratch); the o loads of the pieces are
-// independent, so they pipeline.
+// consumer threads of the CTA that completed the segment's last piece.
 //   M = max_c m_c,  l = sum_c l_c 2^(m_c - M),  O = sV sum_c o_c 2^(m_c - M) / l
+// Warp w forms M, the weights 2^(m_c - M) (into wgt, [n][G]) and l of heads
+// w, w + 4, ...; then every thread sums a float4 of O over the pieces.  The
+// pieces' o vectors come either from so, a shared-memory copy the caller has
+// started (bulk copy completing on sbar, phase 0), or straight from global
+// memory (independent loads, 16 in flight).
 template <int DH>
 KVQ_DEVI void merge_segment(const DecodeParams& p, int b, int gkv, int64_t sigma, int64_t c_lo,
-                            int n, float sv, float* wgt, float* hl, int ctid) {
+                            int n, float sv, float* wgt, const float* so, uint64_t* sbar,
+                            volatile uint32_t* abort_flag, int ctid) {
   const int G = p.G;
   constexpr int NT = kConsumerWarps * 32;
+  constexpr int KR = 10;  // pieces per lane kept in registers (n <= 320 in one pass)
+  const int lane = ctid & 31, warp = ctid >> 5;
   uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + gkv * G) * DH;
-  if (!guard(c_lo >= 0 && c_lo + n - 1 + sigma < p.n_slots && n * G <= kConsumerWarps * G * DH,
-             p.status, 5))
-    return;
-  float* Mh = hl;      // [G]
-  float* Lh = hl + G;  // [G]
-  const float* ml = p.ws_ml + ((c_lo + sigma) * G) * 2;
-  for (int i = ctid; i < n * G; i += NT) wgt[i] = __ldcg(ml + 2 * i);
-  if (ctid < G) Lh[ctid] = 0.f;
-  consumer_bar();
-  if (ctid < G) {
+  const bool ok = guard(c_lo >= 0 && c_lo + n - 1 + sigma < p.n_slots && n <= p.P, p.status, 5);
+  float* Lh = wgt + static_cast<size_t>(n) * G;  // [G]
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + (c_lo + sigma) * G;
+  for (int h = warp; ok && h < G; h += kConsumerWarps) {
+    float2 v[KR];
     float M = -INFINITY;
-    for (int c = 0; c < n; ++c) M = fmaxf(M, wgt[c * G + ctid]);
-    Mh[ctid] = M;
-  }
-  consumer_bar();
-  for (int i = ctid; i < n * G; i += NT) {
-    const int h = i % G;
-    const float m = wgt[i], M = Mh[h];
-    const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
-    wgt[i] = w;
-    atomicAdd(&Lh[h], __ldcg(ml + 2 * i + 1) * w);
-  }
-  consumer_bar();
-  // one float4 of outputs per thread; 16 pieces' loads in flight
-  const float4* ob = reinterpret_cast<const float4*>(p.ws_o + (c_lo + sigma) * G * DH);
-  const int n4 = G * DH / 4;
-  for (int q4 = ctid; q4 < n4; q4 += NT) {
-    const int h = (4 * q4) / DH;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 16
-    for (int c = 0; c < n; ++c) {
-      const float w = wgt[c * G + h];
-      const float4 v = __ldcg(ob + static_cast<int64_t>(c) * n4 + q4);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int c = lane + 32 * k;
+      v[k] = c < n ? __ldcg(ml + c * G + h) : make_float2(-INFINITY, 0.f);
+      M = fmaxf(M, v[k].x);
     }
-    const float ls = Lh[h];
-    const float f = ls > 0.f ? sv / ls : 0.f;
-    uint2 packed;
-    packed.x = f32x2_to_bf16x2(acc.x * f, acc.y * f);
-    packed.y = f32x2_to_bf16x2(acc.z * f, acc.w * f);
-    *reinterpret_cast<uint2*>(out + 4 * q4) = packed;
+    for (int c = lane + 32 * KR; c < n; c += 32) M = fmaxf(M, __ldcg(ml + c * G + h).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    float L = 0.f;
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int c = lane + 32 * k;
+      if (c < n) {
+        const float w = (v[k].x == -INFINITY) ? 0.f : fast_exp2(v[k].x - M);
+        wgt[c * G + h] = w;
+        L += v[k].y * w;
+      }
+    }
+    for (int c = lane + 32 * KR; c < n; c += 32) {
+      const float2 x = __ldcg(ml + c * G + h);
+      const float w = (x.x == -INFINITY) ? 0.f : fast_exp2(x.x - M);
+      wgt[c * G + h] = w;
+      L += x.y * w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+    if (lane == 0) Lh[h] = L;
+  }
+  consumer_bar();
+  bool staged = so != nullptr;
+  if (staged && !mbar_wait(sbar, 0u)) {
+    staged = false;
+    if (ctid == 0) {
+      *abort_flag = 1u;
+      flag_status(p.status, KVQ_DEV_WAIT_TIMEOUT);
+    }
+  }
+  const int n4 = G * DH / 4;
+  if (ok && (so == nullptr || staged)) {
+    const float4* ob = staged ? reinterpret_cast<const float4*>(so)
+                              : reinterpret_cast<const float4*>(p.ws_o + (c_lo + sigma) * G * DH);
+    for (int q4 = ctid; q4 < n4; q4 += NT) {
+      const int h = (4 * q4) / DH;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (staged) {
+#pragma unroll 8
+        for (int c = 0; c < n; ++c) {
+          const float w = wgt[c * G + h];
+          const float4 v = ob[static_cast<int64_t>(c) * n4 + q4];
+          acc.x += w * v.x;
+          acc.y += w * v.y;
+          acc.z += w * v.z;
+          acc.w += w * v.w;
+        }
+      } else {
+#pragma unroll 16
+        for (int c = 0; c < n; ++c) {
+          const float w = wgt[c * G + h];
+          const float4 v = __ldcg(ob + static_cast<int64_t>(c) * n4 + q4);
+          acc.x += w * v.x;
+          acc.y += w * v.y;
+          acc.z += w * v.z;
+          acc.w += w * v.w;
+        }
+      }
+      const float ls = Lh[h];
+      const float f = ls > 0.f ? sv / ls : 0.f;
+      uint2 packed;
+      packed.x = f32x2_to_bf16x2(acc.x * f, acc.y * f);
+      packed.y = f32x2_to_bf16x2(acc.z * f, acc.w * f);
+      *reinterpret_cast<uint2*>(out + 4 * q4) = packed;
+    }
   }
   consumer_bar();
 }
@@ -623,22 +668,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   volatile uint32_t* merge_s = bad_s + S + 1;
   int32_t* warp_tot = reinterpret_cast<int32_t*>(bad_s + S + 2);  // [8]
   int32_t* last_s = warp_tot + 8;  // [S] last position issued into each slot
+  volatile uint32_t* mcopy_s = reinterpret_cast<volatile uint32_t*>(last_s + S);  // merge copy issued
+  uint64_t* mbar = empty + S;  // completion of the segment-merge bulk copy
   float* cm = reinterpret_cast<float*>(smem + SL::comb);   // [warps][G] running max
   float* cl = cm + kConsumerWarps * p.G;                   // [warps][G] denominators
   float* co = cl + kConsumerWarps * p.G;                   // [warps][G][DH] unnormalised O
-  int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq(p.G));  // [B+1]
+  int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq(p.G, p.P));  // [B+1]
   int32_t* len_s = seq_off + p.B + 1;                                  // [B]
-  float* sk_s = reinterpret_cast<float*>(smem + SL::scales(p.G, p.B)); // [Hkv]
+  float* sk_s = reinterpret_cast<float*>(smem + SL::scales(p.G, p.P, p.B)); // [Hkv]
   float* sv_s = sk_s + p.Hkv;                                          // [Hkv]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
+  static_assert(S < kThreads, "one thread per ring slot initialises its barriers");
+  if (tid < S) {
+    mbar_init(&full[tid], 1);
+    mbar_init(&empty[tid], 1);
+    last_s[tid] = -1;
+    fence_mbar_init();
+  } else if (tid == S) {
+    mbar_init(mbar, 1);
+    *mcopy_s = 0u;
     *abort_flag = 0u;
-    for (int s = 0; s < S; ++s) last_s[s] = -1;
     fence_mbar_init();
   }
   if (warp == kConsumerWarps && lane == 0) {
@@ -889,32 +939,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       consumer_bar();
       const bool single = (p0 == 0 && n == pages);
       const int64_t slot_idx = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(b) * p.Hkv + gkv;
-      for (int idx = ctid; idx < p.G * DH; idx += kConsumerWarps * 32) {
-        const int h = idx / DH, d = idx - h * DH;
-        float M = -INFINITY;
+      // Each thread combines four consecutive dims of one head: the four
+      // warps' weights 2^(m_w - M) once, then float4 rows of O.
+      for (int q4 = ctid; q4 < p.G * (DH / 4); q4 += kConsumerWarps * 32) {
+        const int h = q4 / (DH / 4), d = 4 * q4 - h * DH;
+        float mw[kConsumerWarps], M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * p.G + h]);
-        float acc = 0.f, ls = 0.f;
-        if (M != -INFINITY) {
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          mw[w] = cm[w * p.G + h];
+          M = fmaxf(M, mw[w]);
+        }
+        float ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = cm[w * p.G + h];
-            const float sc = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-            acc += co[(w * p.G + h) * DH + d] * sc;
-            ls += cl[w * p.G + h] * sc;
-          }
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float sc = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+          const float4 v = *reinterpret_cast<const float4*>(co + (w * p.G + h) * DH + d);
+          ls += cl[w * p.G + h] * sc;
+          acc.x += v.x * sc;
+          acc.y += v.y * sc;
+          acc.z += v.z * sc;
+          acc.w += v.w * sc;
         }
         if (single) {
-          const float val = ls > 0.f ? acc / ls * sv : 0.f;
+          const float f = ls > 0.f ? sv / ls : 0.f;
           const int64_t oi = (static_cast<int64_t>(b) * p.Hq + gkv * p.G + h) * DH + d;
-          if (guard(oi >= 0 && oi < static_cast<int64_t>(p.B) * p.Hq * DH, p.status, 3))
-            p.out[oi] = to_bf16(val);
-        } else if (guard(slot_idx >= 0 && slot_idx < p.n_slots, p.status, 4)) {
-          p.ws_o[(slot_idx * p.G + h) * DH + d] = acc;
-          if (d == 0) {
-            p.ws_ml[(slot_idx * p.G + h) * 2] = M;
-            p.ws_ml[(slot_idx * p.G + h) * 2 + 1] = ls;
+          if (guard(oi >= 0 && oi + 4 <= static_cast<int64_t>(p.B) * p.Hq * DH, p.status, 3)) {
+            uint2 packed;
+            packed.x = f32x2_to_bf16x2(acc.x * f, acc.y * f);
+            packed.y = f32x2_to_bf16x2(acc.z * f, acc.w * f);
+            *reinterpret_cast<uint2*>(p.out + oi) = packed;
           }
+        } else if (guard(slot_idx >= 0 && slot_idx < p.n_slots, p.status, 4)) {
+          *reinterpret_cast<float4*>(p.ws_o + (slot_idx * p.G + h) * DH + d) = acc;
+          if (d == 0)
+            *reinterpret_cast<float2*>(p.ws_ml + (slot_idx * p.G + h) * 2) = make_float2(M, ls);
         }
       }
       consumer_bar();
@@ -926,16 +985,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         const int64_t c_lo = ((us + 1) * Pe + W - 1) / W - 1;  // CTA holding unit us
         const int64_t c_hi = (ue * Pe + W - 1) / W - 1;        // CTA holding unit ue - 1
         const int npieces = static_cast<int>(c_hi - c_lo + 1);
-        __threadfence();
-        consumer_bar();
+        // The barrier above orders every thread's partial stores before
+        // thread 0's fence and arrival (release); the arrival that completes
+        // the count is followed by a fence (acquire) and the barrier below.
         if (ctid == 0) {
+          __threadfence();
           const uint32_t prev = atomicAdd(p.ws_cnt + sigma, 1u);
-          merge_s[0] = (prev + 1 == static_cast<uint32_t>(npieces)) ? 1u : 0u;
+          const bool last = prev + 1 == static_cast<uint32_t>(npieces);
+          if (last) __threadfence();
+          merge_s[0] = last ? 1u : 0u;
         }
         consumer_bar();
         if (merge_s[0]) {
-          __threadfence();
-          merge_segment<DH>(p, b, gkv, sigma, c_lo, npieces, sv, co, cm, ctid);
+          // After the CTA's last piece the ring is idle (every issued page
+          // has been consumed): the pieces' o vectors are bulk-copied into it
+          // while the weights are formed.
+          const uint32_t pbytes = static_cast<uint32_t>(p.G * DH * sizeof(float));
+          const bool stage = (u + n == u1) && !*abort_flag && c_lo >= 0 && npieces <= p.P &&
+                             c_lo + sigma + npieces <= p.n_slots &&
+                             static_cast<size_t>(npieces) * pbytes <= static_cast<size_t>(S) * C::kSlot;
+          if (stage && warp == 0) {
+            if (lane == 0) {
+              *mcopy_s = 1u;
+              mbar_arrive_expect_tx(mbar, npieces * pbytes);
+            }
+            __syncwarp();
+            fence_proxy_async();
+            const float* src = p.ws_o + (c_lo + sigma) * p.G * DH;
+            for (int c = lane; c < npieces; c += 32)
+              bulk_load(ring + static_cast<size_t>(c) * pbytes, src + static_cast<size_t>(c) * p.G * DH,
+                        pbytes, mbar);
+          }
+          merge_segment<DH>(p, b, gkv, sigma, c_lo, npieces, sv, cm,
+                            stage ? reinterpret_cast<const float*>(ring) : nullptr, mbar, abort_flag,
+                            ctid);
           if (ctid == 0) p.ws_cnt[sigma] = 0u;
         }
       }
@@ -948,6 +1031,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   if (*abort_flag && tid == 0) {
     for (int s = 0; s < S; ++s)
       if (last_s[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>((last_s[s] / S) & 1));
+    if (*mcopy_s) mbar_wait(mbar, 0u);
   }
 }
 
@@ -992,19 +1076,19 @@ static bool make_cache_map(CUtensorMap* m, const void* base, int fmt, int dh, ui
 }
 
 template <int FMT, int DH>
-static size_t smem_bytes(int G, int B, int Hkv) {
-  return SmemLayout<FMT, DH>::total(G, B, Hkv);
+static size_t smem_bytes(int G, int P, int B, int Hkv) {
+  return SmemLayout<FMT, DH>::total(G, P, B, Hkv);
 }
 
 template <int FMT, int DH>
 static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                   cudaStream_t s) {
-  const size_t smem = smem_bytes<FMT, DH>(p.G, p.B, p.Hkv);
+  const size_t smem = smem_bytes<FMT, DH>(p.G, p.P, p.B, p.Hkv);
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    const int maxsmem = static_cast<int>(smem_bytes<FMT, DH>(kMaxGroup, kMaxSeqs, kMaxKvHeads));
+    const int maxsmem = static_cast<int>(smem_bytes<FMT, DH>(kMaxGroup, kCtasPerSM * device_sm_count(), kMaxSeqs, kMaxKvHeads));
     if (cudaFuncSetAttribute(decode_kernel<FMT, DH, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, maxsmem) != cudaSuccess ||
         cudaFuncSetAttribute(decode_kernel<FMT, DH, false>,

@@ -26,8 +26,7 @@ struct WriteParams {
   int dh;
   void* kc;
   void* vc;
-  int64_t capacity;  // num_blocks * block_size
-  int bs;
+  int64_t capacity;  // num_blocks * 16 (block_size is 16)
   const float* ks;
   const float* vs;
   int per_head;
@@ -36,88 +35,148 @@ struct WriteParams {
   int64_t cache_elems;  // elements of one cache tensor
 };
 
-// x / s, correctly rounded (IEEE binary32), for a scale s whose reciprocal
-// r = RN(1/s) and the residuals below stay normal (s in [2^-80, 2^80]): one
-// product and one fused residual correction (Markstein's iteration)
-// q0 = RN(x r), e = RN(x - q0 s), q = RN(q0 + e r).  Exhaustively checked
-// against IEEE division for every bf16 significand and every binary32 scale
-// significand.  e == 0 means q0 is exact (this also keeps the sign of zero);
-// |q0| >= 2^20 saturates every FP8 format, so q0 is kept there (and an
-// infinite or NaN x passes through).  Quotients too small for the residual to
-// stay normal encode to a signed FP8 zero either way.
-KVQ_DEVI float div_by_scale(float x, float s, float r) {
-  const float q0 = __fmul_rn(x, r);
-  const float e = __fmaf_rn(-q0, s, x);
-  return (e == 0.f || !(fabsf(q0) < 1048576.f)) ? q0 : __fmaf_rn(e, r, q0);
+// Per-head constants of the quantizing division x / s.  For s in
+// [2^-80, 2^80] the quotient comes from the reciprocal r = RN(1/s) and one
+// fused residual correction (Markstein's iteration): q0 = RN(x r),
+// e = RN(x - q0 s), q = RN(q0 + e r) -- the IEEE binary32 quotient for every
+// bf16 significand and every binary32 scale significand (checked
+// exhaustively), on the packed f32x2 pipes two elements at a time.  Inputs
+// first go through a bf16x2 clamp to +-L, L = 2^20 s rounded toward zero
+// (L >= 2^19 s): every |x| > L saturates the FP8 format and so does L itself,
+// infinities turn into +-L and NaN stays NaN, so q0, e and q stay finite.
+// The one sign the residual form can lose is that of a zero quotient from
+// x = -0; the FP8 sign bit is therefore OR-ed in from the bf16 sign bit
+// (equal to the quotient's sign everywhere else).  Quotients too small for
+// the residual to stay normal encode to a signed FP8 zero either way.
+struct HeadScale {
+  float2 r2, ns2;  // (r, r), (-s, -s)
+  uint32_t L2, nL2;  // bf16x2 (L, L), (-L, -L)
+  float s;
+  bool fast;
+};
+
+KVQ_DEVI HeadScale head_scale(float s) {
+  HeadScale h;
+  h.s = s;
+  h.fast = s >= 0x1p-80f && s <= 0x1p80f;
+  const float r = __frcp_rn(s);
+  h.r2 = make_float2(r, r);
+  h.ns2 = make_float2(-s, -s);
+  uint16_t L;
+  asm("cvt.rz.bf16.f32 %0, %1;" : "=h"(L) : "f"(h.fast ? s * 1048576.f : 0.f));
+  h.L2 = static_cast<uint32_t>(L) * 0x10001u;
+  h.nL2 = h.L2 | 0x80008000u;
+  return h;
 }
 
-KVQ_DEVI bool scale_is_nice(float s) { return s >= 0x1p-80f && s <= 0x1p80f; }
+KVQ_DEVI uint32_t bf16x2_clamp(uint32_t w, uint32_t lo, uint32_t hi) {
+  uint32_t t, d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(w), "r"(lo));
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(hi));
+  return d;
+}
 
-// Sixteen bf16 values (two uint4) -> sixteen FP8 codes: binary32 IEEE
-// quotient x / s (round to nearest even, no flush to zero), then the
-// saturating RNE conversion to FP8.
+// Two bf16 (one word) -> two FP8 codes (low byte = low element).
 template <int FMT>
-KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, float s, float r, bool fast) {
+KVQ_DEVI uint32_t quantize2(uint32_t w, const HeadScale& h) {
+  float2 q;
+  if (h.fast) {
+    const uint32_t c = bf16x2_clamp(w, h.nL2, h.L2);
+    const float2 x = make_float2(bf16lo_to_f32(c), bf16hi_to_f32(c));
+    const float2 q0 = __fmul2_rn(x, h.r2);
+    const float2 e = __ffma2_rn(q0, h.ns2, x);
+    q = __ffma2_rn(e, h.r2, q0);
+  } else {
+    q = make_float2(__fdiv_rn(bf16lo_to_f32(w), h.s), __fdiv_rn(bf16hi_to_f32(w), h.s));
+  }
+  return f32x2_to_fp8x2<FMT>(q.x, q.y);
+}
+
+// Sixteen bf16 values (two uint4) -> sixteen FP8 codes: binary32 quotient
+// x / s, then the saturating RNE conversion to FP8; signs from the inputs.
+template <int FMT>
+KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, const HeadScale& h) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float x[4] = {bf16lo_to_f32(w[2 * i]), bf16hi_to_f32(w[2 * i]), bf16lo_to_f32(w[2 * i + 1]),
-                  bf16hi_to_f32(w[2 * i + 1])};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] = fast ? div_by_scale(x[j], s, r) : __fdiv_rn(x[j], s);
-    o[i] = static_cast<uint32_t>(f32x2_to_fp8x2<FMT>(x[0], x[1])) |
-           (static_cast<uint32_t>(f32x2_to_fp8x2<FMT>(x[2], x[3])) << 16);
+    const uint32_t codes = quantize2<FMT>(w[2 * i], h) | (quantize2<FMT>(w[2 * i + 1], h) << 16);
+    const uint32_t signs = prmt(w[2 * i], w[2 * i + 1], 0x7531u) & 0x80808080u;
+    o[i] = codes | signs;
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// One thread per 16-element chunk of one (token, KV head) row.  The K/V
-// loads do not depend on the slot, so they are issued before it is checked.
-template <int FMT>
-__global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
+// One thread per 16-element chunk (h, c) of the (token, KV head) rows.  The
+// grid's thread count is a multiple of the Hkv * DH/16 chunks of a token, so
+// a thread keeps its chunk (and its head's scales) and strides over tokens;
+// the next token's K/V and slot loads are issued before the current token is
+// converted.
+template <int FMT, int DH>
+__global__ void __launch_bounds__(256, 3) write_kernel(const WriteParams p) {
+  constexpr int CH = DH / 16;
   pdl_allow_next();
   pdl_wait();  // k, v, slots may come from the previous kernel
-  const int chunks = p.dh >> 4;
-  const int64_t units = p.num_tokens * p.hkv * chunks;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
-       u += stride) {
-    const int c = static_cast<int>(u % chunks);
-    const int64_t th = u / chunks;
-    const int h = static_cast<int>(th % p.hkv);
-    const int64_t t = th / p.hkv;
-    const int64_t src = t * p.token_stride + static_cast<int64_t>(h) * p.dh + c * 16;
-    if (!guard(src >= 0 && src + 16 <= p.in_elems, p.status, 7)) continue;
-    const uint4* ksrc = reinterpret_cast<const uint4*>(p.k + src);
-    const uint4* vsrc = reinterpret_cast<const uint4*>(p.v + src);
-    const uint4 ka = __ldcs(ksrc), kb = __ldcs(ksrc + 1);
-    const uint4 va = __ldcs(vsrc), vb = __ldcs(vsrc + 1);
-    const int64_t slot = __ldg(p.slots + t);
-    if (slot < 0) continue;  // padding token
-    if (slot >= p.capacity) {
-      if (h == 0 && c == 0) flag_status(p.status, KVQ_DEV_BAD_SLOT);
-      continue;
-    }
-    const int64_t blk = slot / p.bs, off = slot - blk * p.bs;
-    const int64_t dst = ((blk * p.hkv + h) * p.bs + off) * p.dh + c * 16;
-    if (!guard(dst >= 0 && dst + 16 <= p.cache_elems, p.status, 8)) continue;
-    if (FMT == KVQ_FMT_BF16) {
-      uint4* kd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.kc) + dst);
-      uint4* vd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.vc) + dst);
-      kd[0] = ka;
-      kd[1] = kb;
-      vd[0] = va;
-      vd[1] = vb;
+  const int row_units = p.hkv * CH;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int rem = static_cast<int>(gtid % row_units);
+  const int h = rem / CH;
+  const int64_t tstride = nthreads / row_units;
+  int64_t t = gtid / row_units;
+  if (t >= p.num_tokens) return;
+  HeadScale hk, hv;
+  if (FMT != KVQ_FMT_BF16) {
+    hk = head_scale(__ldg(p.ks + (p.per_head ? h : 0)));
+    hv = head_scale(__ldg(p.vs + (p.per_head ? h : 0)));
+  }
+  auto load = [&](int64_t tt, uint4 (&kk)[2], uint4 (&vv)[2], int64_t& slot) {
+    const int64_t src = tt * p.token_stride + rem * 16;
+    if (guard(src >= 0 && src + 16 <= p.in_elems, p.status, 7)) {
+      const uint4* ks = reinterpret_cast<const uint4*>(p.k + src);
+      const uint4* vs = reinterpret_cast<const uint4*>(p.v + src);
+      kk[0] = __ldcs(ks);
+      kk[1] = __ldcs(ks + 1);
+      vv[0] = __ldcs(vs);
+      vv[1] = __ldcs(vs + 1);
+      slot = __ldg(p.slots + tt);
     } else {
-      const float sk = __ldg(p.ks + (p.per_head ? h : 0));
-      const float sv = __ldg(p.vs + (p.per_head ? h : 0));
-      const bool fast = scale_is_nice(sk) && scale_is_nice(sv);
-      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.kc) + dst) =
-          quantize16<FMT>(ka, kb, sk, __frcp_rn(sk), fast);
-      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.vc) + dst) =
-          quantize16<FMT>(va, vb, sv, __frcp_rn(sv), fast);
+      slot = -1;
     }
+  };
+  uint4 k[2], v[2];
+  int64_t slot;
+  load(t, k, v, slot);
+  while (true) {
+    const int64_t tn = t + tstride;
+    uint4 kn[2], vn[2];
+    int64_t sn = -1;
+    if (tn < p.num_tokens) load(tn, kn, vn, sn);
+    if (slot >= p.capacity) {
+      if (rem == 0) flag_status(p.status, KVQ_DEV_BAD_SLOT);
+    } else if (slot >= 0) {  // a negative slot is a padding token
+      const int64_t dst = (((slot >> 4) * p.hkv + h) * 16 + (slot & 15)) * DH + (rem % CH) * 16;
+      if (guard(dst >= 0 && dst + 16 <= p.cache_elems, p.status, 8)) {
+        if (FMT == KVQ_FMT_BF16) {
+          uint4* kd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.kc) + dst);
+          uint4* vd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.vc) + dst);
+          kd[0] = k[0];
+          kd[1] = k[1];
+          vd[0] = v[0];
+          vd[1] = v[1];
+        } else {
+          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.kc) + dst) = quantize16<FMT>(k[0], k[1], hk);
+          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.vc) + dst) = quantize16<FMT>(v[0], v[1], hv);
+        }
+      }
+    }
+    if (tn >= p.num_tokens) break;
+    t = tn;
+    k[0] = kn[0];
+    k[1] = kn[1];
+    v[0] = vn[0];
+    v[1] = vn[1];
+    slot = sn;
   }
 }
 
@@ -159,12 +218,38 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
   }
 }
 
-// One work unit per thread while the grid stays under 64 waves of the SMs;
-// beyond that the kernels loop (grid-stride).
+// Grid of a streaming kernel: one work unit per thread while that stays
+// under 64 waves of the SMs; beyond that the kernel loops (grid-stride).
 static int grid_for(int64_t units, int threads) {
   const int64_t need = (units + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8 * 64;
   return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+// Launch shape of the write kernel: a block is the largest multiple of the
+// row_units chunks of one token that fits 256 threads (or 256 threads, with
+// the grid a multiple of the blocks that make up whole tokens); the grid
+// fills the SMs once (3 blocks of 256 per SM) or covers the tokens, if fewer.
+static void write_shape(int64_t num_tokens, int row_units, int& grid, int& block) {
+  int g_mult = 1;
+  if (row_units <= 256) {
+    block = (256 / row_units) * row_units;
+  } else {
+    block = 256;
+    int a = row_units, b = 256;
+    while (b) {
+      const int t = a % b;
+      a = b;
+      b = t;
+    }
+    g_mult = row_units / a;  // row_units / gcd(row_units, 256)
+  }
+  const int64_t threads = num_tokens * row_units;  // one per chunk
+  int64_t need = (threads + block - 1) / block;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 3;  // the blocks resident at once (3 of 256 threads per SM)
+  if (need > cap) need = cap;
+  need = (need + g_mult - 1) / g_mult * g_mult;
+  grid = static_cast<int>(need > 0 ? need : g_mult);
 }
 
 }  // namespace kvq
@@ -210,21 +295,29 @@ extern "C" int kvq_write(const void* k, const void* v, int64_t token_stride,
   p.kc = k_cache;
   p.vc = v_cache;
   p.capacity = num_blocks * block_size;
-  p.bs = block_size;
   p.ks = k_scale;
   p.vs = v_scale;
   p.per_head = scale_granularity == KVQ_SCALE_PER_HEAD;
   p.status = dev_status;
   p.in_elems = (num_tokens - 1) * token_stride + static_cast<int64_t>(num_kv_heads) * head_dim;
   p.cache_elems = num_blocks * num_kv_heads * block_size * head_dim;
-  const int64_t units = num_tokens * num_kv_heads * (head_dim / 16);
-  const int grid = grid_for(units, 256);
+  int grid = 0, block = 0;
+  write_shape(num_tokens, num_kv_heads * (head_dim / 16), grid, block);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  switch (fmt) {
-    case KVQ_FMT_E4M3: e = launch_pdl(write_kernel<KVQ_FMT_E4M3>, dim3(grid), dim3(256), 0, s, p); break;
-    case KVQ_FMT_E5M2: e = launch_pdl(write_kernel<KVQ_FMT_E5M2>, dim3(grid), dim3(256), 0, s, p); break;
-    default: e = launch_pdl(write_kernel<KVQ_FMT_BF16>, dim3(grid), dim3(256), 0, s, p); break;
+  const dim3 gd(grid), bd(block);
+  if (head_dim == 128) {
+    switch (fmt) {
+      case KVQ_FMT_E4M3: e = launch_pdl(write_kernel<KVQ_FMT_E4M3, 128>, gd, bd, 0, s, p); break;
+      case KVQ_FMT_E5M2: e = launch_pdl(write_kernel<KVQ_FMT_E5M2, 128>, gd, bd, 0, s, p); break;
+      default: e = launch_pdl(write_kernel<KVQ_FMT_BF16, 128>, gd, bd, 0, s, p); break;
+    }
+  } else {
+    switch (fmt) {
+      case KVQ_FMT_E4M3: e = launch_pdl(write_kernel<KVQ_FMT_E4M3, 64>, gd, bd, 0, s, p); break;
+      case KVQ_FMT_E5M2: e = launch_pdl(write_kernel<KVQ_FMT_E5M2, 64>, gd, bd, 0, s, p); break;
+      default: e = launch_pdl(write_kernel<KVQ_FMT_BF16, 64>, gd, bd, 0, s, p); break;
+    }
   }
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

@@ -3,8 +3,8 @@
  *
  * The kernel divides a bf16 value x by a per-head scale s with a
  * precomputed reciprocal r = RN(1/s) and one residual correction (the
- * Markstein iteration): q0 = RN(x * r); e = RN(s * -q0 + x) (fused);
- * q = (e == 0) ? q0 : RN(e * r + q0) (fused).  Rounding depends only on the
+ * Markstein iteration): q0 = RN(x * r); e = RN(q0 * -s + x) (fused);
+ * q = RN(e * r + q0) (fused).  Rounding depends only on the
  * significands of x and s while the quotient stays normal, so checking every
  * bf16 significand (128) against every binary32 significand (2^23), with
  * both in [1, 2), covers every normal quotient.  Prints the number of
@@ -26,8 +26,8 @@ int main(void) {
       const float x = bits_to_f(0x3F800000u | (mx << 16));        /* bf16 in [1, 2) */
       const float want = x / s;
       const float q0 = x * r;
-      const float e = fmaf(-q0, s, x);
-      const float q = (e == 0.0f) ? q0 : fmaf(e, r, q0);
+      const float e = fmaf(q0, -s, x);
+      const float q = fmaf(e, r, q0);
       if (q != want) bad += 1;
     }
   }

@@ -115,6 +115,39 @@ def test_write_special_values(kvq, fmt):
     np.testing.assert_array_equal(to_np(d.vc), V)
 
 
+def _fp8_is_nan(codes, fmt):
+    c = codes & 0x7F
+    return c == 0x7F if fmt == workloads.E4M3 else c > 0x7C
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2])
+def test_write_extreme_scales(kvq, fmt):
+    """Per-head scales across the whole binary32 range (both sides of the
+    reciprocal method's [2^-80, 2^80] window, and zero) against inputs of
+    every magnitude, infinities and signed zeros: codes equal the oracle's,
+    NaN codes compared as NaN."""
+    lay = _custom_layer([300, 77], Hq=8, Hkv=8, dh=64, fmt=fmt, seed=11)
+    scales = np.array([2.0 ** -80, 1e-30, 1e-20, 0.01, 3e19, 2.0 ** 80, 2.0 ** 81, 0.0], np.float32)
+    lay.k_scale[:] = scales
+    lay.v_scale[:] = scales[::-1]
+    r = np.random.default_rng(12)
+    for arr in (lay.k, lay.v):
+        x = (r.standard_normal(arr.shape) * 10.0 ** r.uniform(-42, 38, arr.shape)).astype(np.float32)
+        arr[...] = workloads.f32_to_bf16_bits(x)
+        flat = arr.reshape(-1)
+        sp = workloads.f32_to_bf16_bits(np.array([0.0, -0.0, np.inf, -np.inf, 3.3895e38, -3.3895e38,
+                                                   1e-40, -1e-40], np.float32))
+        flat[r.choice(flat.size, 4000, replace=False)] = np.resize(sp, 4000)
+    d = DeviceLayer(lay)
+    d.write()
+    assert d.status_word() == 0
+    K, V = oracle_caches(lay)
+    for got, want in ((to_np(d.kc), K), (to_np(d.vc), V)):
+        gn, wn = _fp8_is_nan(got, fmt), _fp8_is_nan(want, fmt)
+        np.testing.assert_array_equal(gn, wn)
+        np.testing.assert_array_equal(np.where(gn, 0, got), np.where(wn, 0, want))
+
+
 def test_write_nan_gives_a_nan_code(kvq):
     lay = _custom_layer([16], gran=workloads.PER_TENSOR, seed=4)
     lay.k[0, 0, :5] = workloads.f32_to_bf16_bits(np.array([np.nan] * 5, np.float32))
@@ -318,4 +351,27 @@ def test_decode_fewer_units_than_ctas(kvq, lens, fmt):
         got = bf16_out_to_f64(d.decode())
         assert d.status_word() == 0
         check_attention(got, oracle_decode(lay, K, V), f"lens={lens}")
+        d.poison_workspace()
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,dh,fmt", [
+    ([6000], 1, 1, 64, workloads.E4M3),        # one segment over every CTA
+    ([9000], 8, 1, 128, workloads.BF16),       # pieces too large to stage in shared memory
+    ([20000], 32, 8, 128, workloads.E4M3),     # long-context shape: 8 segments, ~38 pieces each
+    ([7000, 3], 16, 4, 64, workloads.E5M2),
+    ([12000], 16, 8, 128, workloads.BF16),
+])
+def test_decode_segments_split_over_many_ctas(kvq, lens, Hq, Hkv, dh, fmt):
+    """Segments cut into many pieces: the CTA finishing a segment's last piece
+    merges up to one partial state per CTA, from shared memory when they fit
+    its idle ring, else from global memory."""
+    lay = _custom_layer(lens, Hq=Hq, Hkv=Hkv, dh=dh, fmt=fmt, seed=90 + Hq + dh)
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    ref = oracle_decode(lay, K, V)
+    for _ in range(2):
+        got = bf16_out_to_f64(d.decode())
+        assert d.status_word() == 0
+        check_attention(got, ref, f"lens={lens} G={Hq // Hkv} dh={dh}")
         d.poison_workspace()
