@@ -467,14 +467,15 @@ def run_reference(args):
 
 
 def run_ncu_case(case: str):
-    """A few launches of one kernel on a case larger than L2, for ncu captures:
-    'decode' and 'write' run one FP8 layer of the mixed skip-layer batch
-    (128 sequences, about 0.9 GB of FP8 cache), 'decode_long' one layer of the
-    long-context workload (64 MiB of cache)."""
+    """A few launches of one kernel for ncu captures (ncu flushes the caches
+    before each captured launch): 'decode' and 'write' run one FP8 layer of
+    the mixed skip-layer batch (128 sequences, about 0.9 GB of FP8 cache),
+    'decode_long' and 'write_long' one layer of the long-context workload
+    (32768 tokens: 128 MiB of bf16 K/V in, 64 MiB of FP8 cache)."""
     import torch
 
     import fp8_quantized_paged_gb300 as kvq
-    cfg, layer = (4, 0) if case == "decode_long" else (5, 2)
+    cfg, layer = (4, 0) if case.endswith("_long") else (5, 2)
     lay = workloads.make_layer(cfg, layer)
     st = lay.st
     dev = torch.device("cuda:0")
@@ -492,7 +493,7 @@ def run_ncu_case(case: str):
     vc = kvq.new_cache(st.num_blocks, lay.Hkv, lay.dh, lay.fmt, dev)
     ws = kvq.new_workspace(lay.B, lay.Hq, lay.Hkv, lay.dh, dev)
     out = torch.empty((lay.B, lay.Hq, lay.dh), dtype=torch.bfloat16, device=dev)
-    n_write = 3 if case == "write" else 1
+    n_write = 3 if case.startswith("write") else 1
     for _ in range(n_write):
         kvq.kvq_write(k, v, slots, kc, vc, ks, vs, lay.gran, lay.fmt)
     for _ in range(3 if case.startswith("decode") else 0):
@@ -511,7 +512,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "write", "decode_long"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "write", "decode_long", "write_long"], default=None,
                     help="run a few launches of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.ncu_case:

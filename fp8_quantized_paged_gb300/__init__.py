@@ -23,6 +23,7 @@ KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA, KVQ_ERR_ARG = -4, -5, -6, 
 KVQ_DEV_BAD_SLOT, KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
 KVQ_DEV_INTERNAL = 16
 KVQ_Q_FP8 = 1
+KVQ_CACHE_READY = 2
 KVQ_STATIC_SCRATCH_BYTES = 16 << 20
 BLOCK_SIZE = 16
 
@@ -194,13 +195,10 @@ def new_cache(num_blocks, num_kv_heads, head_dim, fmt, device="cuda"):
     return torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE, head_dim), dtype=dt, device=device)
 
 
-KVQ_WS_COUNTER_BYTES = 65536 * 4  # leading workspace bytes that must start at zero
-
-
 def new_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, device="cuda"):
-    """A decode workspace, zero-filled (its counters must start at zero)."""
+    """A decode workspace (needs no initialisation)."""
     import torch
     n = kvq_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)
     if n == 0:
         raise KvqError(KVQ_ERR_ARG, "kvq_decode_workspace_size")
-    return torch.zeros(n, dtype=torch.uint8, device=device)
+    return torch.empty(n, dtype=torch.uint8, device=device)

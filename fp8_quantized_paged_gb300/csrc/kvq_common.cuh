@@ -111,6 +111,23 @@ KVQ_DEVI void tma_load_2d(void* dst, const CUtensorMap* map, int32_t c0, int32_t
       : "memory");
 }
 
+// An L2 policy that marks the lines a load brings in as first to evict: for
+// data read once (a stream that would otherwise push everything else out).
+KVQ_DEVI uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+KVQ_DEVI void tma_load_2d_hint(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 KVQ_DEVI void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
                           uint64_t* bar) {
   asm volatile(
@@ -132,6 +149,12 @@ KVQ_DEVI void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* ba
 // Orders this thread's earlier generic-proxy accesses (and what it has
 // acquired from other threads) before its later async-proxy accesses.
 KVQ_DEVI void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
+KVQ_DEVI void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+KVQ_DEVI void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // ------------------------------------------------------------------ MMA (m16n8k16, fp32 accumulate)
 

@@ -50,7 +50,7 @@ struct WriteParams {
 // the residual to stay normal encode to a signed FP8 zero either way.
 struct HeadScale {
   float2 r2, ns2;  // (r, r), (-s, -s)
-  uint32_t L2, nL2;  // bf16x2 (L, L), (-L, -L)
+  uint32_t L2;  // bf16x2 (L, L)
   float s;
   bool fast;
 };
@@ -65,14 +65,13 @@ KVQ_DEVI HeadScale head_scale(float s) {
   uint16_t L;
   asm("cvt.rz.bf16.f32 %0, %1;" : "=h"(L) : "f"(h.fast ? s * 1048576.f : 0.f));
   h.L2 = static_cast<uint32_t>(L) * 0x10001u;
-  h.nL2 = h.L2 | 0x80008000u;
   return h;
 }
 
-KVQ_DEVI uint32_t bf16x2_clamp(uint32_t w, uint32_t lo, uint32_t hi) {
-  uint32_t t, d;
-  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(w), "r"(lo));
-  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(hi));
+// sign(x) * min(|x|, L) on both halves (L positive), NaN propagated.
+KVQ_DEVI uint32_t bf16x2_clamp(uint32_t w, uint32_t L2) {
+  uint32_t d;
+  asm("min.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(L2));
   return d;
 }
 
@@ -81,7 +80,7 @@ template <int FMT>
 KVQ_DEVI uint32_t quantize2(uint32_t w, const HeadScale& h) {
   float2 q;
   if (h.fast) {
-    const uint32_t c = bf16x2_clamp(w, h.nL2, h.L2);
+    const uint32_t c = bf16x2_clamp(w, h.L2);
     const float2 x = make_float2(bf16lo_to_f32(c), bf16hi_to_f32(c));
     const float2 q0 = __fmul2_rn(x, h.r2);
     const float2 e = __ffma2_rn(q0, h.ns2, x);
@@ -100,9 +99,9 @@ KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, const HeadScale& h) {
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t codes = quantize2<FMT>(w[2 * i], h) | (quantize2<FMT>(w[2 * i + 1], h) << 16);
-    const uint32_t signs = prmt(w[2 * i], w[2 * i + 1], 0x7531u) & 0x80808080u;
-    o[i] = codes | signs;
+    const uint32_t codes = prmt(quantize2<FMT>(w[2 * i], h), quantize2<FMT>(w[2 * i + 1], h), 0x5410u);
+    const uint32_t signs = prmt(w[2 * i], w[2 * i + 1], 0x7531u);
+    o[i] = codes | (signs & 0x80808080u);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }

@@ -72,10 +72,9 @@ class DeviceLayer:
         self.out = torch.empty((lay.B, lay.Hq, lay.dh), dtype=torch.bfloat16, device=dev)
 
     def poison_workspace(self):
-        """NaN bytes everywhere but the counters (which must stay zero), so a
-        read of a partial slot nobody wrote shows up."""
+        """NaN bytes everywhere, so a read of a partial slot nobody wrote
+        shows up."""
         self.ws.fill_(0xFF)
-        self.ws[: self.kvq.KVQ_WS_COUNTER_BYTES].zero_()
 
     def write(self, token_idx=None):
         lay = self.lay
@@ -87,14 +86,14 @@ class DeviceLayer:
         self.kvq.kvq_write(k, v, s, self.kc, self.vc, self.ks, self.vs, lay.gran, lay.fmt,
                            dev_status=self.status)
 
-    def decode(self, window=None, seq_lens=None, block_tables=None):
+    def decode(self, window=None, seq_lens=None, block_tables=None, flags=0):
         lay = self.lay
         self.kvq.kvq_decode_attn(self.q, self.kc, self.vc,
                                  self.bt if block_tables is None else block_tables,
                                  self.sl if seq_lens is None else seq_lens, self.qs, self.ks,
                                  self.vs, lay.gran, lay.fmt,
                                  lay.window if window is None else window, self.ws, self.out,
-                                 dev_status=self.status)
+                                 dev_status=self.status, flags=flags)
         return self.out
 
     def status_word(self):

@@ -155,3 +155,22 @@ def test_decode_validation(kvq):
     assert _decode(kvq, gran=1) == kvq.KVQ_ERR_SHAPE            # k/v scale must be [Hkv]
     assert _decode(kvq, gran=1, ksl=8, vsl=8, qs=A, qsl=8) == kvq.KVQ_ERR_SHAPE  # q scale [Hq]
     assert _decode(kvq, qs=A, qsl=32) == kvq.KVQ_ERR_SHAPE      # per tensor q scale is [1]
+
+
+def test_python_constants_mirror_the_header():
+    """Every #define of include/kvq.h that the binding also names has the
+    same value there."""
+    import fp8_quantized_paged_gb300 as kvq
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    found = 0
+    for name, expr in re.findall(r"#define\s+(KVQ_\w+)\s+(.+?)\s*(?:/\*.*)?$", text, re.M):
+        if not hasattr(kvq, name):
+            continue
+        val = eval(re.sub(r"(\d+)u\b", r"\1", expr.replace("(size_t)", "")))
+        assert getattr(kvq, name) == val, name
+        found += 1
+    for name, val in re.findall(r"\b(KVQ_\w+)\s*=\s*(-?\d+)", text):  # enumerators
+        if hasattr(kvq, name):
+            assert getattr(kvq, name) == int(val), name
+            found += 1
+    assert found >= 15

@@ -360,6 +360,9 @@ def test_decode_fewer_units_than_ctas(kvq, lens, fmt):
     ([20000], 32, 8, 128, workloads.E4M3),     # long-context shape: 8 segments, ~38 pieces each
     ([7000, 3], 16, 4, 64, workloads.E5M2),
     ([12000], 16, 8, 128, workloads.BF16),
+    ([3000] * 4, 32, 8, 128, workloads.E4M3),  # ~10 pieces per segment
+    ([1500] * 8, 32, 8, 128, workloads.E4M3),  # ~5 pieces per segment
+    ([2500] * 3, 8, 4, 64, workloads.E5M2),
 ])
 def test_decode_segments_split_over_many_ctas(kvq, lens, Hq, Hkv, dh, fmt):
     """Segments cut into many pieces: the CTA finishing a segment's last piece
@@ -375,3 +378,44 @@ def test_decode_segments_split_over_many_ctas(kvq, lens, Hq, Hkv, dh, fmt):
         assert d.status_word() == 0
         check_attention(got, ref, f"lens={lens} G={Hq // Hkv} dh={dh}")
         d.poison_workspace()
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.BF16])
+def test_decode_cache_ready_after_new_token_write(kvq, fmt):
+    """KVQ_CACHE_READY: the decode may start while the kvq_write of each
+    sequence's newest token still runs; it reads the older pages early and
+    the newest token's page only after that write."""
+    lens = [2048, 700, 33, 1, 16, 17, 4000, 129]
+    lay = _custom_layer(lens, Hq=32, Hkv=8, dh=128, fmt=fmt, seed=130 + fmt)
+    last = np.cumsum(lens) - 1
+    older = np.setdiff1d(np.arange(int(np.sum(lens))), last)
+    d = DeviceLayer(lay)
+    K, V = oracle_caches(lay)
+    ref = oracle_decode(lay, K, V)
+    for _ in range(3):
+        d.kc.zero_()
+        d.vc.zero_()
+        d.write(older)
+        torch.cuda.synchronize()
+        d.write(last)  # the preceding kernel writes only the newest token of each sequence
+        got = bf16_out_to_f64(d.decode(flags=kvq.KVQ_CACHE_READY))
+        assert d.status_word() == 0
+        check_attention(got, ref, "cache ready after write")
+
+
+def test_decode_cache_ready_chained_layers(kvq):
+    """Decodes of different layers back to back, each allowed to start early."""
+    lays = [_custom_layer([5000, 300, 64], Hq=32, Hkv=8, dh=128, seed=140 + i) for i in range(3)]
+    devs = [DeviceLayer(lay) for lay in lays]
+    refs = []
+    for d, lay in zip(devs, lays):
+        d.write()
+        K, V = oracle_caches(lay)
+        refs.append(oracle_decode(lay, K, V))
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for d in devs:
+            d.decode(flags=kvq.KVQ_CACHE_READY)
+        for d, ref in zip(devs, refs):
+            assert d.status_word() == 0
+            check_attention(bf16_out_to_f64(d.out), ref, "chained")
