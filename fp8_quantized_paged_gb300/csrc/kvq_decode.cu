@@ -63,6 +63,12 @@ constexpr int kMaxGroup = 8;
 constexpr int kMaxKvHeads = 256;
 constexpr int kMaxSegments = 65536;  // num_seqs * num_kv_heads
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazily rescale O
+#ifndef KVQ_PIECE_COST
+#define KVQ_PIECE_COST 16
+#endif
+// Fixed cost of one piece (its setup, the warps' combine and the store of
+// its state) counted in pages when the units are split among the CTAs.
+constexpr int kPieceCost = KVQ_PIECE_COST;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 template <int FMT, int DH>
@@ -86,7 +92,7 @@ struct Cfg {
 // Dynamic shared memory of the decode kernel (offsets from a 1024-aligned
 // base): the ring and barriers at fixed offsets, then the warps' merge
 // scratch for the group's G heads, the plan ([B+1] unit offsets, [B] checked
-// lengths) and the k/v scales.
+// lengths, [B+1] cost offsets) and the k/v scales.
 template <int FMT, int DH>
 struct SmemLayout {
   using C = Cfg<FMT, DH>;
@@ -103,7 +109,7 @@ struct SmemLayout {
     return comb + ((comb_floats(G) * sizeof(float) + 15) & ~size_t(15));
   }
   __host__ __device__ static size_t scales(int G, int B) {
-    return seq(G) + (2 * static_cast<size_t>(B) + 1) * sizeof(int32_t);
+    return seq(G) + (3 * static_cast<size_t>(B) + 2) * sizeof(int32_t);
   }
   __host__ __device__ static size_t total(int G, int B, int Hkv) {
     return scales(G, B) + 2 * static_cast<size_t>(Hkv) * sizeof(float) + 1024;
@@ -200,9 +206,10 @@ KVQ_DEVI int find_seq(const int32_t* seq_off, int B, int64_t u) {
   return lo;
 }
 
-// Exclusive scan of per-sequence unit counts into seq_off[0..B], the checked
-// length of every sequence into len_s[0..B), and the k/v scales of the KV
-// heads into sk_s / sv_s (per-tensor scales replicated).
+// Exclusive scans of the per-sequence unit counts into seq_off[0..B] and of
+// the costs into vseq_off[0..B], the checked length of every sequence into
+// len_s[0..B), and the k/v scales of the KV heads into sk_s / sv_s
+// (per-tensor scales replicated).
 KVQ_DEVI int first_page_of(const DecodeParams& p, int L) { return window_lo(p, L) / kBS; }
 
 // Pages sequence b attends to (0 for an empty or invalid length), the unit
@@ -212,13 +219,35 @@ KVQ_DEVI int seq_pages(int raw_len, int max_blocks, int window) {
   return L > 0 ? (L + kBS - 1) / kBS - window_lo(window, L) / kBS : 0;
 }
 
-// CTA holding unit u when W units are split into Pe contiguous ranges
-// [floor(c W / Pe), floor((c + 1) W / Pe)).
-KVQ_DEVI int64_t cta_of_unit(int64_t u, int64_t W, int64_t Pe) { return ((u + 1) * Pe + W - 1) / W - 1; }
+// The split of the units among the CTAs balances cost, not units: segment
+// (b, g) costs kPieceCost + pages_b, laid out as kPieceCost cost units
+// followed by its pages, sequence after sequence, head after head
+// (vseq_off[b] is the cost before sequence b, seq_off[b] the pages).  CTA c
+// takes the cost range [floor(c V / Pe), floor((c + 1) V / Pe)) of the total
+// V, i.e. the pages between the page counts at those two cost positions, so
+// a CTA of many short segments gets fewer pages.
+// Pages before cost position v (0 <= v <= V).
+KVQ_DEVI int64_t pages_before(const int32_t* seq_off, const int32_t* vseq_off, int B, int Hkv,
+                              int64_t v) {
+  if (v >= vseq_off[B]) return seq_off[B];
+  const int b = find_seq(vseq_off, B, v);
+  const int pages = (seq_off[b + 1] - seq_off[b]) / Hkv;
+  const int64_t r = v - vseq_off[b];
+  const int64_t g = r / (pages + kPieceCost);
+  const int64_t in = r - g * (pages + kPieceCost) - kPieceCost;  // < 0: in the fixed cost
+  return seq_off[b] + g * pages + (in < 0 ? 0 : (in > pages ? pages : in));
+}
+
+// First unit of CTA c (c = Pe gives the total W).
+KVQ_DEVI int64_t cta_first_unit(const int32_t* seq_off, const int32_t* vseq_off, int B, int Hkv,
+                                int64_t c, int64_t Pe) {
+  const int64_t V = vseq_off[B];
+  return pages_before(seq_off, vseq_off, B, Hkv, c * V / Pe);
+}
 
 template <bool SCALED>
-KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s, float* sk_s,
-                         float* sv_s, int32_t* warp_tot) {
+KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s,
+                         int32_t* vseq_off, float* sk_s, float* sv_s, int32_t* warp_tot) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int h = tid; h < p.Hkv; h += kThreads) {
     sk_s[h] = SCALED ? __ldg(p.ks + (p.per_head ? h : 0)) : 1.f;
@@ -226,7 +255,7 @@ KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s
   }
   const int per = (p.B + kThreads - 1) / kThreads;
   const int b0 = tid * per, b1 = min(p.B, b0 + per);
-  int local = 0;
+  int local = 0, vlocal = 0;
   for (int b = b0; b < b1; ++b) {
     const int raw = __ldg(p.seq_lens + b);
     if ((raw < 0 || raw > p.max_blocks * kBS) && blockIdx.x == 0)
@@ -235,21 +264,39 @@ KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s
     const int pages = seq_pages(raw, p.max_blocks, p.window);
     len_s[b] = L;
     seq_off[b] = local;
+    vseq_off[b] = vlocal;
     local += pages * p.Hkv;
+    vlocal += pages > 0 ? (pages + kPieceCost) * p.Hkv : 0;
   }
-  int incl = local;
+  auto scan = [&](int v, int& total) {  // block-wide exclusive scan
+    int incl = v;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(kFull, incl, off);
-    if (lane >= off) incl += v;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      base += w < warp ? warp_tot[w] : 0;
+      total += warp_tot[w];
+    }
+    __syncthreads();
+    return base + incl - v;
+  };
+  int total, vtotal;
+  const int excl = scan(local, total);
+  const int vexcl = scan(vlocal, vtotal);
+  for (int b = b0; b < b1; ++b) {
+    seq_off[b] += excl;
+    vseq_off[b] += vexcl;
   }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  int base = 0;
-  for (int w = 0; w < warp; ++w) base += warp_tot[w];
-  const int excl = base + incl - local;
-  for (int b = b0; b < b1; ++b) seq_off[b] += excl;
-  if (tid == kThreads - 1) seq_off[p.B] = base + incl;
+  if (tid == 0) {
+    seq_off[p.B] = total;
+    vseq_off[p.B] = vtotal;
+  }
   __syncthreads();
 }
 
@@ -577,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   float* co = cl + kConsumerWarps * p.G;                   // [warps][G][DH] unnormalised O
   int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq(p.G));  // [B+1]
   int32_t* len_s = seq_off + p.B + 1;                                  // [B]
+  int32_t* vseq_off = len_s + p.B;                                     // [B+1]
   float* sk_s = reinterpret_cast<float*>(smem + SL::scales(p.G, p.B)); // [Hkv]
   float* sv_s = sk_s + p.Hkv;                                          // [Hkv]
 
@@ -603,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     pdl_wait();
     pdl_allow_next();
   }
-  build_plan<FMT != KVQ_FMT_BF16>(p, seq_off, len_s, sk_s, sv_s, warp_tot);  // has __syncthreads
+  build_plan<FMT != KVQ_FMT_BF16>(p, seq_off, len_s, vseq_off, sk_s, sv_s, warp_tot);
 
   const int64_t W = seq_off[p.B];
   // Sequences with nothing to attend to get a zero output row (CTAs share them).
@@ -615,12 +663,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     }
   };
   if (!p.early) zero_empty_rows(tid, kThreads);
-  // Effective partition size: never more CTAs than units, so every CTA of the
-  // partition owns at least one unit (the reduce relies on it); the others idle.
+  // Partition size: never more CTAs than units (the others idle).  CTA c
+  // takes units [u0, u1), a cost-balanced range; a CTA whose cost range lies
+  // in one segment's fixed cost may get none.
   const int64_t Pe = W < p.P ? W : p.P;
   const int64_t c = blockIdx.x;
-  const int64_t u0 = c < Pe ? c * W / Pe : 0;
-  const int64_t u1 = c < Pe ? (c + 1) * W / Pe : 0;
+  const int64_t u0 = c < Pe ? cta_first_unit(seq_off, vseq_off, p.B, p.Hkv, c, Pe) : 0;
+  const int64_t u1 = c < Pe ? cta_first_unit(seq_off, vseq_off, p.B, p.Hkv, c + 1, Pe) : 0;
   const int64_t total = u1 - u0;
 
   if (warp == kConsumerWarps) {
@@ -1117,7 +1166,7 @@ KVQ_DEVI int merge_block_scan(int v, int& excl, int32_t* tot) {
 //   O = sV sum_c w_c o_c / L   (the bf16 output row).
 // A segment is split exactly where a CTA boundary falls inside it, so the
 // split segments are found from the boundaries c = 1 .. Pe-1: boundary c
-// owns the segment holding unit floor(c W / Pe) if that unit is not the
+// owns the segment holding CTA c's first unit if that unit is not the
 // segment's first and CTA c - 1 holds the segment's first piece.  Before
 // waiting for the decode kernel, every CTA lists the owning boundaries and
 // their warp items in shared memory: a segment of at most kMergeSmallN
@@ -1132,7 +1181,9 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeMinBlocks)
   constexpr int NS = DH / 32;  // 32-dim slices of a head row
   extern __shared__ uint8_t smem_raw[];
   int32_t* seq_off = reinterpret_cast<int32_t*>(smem_raw);  // [B + 1]
-  int32_t* item_off = seq_off + p.B + 1;                     // [P + 1] first item of boundary c
+  int32_t* vseq_off = seq_off + p.B + 1;                     // [B + 1]
+  int32_t* ub = vseq_off + p.B + 1;                          // [P + 1] first unit of CTA c
+  int32_t* item_off = ub + p.P + 1;                          // [P + 1] first item of boundary c
   int32_t* own_n = item_off + p.P + 1;                       // [P] pieces (owners only)
   int32_t* own_b = own_n + p.P;                              // [P] sequence
   int32_t* own_g = own_b + p.P;                              // [P] KV head
@@ -1153,38 +1204,64 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeMinBlocks)
   // This kernel starts only once every decode CTA is past its own wait, so
   // seq_lens is final and the work list can be built before waiting; the
   // partial states need the decode kernel complete.
-  {  // seq_off: exclusive scan of pages * Hkv, the decode kernel's plan
+  {  // seq_off, vseq_off: the decode kernel's plan (pages and cost per sequence)
     const int per = (p.B + kMergeThreads - 1) / kMergeThreads;
     const int b0 = tid * per, b1 = min(p.B, b0 + per);
-    int local = 0;
+    int local = 0, vlocal = 0;
     for (int b = b0; b < b1; ++b) {
+      const int pages = seq_pages(__ldg(p.seq_lens + b), p.max_blocks, p.window);
       seq_off[b] = local;
-      local += seq_pages(__ldg(p.seq_lens + b), p.max_blocks, p.window) * p.Hkv;
+      vseq_off[b] = vlocal;
+      local += pages * p.Hkv;
+      vlocal += pages > 0 ? (pages + kPieceCost) * p.Hkv : 0;
     }
-    int excl;
+    int excl, vexcl;
     const int total = merge_block_scan(local, excl, tot);
-    for (int b = b0; b < b1; ++b) seq_off[b] += excl;
-    if (tid == 0) seq_off[p.B] = total;
+    const int vtotal = merge_block_scan(vlocal, vexcl, tot);
+    for (int b = b0; b < b1; ++b) {
+      seq_off[b] += excl;
+      vseq_off[b] += vexcl;
+    }
+    if (tid == 0) {
+      seq_off[p.B] = total;
+      vseq_off[p.B] = vtotal;
+    }
     __syncthreads();
   }
   const int64_t W = seq_off[p.B];
   const int64_t Pe = W < p.P ? W : p.P;
+  for (int c = tid; c <= Pe; c += kMergeThreads)
+    ub[c] = static_cast<int32_t>(cta_first_unit(seq_off, vseq_off, p.B, p.Hkv, c, Pe));
+  __syncthreads();
+  // CTA holding unit u: the last c < Pe with ub[c] <= u (empty CTAs skipped).
+  auto cta_of = [&](int64_t u) {
+    int lo = 0, hi = static_cast<int>(Pe) - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ub[mid] <= u)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    return lo;
+  };
   {  // owning boundaries and their item counts
     const int nb = static_cast<int>(Pe > 1 ? Pe - 1 : 0);  // boundaries 1 .. Pe-1
     const int per = (nb + kMergeThreads - 1) / kMergeThreads;
     const int k0 = tid * per, k1 = min(nb, k0 + per);
     int local = 0;
     for (int k = k0; k < k1; ++k) {
-      const int64_t c = k + 1;
-      const int64_t u = c * W / Pe;  // first unit of CTA c
-      const int b = find_seq(seq_off, p.B, u);
-      const int pages = (seq_off[b + 1] - seq_off[b]) / p.Hkv;
+      const int c = k + 1;
+      const int64_t u = ub[c];  // first unit of CTA c
       int cnt = 0;
-      if (pages > 0) {
+      if (u < W && u > ub[c - 1]) {  // CTA c - 1 holds units; u is inside W
+        const int b = find_seq(seq_off, p.B, u);
+        const int pages = (seq_off[b + 1] - seq_off[b]) / p.Hkv;
         const int g = static_cast<int>((u - seq_off[b]) / pages);
         const int64_t us = seq_off[b] + static_cast<int64_t>(g) * pages;
-        if (u != us && cta_of_unit(us, W, Pe) == c - 1) {
-          const int n = static_cast<int>(cta_of_unit(us + pages - 1, W, Pe) - (c - 1) + 1);
+        // split at c, and c - 1 holds the segment's first unit
+        if (u != us && ub[c - 1] <= us) {
+          const int n = cta_of(us + pages - 1) - (c - 1) + 1;
           own_n[k] = n;
           own_b[k] = b;
           own_g[k] = g;
@@ -1231,7 +1308,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeMinBlocks)
 }
 
 static size_t merge_smem_bytes(int B, int P, int Hkv) {
-  return (static_cast<size_t>(B) + 1 + 4 * static_cast<size_t>(P) + 1 + Hkv) * sizeof(int32_t);
+  return (2 * (static_cast<size_t>(B) + 1) + 5 * static_cast<size_t>(P) + 2 + Hkv) * sizeof(int32_t);
 }
 
 // --------------------------------------------------------------------------
@@ -1378,7 +1455,8 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   const int G = num_q_heads / num_kv_heads;
   if (G > kMaxGroup || num_kv_heads > kMaxKvHeads) return KVQ_ERR_UNSUPPORTED;
   if (num_seqs > kMaxSeqs || num_seqs * num_kv_heads > kMaxSegments) return KVQ_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * num_kv_heads >= (int64_t(1) << 31))
+  if (static_cast<int64_t>(num_seqs) * (max_blocks_per_seq + kPieceCost) * num_kv_heads >=
+      (int64_t(1) << 31))
     return KVQ_ERR_UNSUPPORTED;
   if (num_blocks * num_kv_heads * kBS >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||

@@ -337,7 +337,8 @@ def test_dequant_then_bf16_decode(kvq, cfg, fmt3):
     check_attention(got, ref, "unfused bf16 path")
 
 
-@pytest.mark.parametrize("lens", [[70, 33, 1], [500, 300], [16] * 7, [1] * 40])
+@pytest.mark.parametrize("lens", [[70, 33, 1], [500, 300], [16] * 7, [1] * 40, [1] * 300 + [5000],
+                                  [0, 3, 0, 40000, 2, 0, 17]])
 @pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.BF16])
 def test_decode_fewer_units_than_ctas(kvq, lens, fmt):
     """Batches with fewer KV pages than the persistent grid has CTAs: segments
