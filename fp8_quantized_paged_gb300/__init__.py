@@ -195,10 +195,13 @@ def new_cache(num_blocks, num_kv_heads, head_dim, fmt, device="cuda"):
     return torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE, head_dim), dtype=dt, device=device)
 
 
+KVQ_WS_COUNTER_BYTES = 65536 * 4  # leading workspace bytes that must start at zero
+
+
 def new_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, device="cuda"):
-    """A decode workspace (needs no initialisation)."""
+    """A decode workspace, zero-filled (its counters must start at zero)."""
     import torch
     n = kvq_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim)
     if n == 0:
         raise KvqError(KVQ_ERR_ARG, "kvq_decode_workspace_size")
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)

@@ -14,9 +14,8 @@
 //   range [floor(c W / P), floor((c+1) W / P)) of the W units, so every CTA
 //   streams the same number of bytes whatever the length mix.  A range cut
 //   through a (b, g) segment leaves partial softmax states (m, l, o) in the
-//   workspace, merged by a second, small kernel (merge_kernel) chained to the
-//   first with programmatic dependent launch.  A segment held by one CTA is
-//   written directly.
+//   workspace; the CTA that completes a segment's last piece merges them.
+//   A segment held by one CTA is written directly.
 //
 // Inside a CTA
 //   warp 4 (producer): one lane issues TMA tile loads of the K page and the V
@@ -61,13 +60,13 @@ constexpr int kRingBytes = KVQ_RING_KB * 1024;
 constexpr int kMaxSeqs = 4096;
 constexpr int kMaxGroup = 8;
 constexpr int kMaxKvHeads = 256;
-constexpr int kMaxSegments = 65536;  // num_seqs * num_kv_heads
+constexpr int kMaxSegments = 65536;  // num_seqs * num_kv_heads (counter table entries)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazily rescale O
 #ifndef KVQ_PIECE_COST
 #define KVQ_PIECE_COST 16
 #endif
-// Fixed cost of one piece (its setup, the warps' combine and the store of
-// its state) counted in pages when the units are split among the CTAs.
+// Fixed cost of one piece (its setup, the warps' combine and the publication
+// of its state) counted in pages when the units are split among the CTAs.
 constexpr int kPieceCost = KVQ_PIECE_COST;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
@@ -90,29 +89,34 @@ struct Cfg {
 };
 
 // Dynamic shared memory of the decode kernel (offsets from a 1024-aligned
-// base): the ring and barriers at fixed offsets, then the warps' merge
-// scratch for the group's G heads, the plan ([B+1] unit offsets, [B] checked
-// lengths, [B+1] cost offsets) and the k/v scales.
+// base): the ring and barriers at fixed offsets, then the merge scratch (the
+// warps' states for the group's G heads, reused for the weights of up to P
+// pieces when a split segment is merged), the plan ([B+1] unit offsets, [B]
+// checked lengths, [B+1] cost offsets, [P+1] first unit of every CTA) and the
+// k/v scales.
 template <int FMT, int DH>
 struct SmemLayout {
   using C = Cfg<FMT, DH>;
   static constexpr int S = C::kStages;
   static constexpr size_t ring = 0;
-  static constexpr size_t bars = ring + static_cast<size_t>(S) * C::kSlot;  // full[S], empty[S]
-  // bad[S], abort, spare, tot[8], last[S]
-  static constexpr size_t flags = bars + 2 * S * sizeof(uint64_t);
-  static constexpr size_t comb = (flags + (2 * S + 2 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
-  __host__ __device__ static size_t comb_floats(int G) {
-    return static_cast<size_t>(kConsumerWarps) * G * (DH + 2);
+  // full[S], empty[S], and the barrier of the segment-merge bulk copy
+  static constexpr size_t bars = ring + static_cast<size_t>(S) * C::kSlot;
+  // bad[S], abort, merge decision, tot[8], last[S], merge copy issued
+  static constexpr size_t flags = bars + (2 * S + 1) * sizeof(uint64_t);
+  static constexpr size_t comb = (flags + (2 * S + 3 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
+  __host__ __device__ static size_t comb_floats(int G, int P) {
+    const size_t warps = static_cast<size_t>(kConsumerWarps) * G * (DH + 2);
+    const size_t pieces = (static_cast<size_t>(P) + 1) * G;
+    return warps > pieces ? warps : pieces;
   }
-  __host__ __device__ static size_t seq(int G) {
-    return comb + ((comb_floats(G) * sizeof(float) + 15) & ~size_t(15));
+  __host__ __device__ static size_t seq(int G, int P) {
+    return comb + ((comb_floats(G, P) * sizeof(float) + 15) & ~size_t(15));
   }
-  __host__ __device__ static size_t scales(int G, int B) {
-    return seq(G) + (3 * static_cast<size_t>(B) + 2) * sizeof(int32_t);
+  __host__ __device__ static size_t scales(int G, int P, int B) {
+    return seq(G, P) + (3 * static_cast<size_t>(B) + 2 + static_cast<size_t>(P) + 1) * sizeof(int32_t);
   }
-  __host__ __device__ static size_t total(int G, int B, int Hkv) {
-    return scales(G, B) + 2 * static_cast<size_t>(Hkv) * sizeof(float) + 1024;
+  __host__ __device__ static size_t total(int G, int P, int B, int Hkv) {
+    return scales(G, P, B) + 2 * static_cast<size_t>(Hkv) * sizeof(float) + 1024;
   }
 };
 
@@ -130,6 +134,7 @@ struct DecodeParams {
   int P;
   int early;  // KVQ_CACHE_READY: tables, lengths, scales and all but the last pages before the wait
   float logit_scale;  // log2(e) / sqrt(dh)
+  uint32_t* ws_cnt;  // [B * Hkv] arrivals of the pieces of each segment (zero between calls)
   float* ws_ml;
   float* ws_o;
   uint16_t* out;
@@ -138,13 +143,14 @@ struct DecodeParams {
   int64_t n_slots;  // partial slots in the workspace
 };
 
-// Workspace: per partial slot the (m, l) pairs and the o vectors of the G
-// heads of a group.  The partial slot of the piece of segment
-// sigma = b * Hkv + g held by CTA c is c + sigma (unique: CTA ranges are
-// ordered).  Nothing in it needs initialising: every slot the merge kernel
-// reads was written by the decode kernel of the same call.
+// Workspace: a table of kMaxSegments uint32 arrival counters, one per
+// (sequence, KV head) segment (zero before the first call, left zero by
+// every completed call), then per partial slot the (m, l) pairs
+// and o vectors for the G heads of a group.  The partial slot of the piece of
+// segment sigma = b * Hkv + g held by CTA c is c + sigma (unique: CTA ranges
+// are ordered).
 struct WsLayout {
-  size_t ml, o, total;
+  size_t cnt, ml, o, total;
 };
 
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -152,8 +158,9 @@ static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 static WsLayout ws_layout(int B, int G, int Hkv, int DH, int P) {
   WsLayout w;
   const size_t slots = static_cast<size_t>(P) + static_cast<size_t>(B) * Hkv;
-  w.ml = 0;
-  w.o = round256(slots * G * 2 * sizeof(float));
+  w.cnt = 0;  // a fixed-size table, so every batch shape reuses the same zeroed counters
+  w.ml = round256(sizeof(uint32_t) * static_cast<size_t>(kMaxSegments));
+  w.o = w.ml + round256(slots * G * 2 * sizeof(float));
   w.total = w.o + round256(slots * G * DH * sizeof(float));
   return w;
 }
@@ -227,22 +234,35 @@ KVQ_DEVI int seq_pages(int raw_len, int max_blocks, int window) {
 // V, i.e. the pages between the page counts at those two cost positions, so
 // a CTA of many short segments gets fewer pages.
 // Pages before cost position v (0 <= v <= V).
-KVQ_DEVI int64_t pages_before(const int32_t* seq_off, const int32_t* vseq_off, int B, int Hkv,
-                              int64_t v) {
+// All offsets stay below 2^31 (checked on the host), so 32-bit division does.
+KVQ_DEVI int pages_before(const int32_t* seq_off, const int32_t* vseq_off, int B, int Hkv, int v) {
   if (v >= vseq_off[B]) return seq_off[B];
   const int b = find_seq(vseq_off, B, v);
   const int pages = (seq_off[b + 1] - seq_off[b]) / Hkv;
-  const int64_t r = v - vseq_off[b];
-  const int64_t g = r / (pages + kPieceCost);
-  const int64_t in = r - g * (pages + kPieceCost) - kPieceCost;  // < 0: in the fixed cost
+  const int r = v - vseq_off[b];
+  const int g = r / (pages + kPieceCost);
+  const int in = r - g * (pages + kPieceCost) - kPieceCost;  // < 0: in the fixed cost
   return seq_off[b] + g * pages + (in < 0 ? 0 : (in > pages ? pages : in));
 }
 
-// First unit of CTA c (c = Pe gives the total W).
-KVQ_DEVI int64_t cta_first_unit(const int32_t* seq_off, const int32_t* vseq_off, int B, int Hkv,
-                                int64_t c, int64_t Pe) {
-  const int64_t V = vseq_off[B];
-  return pages_before(seq_off, vseq_off, B, Hkv, c * V / Pe);
+// floor(c V / Pe) for c <= Pe < 2^16, V < 2^31: the binary64 quotient of the
+// exact product rounds to within far less than the 1 / Pe gap to the next
+// integer, so its floor is exact.
+KVQ_DEVI int cost_split(int c, int V, int Pe) {
+  return static_cast<int>(floor(static_cast<double>(c) * V / Pe));
+}
+
+// CTA holding unit u: the last c < Pe with ub[c] <= u (empty CTAs skipped).
+KVQ_DEVI int cta_of(const int32_t* ub, int Pe, int64_t u) {
+  int lo = 0, hi = Pe - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ub[mid] <= u)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
 }
 
 template <bool SCALED>
@@ -597,6 +617,106 @@ KVQ_DEVI void q_fragments(const uint32_t (&w)[DH / 8], uint32_t (&qb)[DH / 16][2
   }
 }
 
+// Merge of the partial states of a segment split across CTAs, run by the
+// consumer threads of the CTA that completed the segment's last piece.
+//   M = max_c m_c,  l = sum_c l_c 2^(m_c - M),  O = sV sum_c o_c 2^(m_c - M) / l
+// Warp w forms M, the weights 2^(m_c - M) (into wgt, [n][G]) and l of heads
+// w, w + 4, ...; then every thread sums a float4 of O over the pieces.  The
+// pieces' o vectors come either from so, a shared-memory copy the caller has
+// started (bulk copy completing on sbar, phase 0), or straight from global
+// memory (independent loads, 16 in flight).
+template <int DH>
+KVQ_DEVI void merge_segment(const DecodeParams& p, int b, int gkv, int64_t sigma, int64_t c_lo,
+                            int n, float sv, float* wgt, const float* so, uint64_t* sbar,
+                            volatile uint32_t* abort_flag, int ctid) {
+  const int G = p.G;
+  constexpr int NT = kConsumerWarps * 32;
+  constexpr int KR = 10;  // pieces per lane kept in registers (n <= 320 in one pass)
+  const int lane = ctid & 31, warp = ctid >> 5;
+  uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + gkv * G) * DH;
+  const bool ok = guard(c_lo >= 0 && c_lo + n - 1 + sigma < p.n_slots && n <= p.P, p.status, 5);
+  float* Lh = wgt + static_cast<size_t>(n) * G;  // [G]
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + (c_lo + sigma) * G;
+  for (int h = warp; ok && h < G; h += kConsumerWarps) {
+    float2 v[KR];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int c = lane + 32 * k;
+      v[k] = c < n ? __ldcg(ml + c * G + h) : make_float2(-INFINITY, 0.f);
+      M = fmaxf(M, v[k].x);
+    }
+    for (int c = lane + 32 * KR; c < n; c += 32) M = fmaxf(M, __ldcg(ml + c * G + h).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    float L = 0.f;
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int c = lane + 32 * k;
+      if (c < n) {
+        const float w = (v[k].x == -INFINITY) ? 0.f : fast_exp2(v[k].x - M);
+        wgt[c * G + h] = w;
+        L += v[k].y * w;
+      }
+    }
+    for (int c = lane + 32 * KR; c < n; c += 32) {
+      const float2 x = __ldcg(ml + c * G + h);
+      const float w = (x.x == -INFINITY) ? 0.f : fast_exp2(x.x - M);
+      wgt[c * G + h] = w;
+      L += x.y * w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+    if (lane == 0) Lh[h] = L;
+  }
+  consumer_bar();
+  bool staged = so != nullptr;
+  if (staged && !mbar_wait(sbar, 0u)) {
+    staged = false;
+    if (ctid == 0) {
+      *abort_flag = 1u;
+      flag_status(p.status, KVQ_DEV_WAIT_TIMEOUT);
+    }
+  }
+  const int n4 = G * DH / 4;
+  if (ok && (so == nullptr || staged)) {
+    const float4* ob = staged ? reinterpret_cast<const float4*>(so)
+                              : reinterpret_cast<const float4*>(p.ws_o + (c_lo + sigma) * G * DH);
+    for (int q4 = ctid; q4 < n4; q4 += NT) {
+      const int h = (4 * q4) / DH;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (staged) {
+#pragma unroll 8
+        for (int c = 0; c < n; ++c) {
+          const float w = wgt[c * G + h];
+          const float4 v = ob[static_cast<int64_t>(c) * n4 + q4];
+          acc.x += w * v.x;
+          acc.y += w * v.y;
+          acc.z += w * v.z;
+          acc.w += w * v.w;
+        }
+      } else {
+#pragma unroll 16
+        for (int c = 0; c < n; ++c) {
+          const float w = wgt[c * G + h];
+          const float4 v = __ldcg(ob + static_cast<int64_t>(c) * n4 + q4);
+          acc.x += w * v.x;
+          acc.y += w * v.y;
+          acc.z += w * v.z;
+          acc.w += w * v.w;
+        }
+      }
+      const float ls = Lh[h];
+      const float f = ls > 0.f ? sv / ls : 0.f;
+      uint2 packed;
+      packed.x = f32x2_to_bf16x2(acc.x * f, acc.y * f);
+      packed.y = f32x2_to_bf16x2(acc.z * f, acc.w * f);
+      *reinterpret_cast<uint2*>(out + 4 * q4) = packed;
+    }
+  }
+  consumer_bar();
+}
+
 // --------------------------------------------------------------------------
 // Decode kernel
 // --------------------------------------------------------------------------
@@ -617,15 +737,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   uint64_t* empty = full + S;
   uint32_t* bad_s = reinterpret_cast<uint32_t*>(smem + SL::flags);
   volatile uint32_t* abort_flag = bad_s + S;
+  volatile uint32_t* merge_s = bad_s + S + 1;
   int32_t* warp_tot = reinterpret_cast<int32_t*>(bad_s + S + 2);  // [8]
   int32_t* last_s = warp_tot + 8;  // [S] last position issued into each slot
+  volatile uint32_t* mcopy_s = reinterpret_cast<volatile uint32_t*>(last_s + S);  // merge copy issued
+  uint64_t* mbar = empty + S;  // completion of the segment-merge bulk copy
   float* cm = reinterpret_cast<float*>(smem + SL::comb);   // [warps][G] running max
   float* cl = cm + kConsumerWarps * p.G;                   // [warps][G] denominators
   float* co = cl + kConsumerWarps * p.G;                   // [warps][G][DH] unnormalised O
-  int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq(p.G));  // [B+1]
+  int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq(p.G, p.P));  // [B+1]
   int32_t* len_s = seq_off + p.B + 1;                                  // [B]
   int32_t* vseq_off = len_s + p.B;                                     // [B+1]
-  float* sk_s = reinterpret_cast<float*>(smem + SL::scales(p.G, p.B)); // [Hkv]
+  int32_t* ub = vseq_off + p.B + 1;                                    // [P+1] first unit of CTA c
+  float* sk_s = reinterpret_cast<float*>(smem + SL::scales(p.G, p.P, p.B)); // [Hkv]
   float* sv_s = sk_s + p.Hkv;                                          // [Hkv]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -636,7 +760,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     last_s[tid] = -1;
     fence_mbar_init();
   } else if (tid == S) {
+    mbar_init(mbar, 1);
+    *mcopy_s = 0u;
     *abort_flag = 0u;
+    fence_mbar_init();
   }
   if (warp == kConsumerWarps && lane == 0) {
     tma_prefetch_desc(&tmk);
@@ -644,9 +771,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   }
   // Inputs may come from the kernel before this one on the stream: wait for
   // it here, or -- under KVQ_CACHE_READY -- only before reading q or a
-  // sequence's last page and before the first write.  The merge kernel that
-  // follows is released once every CTA is past that wait, so it may read
-  // seq_lens right away.
+  // sequence's last page and before the first write.
   if (!p.early) {
     pdl_wait();
     pdl_allow_next();
@@ -664,12 +789,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   };
   if (!p.early) zero_empty_rows(tid, kThreads);
   // Partition size: never more CTAs than units (the others idle).  CTA c
-  // takes units [u0, u1), a cost-balanced range; a CTA whose cost range lies
-  // in one segment's fixed cost may get none.
-  const int64_t Pe = W < p.P ? W : p.P;
-  const int64_t c = blockIdx.x;
-  const int64_t u0 = c < Pe ? cta_first_unit(seq_off, vseq_off, p.B, p.Hkv, c, Pe) : 0;
-  const int64_t u1 = c < Pe ? cta_first_unit(seq_off, vseq_off, p.B, p.Hkv, c + 1, Pe) : 0;
+  // takes units [ub[c], ub[c + 1]), a cost-balanced range; a CTA whose cost
+  // range lies in one segment's fixed cost may get none.
+  const int Pe = static_cast<int>(W < p.P ? W : p.P);
+  if (Pe > 0) {
+    const int V = vseq_off[p.B];
+    for (int cc = tid; cc <= Pe; cc += kThreads)
+      ub[cc] = pages_before(seq_off, vseq_off, p.B, p.Hkv, cost_split(cc, V, Pe));
+  }
+  __syncthreads();
+  const int c = blockIdx.x;
+  const int64_t u0 = c < Pe ? ub[c] : 0;
+  const int64_t u1 = c < Pe ? ub[c + 1] : 0;
   const int64_t total = u1 - u0;
 
   if (warp == kConsumerWarps) {
@@ -957,6 +1088,51 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         }
       }
       consumer_bar();
+      if (!single) {
+        // Publish this piece; the CTA whose piece completes the segment merges
+        // all of its pieces and resets the segment's counter.
+        const int64_t sigma = static_cast<int64_t>(b) * p.Hkv + gkv;
+        const int64_t us = seq_off[b] + static_cast<int64_t>(gkv) * pages, ue = us + pages;
+        const int64_t c_lo = cta_of(ub, Pe, us);      // CTA holding unit us
+        const int64_t c_hi = cta_of(ub, Pe, ue - 1);  // CTA holding unit ue - 1
+        const int npieces = static_cast<int>(c_hi - c_lo + 1);
+        // The barrier above orders every thread's partial stores before
+        // thread 0's fence and arrival (release); the arrival that completes
+        // the count is followed by a fence (acquire) and the barrier below.
+        if (ctid == 0) {
+          __threadfence();
+          const uint32_t prev = atomicAdd(p.ws_cnt + sigma, 1u);
+          const bool last = prev + 1 == static_cast<uint32_t>(npieces);
+          if (last) __threadfence();
+          merge_s[0] = last ? 1u : 0u;
+        }
+        consumer_bar();
+        if (merge_s[0]) {
+          // After the CTA's last piece the ring is idle (every issued page
+          // has been consumed): the pieces' o vectors are bulk-copied into it
+          // while the weights are formed.
+          const uint32_t pbytes = static_cast<uint32_t>(p.G * DH * sizeof(float));
+          const bool stage = (u + n == u1) && !*abort_flag && c_lo >= 0 && npieces <= p.P &&
+                             c_lo + sigma + npieces <= p.n_slots &&
+                             static_cast<size_t>(npieces) * pbytes <= static_cast<size_t>(S) * C::kSlot;
+          if (stage && warp == 0) {
+            if (lane == 0) {
+              *mcopy_s = 1u;
+              mbar_arrive_expect_tx(mbar, npieces * pbytes);
+            }
+            __syncwarp();
+            fence_proxy_async();
+            const float* src = p.ws_o + (c_lo + sigma) * p.G * DH;
+            for (int c = lane; c < npieces; c += 32)
+              bulk_load(ring + static_cast<size_t>(c) * pbytes, src + static_cast<size_t>(c) * p.G * DH,
+                        pbytes, mbar);
+          }
+          merge_segment<DH>(p, b, gkv, sigma, c_lo, npieces, sv, cm,
+                            stage ? reinterpret_cast<const float*>(ring) : nullptr, mbar, abort_flag,
+                            ctid);
+          if (ctid == 0) p.ws_cnt[sigma] = 0u;
+        }
+      }
       pos_base += n;
       u += n;
     }
@@ -966,349 +1142,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   if (*abort_flag && tid == 0) {
     for (int s = 0; s < S; ++s)
       if (last_s[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>((last_s[s] / S) & 1));
+    if (*mcopy_s) mbar_wait(mbar, 0u);
   }
-}
-
-// --------------------------------------------------------------------------
-// Merge kernel: segments split across CTAs
-// --------------------------------------------------------------------------
-
-constexpr int kMergeThreads = 128;
-constexpr int kMergeWarps = kMergeThreads / 32;
-// Merge CTAs stay resident beside two decode CTAs per SM: at most 80
-// registers a thread (launch bound of 6 CTAs of 128 threads).
-constexpr int kMergeMinBlocks = 6;
-constexpr int kMergeSmallN = 8;  // pieces up to which one warp merges a whole head row
-
-struct MergeParams {
-  const int32_t* seq_lens;
-  int B, Hkv, G, Hq, window, max_blocks, P;
-  const float* vs;  // per-head or per-tensor V scales; nullptr = 1 (bf16 cache)
-  int per_head;
-  const float* ws_ml;
-  const float* ws_o;
-  uint16_t* out;
-  int64_t n_slots;
-  uint32_t* status;
-};
-
-template <int NV> struct VecF;
-template <> struct VecF<1> { using T = float; };
-template <> struct VecF<2> { using T = float2; };
-template <> struct VecF<4> { using T = float4; };
-
-KVQ_DEVI void fma_vec(float4& a, float w, const float4& v) {
-  a.x += w * v.x; a.y += w * v.y; a.z += w * v.z; a.w += w * v.w;
-}
-KVQ_DEVI void fma_vec(float2& a, float w, const float2& v) { a.x += w * v.x; a.y += w * v.y; }
-KVQ_DEVI void fma_vec(float& a, float w, const float& v) { a += w * v; }
-KVQ_DEVI void store_bf16(uint16_t* dst, const float4& a, float f) {
-  uint2 pk;
-  pk.x = f32x2_to_bf16x2(a.x * f, a.y * f);
-  pk.y = f32x2_to_bf16x2(a.z * f, a.w * f);
-  *reinterpret_cast<uint2*>(dst) = pk;
-}
-KVQ_DEVI void store_bf16(uint16_t* dst, const float2& a, float f) {
-  *reinterpret_cast<uint32_t*>(dst) = f32x2_to_bf16x2(a.x * f, a.y * f);
-}
-KVQ_DEVI void store_bf16(uint16_t* dst, const float& a, float f) {
-  *dst = static_cast<uint16_t>(f32x2_to_bf16x2(a * f, 0.f));
-}
-
-// One warp merges NV consecutive dims per lane, starting at dim d0 + NV * lane,
-// of head h over the n pieces whose partial slots start at s0.  The o loads
-// of the first CH pieces and the (m, l) of pieces lane and lane + 32 are all
-// issued before anything waits, so up to CH pieces take one memory round
-// trip; later batches of CH follow.  The weight of piece c is taken from lane
-// c % 32 (pieces past 64 reload theirs).
-template <int DH, int NV, int CH>
-KVQ_DEVI void merge_warp(const MergeParams& p, int64_t s0, int n, int h, int64_t out_row, float sv,
-                         int d0, int lane) {
-  using V = typename VecF<NV>::T;
-  const V* o_v = reinterpret_cast<const V*>(p.ws_o);
-  const float2* ml2 = reinterpret_cast<const float2*>(p.ws_ml);
-  const int col = d0 / NV + lane;
-  auto o_at = [&](int cc) { return __ldcg(o_v + ((s0 + cc) * p.G + h) * (DH / NV) + col); };
-  V A[CH];
-#pragma unroll
-  for (int k = 0; k < CH; ++k) A[k] = k < n ? o_at(k) : V{};
-  const float2 x0 = lane < n ? __ldcg(ml2 + (s0 + lane) * p.G + h) : make_float2(-INFINITY, 0.f);
-  const float2 x1 =
-      lane + 32 < n ? __ldcg(ml2 + (s0 + lane + 32) * p.G + h) : make_float2(-INFINITY, 0.f);
-  float M = fmaxf(x0.x, x1.x);
-  for (int cc = lane + 64; cc < n; cc += 32) M = fmaxf(M, __ldcg(ml2 + (s0 + cc) * p.G + h).x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-  auto weight = [&](float m) { return (m == -INFINITY) ? 0.f : fast_exp2(m - M); };
-  const float w0 = weight(x0.x), w1 = weight(x1.x);
-  float L = x0.y * w0 + x1.y * w1;
-  for (int cc = lane + 64; cc < n; cc += 32) {
-    const float2 x = __ldcg(ml2 + (s0 + cc) * p.G + h);
-    L += x.y * weight(x.x);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
-  V acc{};
-  for (int base = 0; base < n; base += CH) {
-    if (base > 0) {
-#pragma unroll
-      for (int k = 0; k < CH; ++k) A[k] = base + k < n ? o_at(base + k) : V{};
-    }
-#pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      const int cc = base + k;  // warp-uniform
-      if (cc < n) {
-        const float w = cc < 32 ? __shfl_sync(kFull, w0, cc)
-                        : cc < 64 ? __shfl_sync(kFull, w1, cc - 32)
-                                  : weight(__ldcg(ml2 + (s0 + cc) * p.G + h).x);
-        fma_vec(acc, w, A[k]);
-      }
-    }
-  }
-  const float f = L > 0.f ? sv / L : 0.f;
-  store_bf16(p.out + out_row * DH + d0 + NV * lane, acc, f);
-}
-
-constexpr int kMergeStage = 40;  // 128-byte slices of pieces staged per warp and batch
-
-// Merge of one 32-dim slice (dims d0 .. d0 + 31) of head h over n pieces,
-// for segments cut into many pieces: the slice of every piece (128 bytes)
-// is bulk-copied into this warp's shared-memory stage (up to kMergeStage
-// pieces a batch, one mbarrier), which keeps them all in flight at once;
-// lane l then sums dim d0 + l over the staged pieces.
-template <int DH>
-KVQ_DEVI bool merge_warp_staged(const MergeParams& p, int64_t s0, int n, int h, int64_t out_row,
-                                float sv, int d0, int lane, float* stage, float* wsm, uint64_t* bar,
-                                uint32_t& phase) {
-  const float2* ml2 = reinterpret_cast<const float2*>(p.ws_ml);
-  auto issue = [&](int base) {
-    const int cnt = min(kMergeStage, n - base);
-    __syncwarp();
-    fence_proxy_async_smem();  // this warp's earlier reads of the stage come first
-    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * 128u);
-    __syncwarp();
-    for (int k = lane; k < cnt; k += 32)
-      bulk_load(stage + 32 * k, p.ws_o + ((s0 + base + k) * p.G + h) * DH + d0, 128u, bar);
-  };
-  issue(0);  // the copies go first, so the (m, l) loads below overlap them
-  const float2 x0 = lane < n ? __ldcg(ml2 + (s0 + lane) * p.G + h) : make_float2(-INFINITY, 0.f);
-  const float2 x1 =
-      lane + 32 < n ? __ldcg(ml2 + (s0 + lane + 32) * p.G + h) : make_float2(-INFINITY, 0.f);
-  float M = fmaxf(x0.x, x1.x);
-  for (int cc = lane + 64; cc < n; cc += 32) M = fmaxf(M, __ldcg(ml2 + (s0 + cc) * p.G + h).x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-  auto weight = [&](float m) { return (m == -INFINITY) ? 0.f : fast_exp2(m - M); };
-  const float w0 = weight(x0.x), w1 = weight(x1.x);
-  float L = x0.y * w0 + x1.y * w1;
-  for (int cc = lane + 64; cc < n; cc += 32) {
-    const float2 x = __ldcg(ml2 + (s0 + cc) * p.G + h);
-    L += x.y * weight(x.x);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
-  wsm[lane] = w0;  // weights of pieces 0 .. 63 for the lanes to broadcast
-  wsm[lane + 32] = w1;
-  __syncwarp();
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int base = 0; base < n; base += kMergeStage) {
-    if (base > 0) issue(base);
-    if (!mbar_wait(bar, phase)) {  // timed out: give the copies one more bounded wait, stop
-      if (lane == 0) flag_status(p.status, KVQ_DEV_WAIT_TIMEOUT);
-      mbar_wait(bar, phase);
-      return false;
-    }
-    phase ^= 1u;
-    const int cnt = min(kMergeStage, n - base);
-    for (int k0 = 0; k0 < cnt; k0 += 4) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int k = k0 + i, cc = base + k;  // warp-uniform
-        if (k < cnt) {
-          const float w = cc < 64 ? wsm[cc] : weight(__ldcg(ml2 + (s0 + cc) * p.G + h).x);
-          acc[i] += w * stage[32 * k + lane];
-        }
-      }
-    }
-  }
-  const float f = L > 0.f ? sv / L : 0.f;
-  store_bf16(p.out + out_row * DH + d0 + lane, (acc[0] + acc[1]) + (acc[2] + acc[3]), f);
-  __syncwarp();  // wsm is rewritten by the next item
-  return true;
-}
-
-// Block-wide exclusive scan of one int per thread (kMergeThreads threads);
-// returns the total.  tot is kMergeWarps ints of shared scratch.
-KVQ_DEVI int merge_block_scan(int v, int& excl, int32_t* tot) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int t = __shfl_up_sync(kFull, incl, off);
-    if (lane >= off) incl += t;
-  }
-  if (lane == 31) tot[warp] = incl;
-  __syncthreads();
-  int base = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) {
-    base += w < warp ? tot[w] : 0;
-    total += tot[w];
-  }
-  excl = base + incl - v;
-  __syncthreads();
-  return total;
-}
-
-// The partial states (m_c, l_c, o_c) of the n pieces of a split segment
-// sigma, head h:
-//   M = max_c m_c,  w_c = 2^(m_c - M),  L = sum_c l_c w_c,
-//   O = sV sum_c w_c o_c / L   (the bf16 output row).
-// A segment is split exactly where a CTA boundary falls inside it, so the
-// split segments are found from the boundaries c = 1 .. Pe-1: boundary c
-// owns the segment holding CTA c's first unit if that unit is not the
-// segment's first and CTA c - 1 holds the segment's first piece.  Before
-// waiting for the decode kernel, every CTA lists the owning boundaries and
-// their warp items in shared memory: a segment of at most kMergeSmallN
-// pieces gives one item per head (one warp merges the whole row, four dims
-// a lane), a longer one DH/32 items per head (one 32-dim slice each, its
-// pieces bulk-copied into shared memory), so every item needs about one
-// memory round trip.  The grid is one small CTA
-// per SM, so it stays resident beside the next decode kernel.
-template <int DH>
-__global__ void __launch_bounds__(kMergeThreads, kMergeMinBlocks)
-    merge_kernel(const __grid_constant__ MergeParams p) {
-  constexpr int NS = DH / 32;  // 32-dim slices of a head row
-  extern __shared__ uint8_t smem_raw[];
-  int32_t* seq_off = reinterpret_cast<int32_t*>(smem_raw);  // [B + 1]
-  int32_t* vseq_off = seq_off + p.B + 1;                     // [B + 1]
-  int32_t* ub = vseq_off + p.B + 1;                          // [P + 1] first unit of CTA c
-  int32_t* item_off = ub + p.P + 1;                          // [P + 1] first item of boundary c
-  int32_t* own_n = item_off + p.P + 1;                       // [P] pieces (owners only)
-  int32_t* own_b = own_n + p.P;                              // [P] sequence
-  int32_t* own_g = own_b + p.P;                              // [P] KV head
-  float* sv_s = reinterpret_cast<float*>(own_g + p.P);       // [Hkv] V scales
-  __shared__ int32_t tot[kMergeWarps];
-  __shared__ __align__(16) float stage_all[kMergeWarps][kMergeStage * 32];
-  __shared__ float wsm_all[kMergeWarps][64];
-  __shared__ __align__(8) uint64_t bars[kMergeWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (lane == 0) {
-    mbar_init(&bars[warp], 1);
-    fence_mbar_init();
-  }
-  uint32_t phase = 0;
-  pdl_allow_next();
-  for (int g = tid; g < p.Hkv; g += kMergeThreads)  // scales are inputs of the decode call
-    sv_s[g] = p.vs ? __ldg(p.vs + (p.per_head ? g : 0)) : 1.f;
-  // This kernel starts only once every decode CTA is past its own wait, so
-  // seq_lens is final and the work list can be built before waiting; the
-  // partial states need the decode kernel complete.
-  {  // seq_off, vseq_off: the decode kernel's plan (pages and cost per sequence)
-    const int per = (p.B + kMergeThreads - 1) / kMergeThreads;
-    const int b0 = tid * per, b1 = min(p.B, b0 + per);
-    int local = 0, vlocal = 0;
-    for (int b = b0; b < b1; ++b) {
-      const int pages = seq_pages(__ldg(p.seq_lens + b), p.max_blocks, p.window);
-      seq_off[b] = local;
-      vseq_off[b] = vlocal;
-      local += pages * p.Hkv;
-      vlocal += pages > 0 ? (pages + kPieceCost) * p.Hkv : 0;
-    }
-    int excl, vexcl;
-    const int total = merge_block_scan(local, excl, tot);
-    const int vtotal = merge_block_scan(vlocal, vexcl, tot);
-    for (int b = b0; b < b1; ++b) {
-      seq_off[b] += excl;
-      vseq_off[b] += vexcl;
-    }
-    if (tid == 0) {
-      seq_off[p.B] = total;
-      vseq_off[p.B] = vtotal;
-    }
-    __syncthreads();
-  }
-  const int64_t W = seq_off[p.B];
-  const int64_t Pe = W < p.P ? W : p.P;
-  for (int c = tid; c <= Pe; c += kMergeThreads)
-    ub[c] = static_cast<int32_t>(cta_first_unit(seq_off, vseq_off, p.B, p.Hkv, c, Pe));
-  __syncthreads();
-  // CTA holding unit u: the last c < Pe with ub[c] <= u (empty CTAs skipped).
-  auto cta_of = [&](int64_t u) {
-    int lo = 0, hi = static_cast<int>(Pe) - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (ub[mid] <= u)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    return lo;
-  };
-  {  // owning boundaries and their item counts
-    const int nb = static_cast<int>(Pe > 1 ? Pe - 1 : 0);  // boundaries 1 .. Pe-1
-    const int per = (nb + kMergeThreads - 1) / kMergeThreads;
-    const int k0 = tid * per, k1 = min(nb, k0 + per);
-    int local = 0;
-    for (int k = k0; k < k1; ++k) {
-      const int c = k + 1;
-      const int64_t u = ub[c];  // first unit of CTA c
-      int cnt = 0;
-      if (u < W && u > ub[c - 1]) {  // CTA c - 1 holds units; u is inside W
-        const int b = find_seq(seq_off, p.B, u);
-        const int pages = (seq_off[b + 1] - seq_off[b]) / p.Hkv;
-        const int g = static_cast<int>((u - seq_off[b]) / pages);
-        const int64_t us = seq_off[b] + static_cast<int64_t>(g) * pages;
-        // split at c, and c - 1 holds the segment's first unit
-        if (u != us && ub[c - 1] <= us) {
-          const int n = cta_of(us + pages - 1) - (c - 1) + 1;
-          own_n[k] = n;
-          own_b[k] = b;
-          own_g[k] = g;
-          cnt = p.G * (n <= kMergeSmallN ? 1 : NS);
-        }
-      }
-      item_off[k] = local;
-      local += cnt;
-    }
-    int excl;
-    const int total = merge_block_scan(local, excl, tot);
-    for (int k = k0; k < k1; ++k) item_off[k] += excl;
-    if (tid == 0) item_off[nb] = total;
-    __syncthreads();
-  }
-  // Every CTA waits, so this kernel never completes before the decode kernel.
-  pdl_wait();
-  fence_proxy_async_global();  // the partial states are read through bulk copies too
-  const int nb = static_cast<int>(Pe > 1 ? Pe - 1 : 0);
-  const int items = item_off[nb];
-  for (int it = blockIdx.x * kMergeWarps + warp; it < items; it += gridDim.x * kMergeWarps) {
-    int lo = 0, hi = nb - 1;  // last boundary k with item_off[k] <= it
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (item_off[mid] <= it)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    const int k = lo, r = it - item_off[k];
-    const int n = own_n[k], b = own_b[k], g = own_g[k];
-    const bool small = n <= kMergeSmallN;
-    const int h = small ? r : r / NS, j = small ? 0 : r - (r / NS) * NS;
-    const int64_t s0 = static_cast<int64_t>(k) + static_cast<int64_t>(b) * p.Hkv + g;  // c_lo = k
-    if (!guard(s0 + n <= p.n_slots && n <= p.P && h < p.G, p.status, 12)) continue;
-    const float sv = sv_s[g];
-    const int64_t out_row = static_cast<int64_t>(b) * p.Hq + g * p.G + h;
-    if (small)
-      merge_warp<DH, DH / 32, kMergeSmallN>(p, s0, n, h, out_row, sv, 0, lane);
-    else if (!merge_warp_staged<DH>(p, s0, n, h, out_row, sv, 32 * j, lane, stage_all[warp],
-                                     wsm_all[warp], &bars[warp], phase))
-      break;
-  }
-}
-
-static size_t merge_smem_bytes(int B, int P, int Hkv) {
-  return (2 * (static_cast<size_t>(B) + 1) + 5 * static_cast<size_t>(P) + 2 + Hkv) * sizeof(int32_t);
 }
 
 // --------------------------------------------------------------------------
@@ -1352,21 +1187,20 @@ static bool make_cache_map(CUtensorMap* m, const void* base, int fmt, int dh, ui
 }
 
 template <int FMT, int DH>
-static size_t smem_bytes(int G, int B, int Hkv) {
-  return SmemLayout<FMT, DH>::total(G, B, Hkv);
+static size_t smem_bytes(int G, int P, int B, int Hkv) {
+  return SmemLayout<FMT, DH>::total(G, P, B, Hkv);
 }
 
 template <int FMT, int DH>
 static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                   cudaStream_t s) {
-  const size_t smem = smem_bytes<FMT, DH>(p.G, p.B, p.Hkv);
+  const size_t smem = smem_bytes<FMT, DH>(p.G, p.P, p.B, p.Hkv);
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    const int maxsmem = static_cast<int>(smem_bytes<FMT, DH>(kMaxGroup, kMaxSeqs, kMaxKvHeads));
-    // Both kernels ask for the largest shared-memory carveout, so a merge CTA
-    // can sit on an SM beside two decode CTAs (of this call or the next).
+    const int maxsmem = static_cast<int>(smem_bytes<FMT, DH>(kMaxGroup, kCtasPerSM * device_sm_count(), kMaxSeqs, kMaxKvHeads));
+    // The largest shared-memory carveout, so that two CTAs fit on every SM.
     if (cudaFuncSetAttribute(decode_kernel<FMT, DH, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, maxsmem) != cudaSuccess ||
         cudaFuncSetAttribute(decode_kernel<FMT, DH, false>,
@@ -1376,40 +1210,13 @@ static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMa
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaFuncSetAttribute(decode_kernel<FMT, DH, false>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-        cudaFuncSetAttribute(merge_kernel<DH>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return KVQ_ERR_CUDA;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  cudaError_t e =
+  const cudaError_t e =
       p.G <= 4 ? launch_pdl(decode_kernel<FMT, DH, true>, dim3(p.P), dim3(kThreads), smem, s, p, tk, tv)
                : launch_pdl(decode_kernel<FMT, DH, false>, dim3(p.P), dim3(kThreads), smem, s, p, tk, tv);
-  if (e != cudaSuccess) return KVQ_ERR_CUDA;
-  // The merge of split segments, a programmatic dependent of the decode kernel.
-  MergeParams m;
-  m.seq_lens = p.seq_lens;
-  m.B = p.B;
-  m.Hkv = p.Hkv;
-  m.G = p.G;
-  m.Hq = p.Hq;
-  m.window = p.window;
-  m.max_blocks = p.max_blocks;
-  m.P = p.P;
-  m.vs = p.vs;
-  m.per_head = p.per_head;
-  m.ws_ml = p.ws_ml;
-  m.ws_o = p.ws_o;
-  m.out = p.out;
-  m.n_slots = p.n_slots;
-  m.status = p.status;
-  // Warp items (CTA boundary, head, 32-dim slice); boundaries past the units
-  // of a small batch exit at once.  At most one CTA per SM.
-  const int64_t items = static_cast<int64_t>(p.P - 1) * p.G * (DH / 32);
-  const int64_t need = (items + kMergeWarps - 1) / kMergeWarps;
-  const int64_t cap = static_cast<int64_t>(device_sm_count());
-  const int grid = static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
-  e = launch_pdl(merge_kernel<DH>, dim3(grid), dim3(kMergeThreads), merge_smem_bytes(p.B, p.P, p.Hkv), s, m);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
@@ -1498,6 +1305,7 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   p.early = (flags & KVQ_CACHE_READY) ? 1 : 0;
   p.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt);
   p.ws_ml = reinterpret_cast<float*>(ws + wl.ml);
   p.ws_o = reinterpret_cast<float*>(ws + wl.o);
   p.out = static_cast<uint16_t*>(out);

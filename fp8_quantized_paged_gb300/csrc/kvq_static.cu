@@ -56,8 +56,8 @@ extern "C" int kvq_decode_attn_static(const void* q, const void* k_cache, const 
   if (need > kScratchBytes) return KVQ_ERR_WORKSPACE;
   std::call_once(g_once[dev], look_up_scratch, dev);
   if (!g_scratch_ptr[dev]) return KVQ_ERR_CUDA;
-  // Every byte of the array that a call reads was written earlier in the
-  // same call, so it needs no initialisation.
+  // The array's counters are zero at load, and every completed call leaves
+  // them zero; the rest is overwritten before it is read.
   return kvq_decode_attn(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                          num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
                          q_scale, q_scale_len, k_scale, k_scale_len, v_scale, v_scale_len,

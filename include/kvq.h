@@ -95,6 +95,11 @@ typedef enum {
 #define KVQ_DEV_INTERNAL 16u    /* an internal index guard failed (bits 16..31 name it); */
                                 /* the access was skipped and the output is invalid      */
 
+/* Bytes at the start of every decode workspace that must be zero before the
+ * first call: the arrival counters of kvq_decode_attn, one 32-bit word per
+ * (sequence, KV head), in a fixed-size table whatever the batch shape. */
+#define KVQ_WS_COUNTER_BYTES ((size_t)65536 * 4u)
+
 /* Flags of kvq_decode_attn. */
 #define KVQ_Q_FP8 1u /* reserved: FP8-domain attention with Q quantized; not built */
 #define KVQ_CACHE_READY 2u /* start before the preceding kernel ends; see kvq_decode_attn */
@@ -173,13 +178,16 @@ KVQ_API size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_
  *                   or a decode of another layer).
  *   workspace       device scratch of at least
  *                   kvq_decode_workspace_size(num_seqs, ...) bytes, 256-byte
- *                   aligned, for the partial softmax states of (sequence,
- *                   KV head) segments split across CTAs.  It needs no
- *                   initialisation.  Successive calls on one stream may
- *                   share it (each call writes it only after the kernel
- *                   before it has completed, with or without
- *                   KVQ_CACHE_READY); calls that may run concurrently on
- *                   different streams must not.
+ *                   aligned.  Its first KVQ_WS_COUNTER_BYTES bytes are
+ *                   per-(sequence, KV head) arrival counters: zero them
+ *                   once before the first call (for instance
+ *                   cudaMemsetAsync of the whole buffer); every completed
+ *                   call leaves them zero again (re-zero after a
+ *                   KVQ_DEV_WAIT_TIMEOUT).  The rest needs no initialisation.
+ *                   Successive calls on one stream may share it (each call
+ *                   writes it only after the kernel before it has completed,
+ *                   with or without KVQ_CACHE_READY); calls that may run
+ *                   concurrently on different streams must not.
  *   out             bf16 [num_seqs][num_q_heads][head_dim] (fp32
  *                   accumulation, round to nearest even).
  *   dev_status      optional; KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN,
@@ -217,8 +225,11 @@ KVQ_API int kvq_decode_attn(const void* q, const void* k_cache, const void* v_ca
  * The first call on a device, made with that device current, looks up the
  * array's device address (cudaGetSymbolAddress) and keeps it; make that
  * first call before any stream capture.  All calls on a device share the
- * one array, which keeps the last call's contents; nothing in it needs
- * initialising or clearing.  Calls on one stream are ordered; calls that
+ * one array, which keeps the last call's contents.  Its counters start at
+ * zero (device variables are zero-initialized when the library's device
+ * code is loaded) and every completed call leaves them zero, so nothing
+ * needs clearing unless a call reported KVQ_DEV_WAIT_TIMEOUT.  Calls on one
+ * stream are ordered; calls that
  * may overlap on the GPU (different streams, or different host threads)
  * race on it: serialize them, or give each its own workspace through
  * kvq_decode_attn.

@@ -72,9 +72,10 @@ class DeviceLayer:
         self.out = torch.empty((lay.B, lay.Hq, lay.dh), dtype=torch.bfloat16, device=dev)
 
     def poison_workspace(self):
-        """NaN bytes everywhere, so a read of a partial slot nobody wrote
-        shows up."""
+        """NaN bytes everywhere but the counters (which must stay zero), so a
+        read of a partial slot nobody wrote shows up."""
         self.ws.fill_(0xFF)
+        self.ws[: self.kvq.KVQ_WS_COUNTER_BYTES].zero_()
 
     def write(self, token_idx=None):
         lay = self.lay
