@@ -792,13 +792,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   // takes units [ub[c], ub[c + 1]), a cost-balanced range; a CTA whose cost
   // range lies in one segment's fixed cost may get none.
   const int Pe = static_cast<int>(W < p.P ? W : p.P);
-  if (Pe > 0) {
-    const int V = vseq_off[p.B];
-    for (int cc = tid; cc <= Pe; cc += kThreads)
-      ub[cc] = pages_before(seq_off, vseq_off, p.B, p.Hkv, cost_split(cc, V, Pe));
+  const int c = blockIdx.x;
+  const int V = vseq_off[p.B];
+  // This CTA's own bounds first (two warps); the consumer warps tabulate the
+  // rest while the first pages load (they need it only to publish pieces).
+  if ((tid == 0 || tid == 32) && c < Pe) {
+    const int cc = c + (tid >> 5);
+    ub[cc] = pages_before(seq_off, vseq_off, p.B, p.Hkv, cost_split(cc, V, Pe));
   }
   __syncthreads();
-  const int c = blockIdx.x;
   const int64_t u0 = c < Pe ? ub[c] : 0;
   const int64_t u1 = c < Pe ? ub[c + 1] : 0;
   const int64_t total = u1 - u0;
@@ -920,6 +922,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     int pos_base = 0;
     bool aborted = false;
     // piece = the part of one (sequence, KV head) segment inside [u0, u1)
+    for (int cc = ctid; cc <= Pe; cc += kConsumerWarps * 32)
+      if (cc != c && cc != c + 1) ub[cc] = pages_before(seq_off, vseq_off, p.B, p.Hkv, cost_split(cc, V, Pe));
+    consumer_bar();
     if (p.early) {  // q and every write wait for the previous kernel
       pdl_wait();
       pdl_allow_next();
