@@ -92,8 +92,7 @@ struct Cfg {
 // base): the ring and barriers at fixed offsets, then the merge scratch (the
 // warps' states for the group's G heads, reused for the weights of up to P
 // pieces when a split segment is merged), the plan ([B+1] unit offsets, [B]
-// checked lengths, [B+1] cost offsets, [P+1] first unit of every CTA) and the
-// k/v scales.
+// checked lengths, [B+1] cost offsets) and the k/v scales.
 template <int FMT, int DH>
 struct SmemLayout {
   using C = Cfg<FMT, DH>;
@@ -101,9 +100,9 @@ struct SmemLayout {
   static constexpr size_t ring = 0;
   // full[S], empty[S], and the barrier of the segment-merge bulk copy
   static constexpr size_t bars = ring + static_cast<size_t>(S) * C::kSlot;
-  // bad[S], abort, merge decision, tot[8], last[S], merge copy issued
+  // bad[S], abort, merge decision, tot[8], last[S], merge copy issued, u0, u1
   static constexpr size_t flags = bars + (2 * S + 1) * sizeof(uint64_t);
-  static constexpr size_t comb = (flags + (2 * S + 3 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
+  static constexpr size_t comb = (flags + (2 * S + 5 + 8) * sizeof(uint32_t) + 15) & ~size_t(15);
   __host__ __device__ static size_t comb_floats(int G, int P) {
     const size_t warps = static_cast<size_t>(kConsumerWarps) * G * (DH + 2);
     const size_t pieces = (static_cast<size_t>(P) + 1) * G;
@@ -113,7 +112,7 @@ struct SmemLayout {
     return comb + ((comb_floats(G, P) * sizeof(float) + 15) & ~size_t(15));
   }
   __host__ __device__ static size_t scales(int G, int P, int B) {
-    return seq(G, P) + (3 * static_cast<size_t>(B) + 2 + static_cast<size_t>(P) + 1) * sizeof(int32_t);
+    return seq(G, P) + (3 * static_cast<size_t>(B) + 2) * sizeof(int32_t);
   }
   __host__ __device__ static size_t total(int G, int P, int B, int Hkv) {
     return scales(G, P, B) + 2 * static_cast<size_t>(Hkv) * sizeof(float) + 1024;
@@ -245,25 +244,27 @@ KVQ_DEVI int pages_before(const int32_t* seq_off, const int32_t* vseq_off, int B
   return seq_off[b] + g * pages + (in < 0 ? 0 : (in > pages ? pages : in));
 }
 
-// floor(c V / Pe) for c <= Pe < 2^16, V < 2^31: the binary64 quotient of the
-// exact product rounds to within far less than the 1 / Pe gap to the next
-// integer, so its floor is exact.
-KVQ_DEVI int cost_split(int c, int V, int Pe) {
-  return static_cast<int>(floor(static_cast<double>(c) * V / Pe));
-}
-
-// CTA holding unit u: the last c < Pe with ub[c] <= u (empty CTAs skipped).
-KVQ_DEVI int cta_of(const int32_t* ub, int Pe, int64_t u) {
-  int lo = 0, hi = Pe - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (ub[mid] <= u)
-      lo = mid;
-    else
-      hi = mid - 1;
+// Cost position where CTA c's range starts, floor(c V / Pe), for
+// 0 <= c <= Pe < 2^15 and V < 2^31, in 32-bit integers: with V = a Pe + r,
+// c V / Pe = c a + c r / Pe and c r < Pe^2.
+struct CostSplit {
+  int V, a, r, Pe;
+  KVQ_DEVI CostSplit(int V_, int Pe_)
+      : V(V_), a(Pe_ > 0 ? V_ / Pe_ : 0), r(Pe_ > 0 ? V_ % Pe_ : 0), Pe(Pe_) {}
+  KVQ_DEVI int operator()(int c) const { return c * a + (c * r) / Pe; }
+  // The CTA whose cost range holds cost position v (0 <= v < V, Pe > 0): a
+  // binary32 estimate of ceil((v + 1) Pe / V) - 1, off by at most one, then
+  // corrected against the exact range starts.
+  KVQ_DEVI int cta_of(int v) const {
+    int cc = static_cast<int>(static_cast<float>(v + 1) * static_cast<float>(Pe) / static_cast<float>(V));
+    cc = cc < 0 ? 0 : (cc > Pe - 1 ? Pe - 1 : cc);
+    for (int i = 0; i < 3 && cc > 0 && (*this)(cc) > v; ++i) --cc;
+    for (int i = 0; i < 3 && cc + 1 < Pe && (*this)(cc + 1) <= v; ++i) ++cc;
+    return cc;
   }
-  return lo;
-}
+};
+
+
 
 template <bool SCALED>
 KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s,
@@ -742,13 +743,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   int32_t* last_s = warp_tot + 8;  // [S] last position issued into each slot
   volatile uint32_t* mcopy_s = reinterpret_cast<volatile uint32_t*>(last_s + S);  // merge copy issued
   uint64_t* mbar = empty + S;  // completion of the segment-merge bulk copy
+  int32_t* ub = reinterpret_cast<int32_t*>(const_cast<uint32_t*>(mcopy_s + 1));  // [2] u0, u1
   float* cm = reinterpret_cast<float*>(smem + SL::comb);   // [warps][G] running max
   float* cl = cm + kConsumerWarps * p.G;                   // [warps][G] denominators
   float* co = cl + kConsumerWarps * p.G;                   // [warps][G][DH] unnormalised O
   int32_t* seq_off = reinterpret_cast<int32_t*>(smem + SL::seq(p.G, p.P));  // [B+1]
   int32_t* len_s = seq_off + p.B + 1;                                  // [B]
   int32_t* vseq_off = len_s + p.B;                                     // [B+1]
-  int32_t* ub = vseq_off + p.B + 1;                                    // [P+1] first unit of CTA c
   float* sk_s = reinterpret_cast<float*>(smem + SL::scales(p.G, p.P, p.B)); // [Hkv]
   float* sv_s = sk_s + p.Hkv;                                          // [Hkv]
 
@@ -789,20 +790,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
   };
   if (!p.early) zero_empty_rows(tid, kThreads);
   // Partition size: never more CTAs than units (the others idle).  CTA c
-  // takes units [ub[c], ub[c + 1]), a cost-balanced range; a CTA whose cost
+  // takes units [u0, u1), a cost-balanced range; a CTA whose cost
   // range lies in one segment's fixed cost may get none.
   const int Pe = static_cast<int>(W < p.P ? W : p.P);
   const int c = blockIdx.x;
-  const int V = vseq_off[p.B];
-  // This CTA's own bounds first (two warps); the consumer warps tabulate the
-  // rest while the first pages load (they need it only to publish pieces).
-  if ((tid == 0 || tid == 32) && c < Pe) {
-    const int cc = c + (tid >> 5);
-    ub[cc] = pages_before(seq_off, vseq_off, p.B, p.Hkv, cost_split(cc, V, Pe));
-  }
+  const CostSplit cost_split(vseq_off[p.B], Pe);
+  if ((tid == 0 || tid == 32) && c < Pe)  // this CTA's bounds, two warps in parallel
+    ub[tid >> 5] = pages_before(seq_off, vseq_off, p.B, p.Hkv, cost_split(c + (tid >> 5)));
   __syncthreads();
-  const int64_t u0 = c < Pe ? ub[c] : 0;
-  const int64_t u1 = c < Pe ? ub[c + 1] : 0;
+  const int64_t u0 = c < Pe ? ub[0] : 0;
+  const int64_t u1 = c < Pe ? ub[1] : 0;
   const int64_t total = u1 - u0;
 
   if (warp == kConsumerWarps) {
@@ -922,9 +919,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     int pos_base = 0;
     bool aborted = false;
     // piece = the part of one (sequence, KV head) segment inside [u0, u1)
-    for (int cc = ctid; cc <= Pe; cc += kConsumerWarps * 32)
-      if (cc != c && cc != c + 1) ub[cc] = pages_before(seq_off, vseq_off, p.B, p.Hkv, cost_split(cc, V, Pe));
-    consumer_bar();
     if (p.early) {  // q and every write wait for the previous kernel
       pdl_wait();
       pdl_allow_next();
@@ -942,6 +936,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       piece_at(u0, b, gkv, pages, p0);
       load_q_raw<DH>(p, b, gkv, qhead, t, qraw);
     }
+
     for (int64_t u = u0; u < u1;) {
       int b, gkv, pages, p0;
       piece_at(u, b, gkv, pages, p0);
@@ -952,6 +947,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       const int fp = lo / kBS;
       const float sv = sv_s[gkv];
       const float lscale = sk_s[gkv] * p.logit_scale;
+      const bool single = (p0 == 0 && n == pages);
+      // A split segment's pieces are those of CTAs seg_lo .. seg_lo + seg_n - 1:
+      // the CTAs holding the cost positions of its first and last pages.
+      int seg_lo = c, seg_n = 1;
+      if (!single) {
+        const int v_first = vseq_off[b] + gkv * (pages + kPieceCost) + kPieceCost;
+        seg_lo = cost_split.cta_of(v_first);
+        seg_n = cost_split.cta_of(v_first + pages - 1) - seg_lo + 1;
+      }
       q_fragments<FMT, DH>(qraw, qb);
       if (u + n < u1) {  // next piece's Q, in flight while this piece runs
         int nb, ng, npg, np0;
@@ -1053,7 +1057,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         }
       }
       consumer_bar();
-      const bool single = (p0 == 0 && n == pages);
       const int64_t slot_idx = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(b) * p.Hkv + gkv;
       // Each thread combines four consecutive dims of one head: the four
       // warps' weights 2^(m_w - M) once, then float4 rows of O.
@@ -1097,13 +1100,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         // Publish this piece; the CTA whose piece completes the segment merges
         // all of its pieces and resets the segment's counter.
         const int64_t sigma = static_cast<int64_t>(b) * p.Hkv + gkv;
-        const int64_t us = seq_off[b] + static_cast<int64_t>(gkv) * pages, ue = us + pages;
-        const int64_t c_lo = cta_of(ub, Pe, us);      // CTA holding unit us
-        const int64_t c_hi = cta_of(ub, Pe, ue - 1);  // CTA holding unit ue - 1
-        const int npieces = static_cast<int>(c_hi - c_lo + 1);
         // The barrier above orders every thread's partial stores before
         // thread 0's fence and arrival (release); the arrival that completes
         // the count is followed by a fence (acquire) and the barrier below.
+        const int64_t c_lo = seg_lo;  // CTA holding the segment's first unit
+        const int npieces = seg_n;
         if (ctid == 0) {
           __threadfence();
           const uint32_t prev = atomicAdd(p.ws_cnt + sigma, 1u);
