@@ -360,7 +360,9 @@ def run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barri
             rank_max):
     """Host buffers in, host result out: per step, copy every layer's K/V/Q from
     pinned host memory (copy stream, one event per layer), run the same calls,
-    read the outputs back."""
+    read the outputs back.  A layer's next copy waits only for the kernels of
+    the previous step that read its buffers, so the copy stream never idles
+    behind a whole step."""
     hk = [torch.from_numpy(np.ascontiguousarray(l.k).view(np.int16)).pin_memory() for l in layers]
     hv = [torch.from_numpy(np.ascontiguousarray(l.v).view(np.int16)).pin_memory() for l in layers]
     hq = [torch.from_numpy(np.ascontiguousarray(l.q).view(np.int16)).pin_memory() for l in layers]
@@ -373,25 +375,34 @@ def run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barri
     copy = torch.cuda.Stream(device=dev)
     E4, PH = kvq.KVQ_FMT_E4M3, kvq.KVQ_SCALE_PER_HEAD
     ready = [torch.cuda.Event() for _ in range(LAYERS)]
+    written = [torch.cuda.Event() for _ in range(LAYERS)]   # layer's K/V consumed
+    decoded = [torch.cuda.Event() for _ in range(LAYERS)]   # layer's Q consumed
+    for i in range(LAYERS):
+        written[i].record(comp)
+        decoded[i].record(comp)
     h2d = sum(x.numel() * 2 for x in hk + hv + hq) + hslot.numel() * 8
     d2h = hout.numel() * 2
 
     def step():
         with torch.cuda.stream(copy):
-            copy.wait_stream(comp)
+            copy.wait_event(written[LAYERS - 1])  # every write of the last step read the slots
             slot_d.copy_(hslot, non_blocking=True)
             for i, x in enumerate(L):
+                copy.wait_event(written[i])
                 x["k"].view(torch.int16).copy_(hk[i], non_blocking=True)
                 x["v"].view(torch.int16).copy_(hv[i], non_blocking=True)
+                copy.wait_event(decoded[i])
                 x["q"].view(torch.int16).copy_(hq[i], non_blocking=True)
                 ready[i].record(copy)
         for i, x in enumerate(L):
             comp.wait_event(ready[i])
             kvq.kvq_write(x["k"], x["v"], slot_d, x["kc"], x["vc"], x["ks"], x["vs"], PH, E4,
                           dev_status=status)
+            written[i].record(comp)
         for i, x in enumerate(L):
             kvq.kvq_decode_attn(x["q"], x["kc"], x["vc"], bt, sl, None, x["ks"], x["vs"], PH, E4,
                                 0, ws, x["out"], dev_status=status)
+            decoded[i].record(comp)
         for i, x in enumerate(L):
             hout[i].copy_(x["out"][0].view(torch.int16), non_blocking=True)
 

@@ -1127,7 +1127,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
               mbar_arrive_expect_tx(mbar, npieces * pbytes);
             }
             __syncwarp();
-            fence_proxy_async();
+            fence_proxy_async_global();  // the partials were acquired through the counter
+            fence_proxy_async_smem();    // the ring was last read by generic loads
             const float* src = p.ws_o + (c_lo + sigma) * p.G * DH;
             for (int c = lane; c < npieces; c += 32)
               bulk_load(ring + static_cast<size_t>(c) * pbytes, src + static_cast<size_t>(c) * p.G * DH,
