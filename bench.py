@@ -256,6 +256,18 @@ def run_gpu(args, rank, world, local_rank):
     # (the caches, tables and lengths are complete before the decode graph).
     with torch.cuda.graph(g_decode_ready):
         decodes(kvq.KVQ_CACHE_READY)
+    # Per-head scale calibration of every layer's K/V (into scratch scales).
+    cal_k = torch.empty(HKV, dtype=torch.float32, device=dev)
+    cal_v = torch.empty(HKV, dtype=torch.float32, device=dev)
+
+    def calibrations():
+        for x in L:
+            kvq.kvq_calibrate_scales(x["k"], x["v"], cal_k, cal_v, PH, E4, dev_status=status)
+
+    calibrations()
+    g_calib = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_calib):
+        calibrations()
     stream = torch.cuda.current_stream()
 
     def step(_timed=False):
@@ -291,12 +303,14 @@ def run_gpu(args, rank, world, local_rank):
         write_total = timed_replays(g_write.replay, args.steps)
         decode_total = timed_replays(g_decode.replay, args.steps)
         ready_total = timed_replays(g_decode_ready.replay, args.steps)
+        calib_total = timed_replays(g_calib.replay, args.steps)
     barrier()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     ms_step = rank_max(total_ms) / args.steps
     write_ms = rank_max(write_total) / args.steps
     decode_ms = rank_max(decode_total) / args.steps
     ready_ms = rank_max(ready_total) / args.steps
+    calib_ms = rank_max(calib_total) / args.steps
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barrier,
@@ -309,6 +323,8 @@ def run_gpu(args, rank, world, local_rank):
     d_ach = decode_bytes(SEQ) / (decode_launch_us * 1e-6) / 1e9
     ready_launch_us = ready_ms * 1e3 / LAYERS
     r_ach = decode_bytes(SEQ) / (ready_launch_us * 1e-6) / 1e9
+    calib_launch_us = calib_ms * 1e3 / LAYERS
+    c_ach = SEQ * 2 * HKV * DH * 2 / (calib_launch_us * 1e-6) / 1e9  # bf16 K and V read once
 
     def roof(name, ach, per_launch_bytes):
         return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
@@ -337,6 +353,9 @@ def run_gpu(args, rank, world, local_rank):
         "decode_attn_cache_ready": {"gbs": round(r_ach, 1), "frac_of_peak": round(r_ach / peak, 4),
                                     "us_per_layer": round(ready_launch_us, 2),
                                     "flags": "KVQ_CACHE_READY"},
+        "kv_calibrate": {"gbs": round(c_ach, 1), "frac_of_peak": round(c_ach / peak, 4),
+                         "us_per_layer": round(calib_launch_us, 2),
+                         "what": "per-head amax scales of one layer's 32768 bf16 K/V tokens"},
         "kv_write": {"gbs": round(w_ach, 1), "frac_of_peak": round(w_ach / peak, 4),
                      "us_per_layer": round(write_launch_us, 2),
                      "tok_s": round(SEQ / (write_launch_us * 1e-6), 0)},
@@ -348,7 +367,8 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "timing": "CUDA graphs (32 writes, 32 decodes) replayed; events on the replay stream; "
                   "per-kernel figures from replaying each graph alone; decode_attn_cache_ready "
-                  "replays the 32 decodes with KVQ_CACHE_READY (not part of the step)",
+                  "replays the 32 decodes with KVQ_CACHE_READY and kv_calibrate 32 scale "
+                  "calibrations (neither part of the step)",
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

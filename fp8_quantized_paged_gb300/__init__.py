@@ -40,6 +40,8 @@ SIGNATURES = {
                                       _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                       _u32, _vp, _vp, _vp]),
     "kvq_dequant_cache": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
+    "kvq_calibrate_scales": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                    _vp]),
     "kvq_parse_dtype": (_i32, [ctypes.c_char_p]),
     "kvq_layer_fmt": (_i32, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_char_p), _i32]),
     "kvq_status_string": (ctypes.c_char_p, [_i32]),
@@ -113,6 +115,23 @@ def kvq_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, scale_gran
                         _ptr(v_cache), nb, bs, _ptr(k_scale), _len(k_scale), _ptr(v_scale),
                         _len(v_scale), scale_granularity, fmt, _ptr(dev_status), _stream(stream))
     _check(st, "kvq_write")
+
+
+def kvq_calibrate_scales(k, v, k_scale, v_scale, scale_granularity, fmt, dev_status=None,
+                         stream=None, token_stride=None) -> None:
+    """Scales from the data: k, v bf16 [N][Hkv][dh] -> k_scale, v_scale fp32
+    ([1] or [Hkv]) = amax / fmt_max."""
+    n, hkv, dh = k.shape
+    stride = k.stride(0) if token_stride is None else token_stride
+    if v.stride(0) != stride or k.stride(1) != dh or k.stride(2) != 1 or v.stride(1) != dh or \
+            tuple(v.shape) != (n, hkv, dh):
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_calibrate_scales")
+    want = hkv if scale_granularity == KVQ_SCALE_PER_HEAD else 1
+    if k_scale.numel() != want or v_scale.numel() != want:
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_calibrate_scales")
+    st = _lib.kvq_calibrate_scales(_ptr(k), _ptr(v), stride, n, hkv, dh, scale_granularity, fmt,
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(dev_status), _stream(stream))
+    _check(st, "kvq_calibrate_scales")
 
 
 def kvq_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, num_sms=0) -> int:

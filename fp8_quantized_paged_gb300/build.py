@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
-SOURCES = ["kvq_host.cu", "kvq_write.cu", "kvq_decode.cu", "kvq_static.cu"]
+SOURCES = ["kvq_host.cu", "kvq_write.cu", "kvq_decode.cu", "kvq_static.cu", "kvq_calib.cu"]
 HEADERS = ["kvq_common.cuh", "kvq_host.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

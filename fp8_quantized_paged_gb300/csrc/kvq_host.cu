@@ -17,6 +17,28 @@
 
 namespace kvq {
 
+void token_row_shape(int64_t num_tokens, int row_units, int blocks_per_sm, int& grid, int& block) {
+  int g_mult = 1;
+  if (row_units <= 256) {
+    block = (256 / row_units) * row_units;
+  } else {
+    block = 256;
+    int a = row_units, b = 256;
+    while (b) {
+      const int t = a % b;
+      a = b;
+      b = t;
+    }
+    g_mult = row_units / a;  // row_units / gcd(row_units, 256)
+  }
+  const int64_t threads = num_tokens * row_units;  // one per chunk
+  int64_t need = (threads + block - 1) / block;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * blocks_per_sm;
+  if (need > cap) need = cap;
+  need = (need + g_mult - 1) / g_mult * g_mult;
+  grid = static_cast<int>(need > 0 ? need : g_mult);
+}
+
 int device_sm_count() {
   static std::atomic<int> cache[64];
   int dev = 0;

@@ -225,32 +225,6 @@ static int grid_for(int64_t units, int threads) {
   return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
-// Launch shape of the write kernel: a block is the largest multiple of the
-// row_units chunks of one token that fits 256 threads (or 256 threads, with
-// the grid a multiple of the blocks that make up whole tokens); the grid
-// fills the SMs once (3 blocks of 256 per SM) or covers the tokens, if fewer.
-static void write_shape(int64_t num_tokens, int row_units, int& grid, int& block) {
-  int g_mult = 1;
-  if (row_units <= 256) {
-    block = (256 / row_units) * row_units;
-  } else {
-    block = 256;
-    int a = row_units, b = 256;
-    while (b) {
-      const int t = a % b;
-      a = b;
-      b = t;
-    }
-    g_mult = row_units / a;  // row_units / gcd(row_units, 256)
-  }
-  const int64_t threads = num_tokens * row_units;  // one per chunk
-  int64_t need = (threads + block - 1) / block;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 3;  // the blocks resident at once (3 of 256 threads per SM)
-  if (need > cap) need = cap;
-  need = (need + g_mult - 1) / g_mult * g_mult;
-  grid = static_cast<int>(need > 0 ? need : g_mult);
-}
-
 }  // namespace kvq
 
 using namespace kvq;
@@ -301,7 +275,7 @@ extern "C" int kvq_write(const void* k, const void* v, int64_t token_stride,
   p.in_elems = (num_tokens - 1) * token_stride + static_cast<int64_t>(num_kv_heads) * head_dim;
   p.cache_elems = num_blocks * num_kv_heads * block_size * head_dim;
   int grid = 0, block = 0;
-  write_shape(num_tokens, num_kv_heads * (head_dim / 16), grid, block);
+  token_row_shape(num_tokens, num_kv_heads * (head_dim / 16), 3, grid, block);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   const dim3 gd(grid), bd(block);

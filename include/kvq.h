@@ -135,6 +135,32 @@ KVQ_API int kvq_write(const void* k, const void* v, int64_t token_stride, const 
               uint32_t* dev_status, kvq_stream_t stream);
 
 /*
+ * kvq_calibrate_scales -- per-tensor or per-KV-head scales from the data
+ * ("vLLM FP8 quantized KV cache guide", scale calibration, way two: scales
+ * estimated from statistics of the K/V activations).  The statistic is the
+ * absolute maximum over the finite values of the given tokens (NaN and +-inf
+ * are ignored), of one KV head or of the whole tensor:
+ *   s = amax / fmt_max   (binary32 division, round to nearest even;
+ *                         fmt_max = 448 for E4M3, 57344 for E5M2),
+ * and s = 1 where that quotient is 0.  Quantizing the same tokens with s
+ * (kvq_write) maps amax onto the format's largest finite value.
+ *
+ *   k, v            bf16 [num_tokens][num_kv_heads][head_dim], consecutive
+ *                   tokens token_stride elements apart (as for kvq_write).
+ *   k_scale,v_scale fp32 device arrays, outputs: 1 float for
+ *                   KVQ_SCALE_PER_TENSOR, num_kv_heads for KVQ_SCALE_PER_HEAD
+ *                   (4-byte aligned).  Overwritten on the stream (a memset,
+ *                   then two kernels).
+ *   fmt             KVQ_FMT_E4M3 or KVQ_FMT_E5M2 (else KVQ_ERR_UNSUPPORTED).
+ *   dev_status      optional; an internal guard bit if a load index fails.
+ * num_tokens == 0 gives scales of 1.
+ */
+KVQ_API int kvq_calibrate_scales(const void* k, const void* v, int64_t token_stride,
+                                 int64_t num_tokens, int num_kv_heads, int head_dim,
+                                 int scale_granularity, int fmt, float* k_scale, float* v_scale,
+                                 uint32_t* dev_status, kvq_stream_t stream);
+
+/*
  * kvq_decode_workspace_size -- bytes of device workspace kvq_decode_attn
  * needs for these sizes.  num_sms <= 0 queries the current device (the value
  * depends on the device's SM count).  Returns 0 for invalid sizes.

@@ -13,7 +13,8 @@ Sources (page titles and sections):
     cache), 10.4.5 (FP8 path: cast_fp8(K/sK) then cast_float(K_fp8) * sK).
   * "vLLM FP8 quantized KV cache guide": scale shapes [1] (per tensor) and
     [num_kv_heads] (per attention head), ``fp8`` as an alias of ``fp8_e4m3``,
-    uint8 storage with FP8 bit semantics.
+    uint8 storage with FP8 bit semantics; scale calibration, way two (scales
+    from statistics of the K/V activations; here their absolute maximum).
 
 Every function here is pinned by tests in ``tests/test_oracle_*.py``.
 """
@@ -206,6 +207,31 @@ def dequant(cache_codes, scale, granularity, fmt) -> np.ndarray:
     out = np.empty(c.shape, dtype=np.uint16)
     lib().kvqo_dequant(_p(c), _p(out), nb, hkv, bs, dh, _p(s), granularity, fmt)
     return out
+
+
+# --------------------------------------------------------------------------
+# Scale calibration ("vLLM FP8 quantized KV cache guide", scale calibration,
+# way two; scale = amax / format max)
+# --------------------------------------------------------------------------
+
+FMT_MAX = {E4M3: 448.0, E5M2: 57344.0}
+
+
+def calibrate(x_bf16_bits, granularity, fmt) -> np.ndarray:
+    """Scales of one tensor x, bf16 bits [N][Hkv][dh]: amax = the largest
+    |x| over its finite values, of each KV head (per head) or of all of them
+    (per tensor); s = float32(amax) / float32(fmt_max), one binary32 division
+    rounded to nearest even; s = 1 where that is 0."""
+    b = np.asarray(x_bf16_bits, dtype=np.uint16)
+    hkv = b.shape[1]
+    a = np.abs((b.astype(np.uint32) << 16).view(np.float32))
+    a = np.where(np.isfinite(a), a, np.float32(0))
+    if granularity == PER_HEAD:
+        amax = a.transpose(1, 0, 2).reshape(hkv, -1).max(axis=1) if b.shape[0] else np.zeros(hkv, np.float32)
+    else:
+        amax = np.array([a.max() if a.size else 0.0], np.float32)
+    s = (amax.astype(np.float32) / np.float32(FMT_MAX[fmt])).astype(np.float32)
+    return np.where(s > 0, s, np.float32(1)).astype(np.float32)
 
 
 def max_threads() -> int:

@@ -28,7 +28,7 @@ def test_exports_every_declared_symbol(kvq):
     declared = header_functions()
     assert declared == {"kvq_write", "kvq_decode_workspace_size", "kvq_decode_attn",
                         "kvq_decode_attn_static", "kvq_dequant_cache", "kvq_parse_dtype",
-                        "kvq_layer_fmt", "kvq_status_string", "kvq_version"}
+                        "kvq_layer_fmt", "kvq_status_string", "kvq_version", "kvq_calibrate_scales"}
     raw = ctypes.CDLL(kvq.LIB_PATH)
     for name in declared:
         assert getattr(raw, name) is not None

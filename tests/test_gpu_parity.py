@@ -420,3 +420,68 @@ def test_decode_cache_ready_chained_layers(kvq):
         for d, ref in zip(devs, refs):
             assert d.status_word() == 0
             check_attention(bf16_out_to_f64(d.out), ref, "chained")
+
+
+# ---------------------------------------------------------------- scale calibration
+
+def _calib(kvq, k, v, gran, fmt, hkv, stride=None, status=None):
+    n = hkv if gran == workloads.PER_HEAD else 1
+    ks = torch.full((n,), float("nan"), device="cuda")
+    vs = torch.full((n,), float("nan"), device="cuda")
+    kvq.kvq_calibrate_scales(k, v, ks, vs, gran, fmt, dev_status=status, token_stride=stride)
+    return to_np(ks), to_np(vs)
+
+
+@pytest.mark.parametrize("cfg,layer,fmt", [(2, 0, workloads.E4M3), (3, 1, workloads.E4M3),
+                                           (3, 1, workloads.E5M2), (1, 0, workloads.E4M3)])
+@pytest.mark.parametrize("gran", [workloads.PER_TENSOR, workloads.PER_HEAD])
+def test_calibrate_matches_oracle(kvq, cfg, layer, fmt, gran):
+    lay = workloads.make_layer(cfg, layer)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ks, vs = _calib(kvq, to_dev(lay.k), to_dev(lay.v), gran, fmt, lay.Hkv, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    np.testing.assert_array_equal(ks, oracle.calibrate(lay.k, gran, fmt))
+    np.testing.assert_array_equal(vs, oracle.calibrate(lay.v, gran, fmt))
+
+
+def test_calibrate_specials_stride_and_empty(kvq):
+    r = np.random.default_rng(21)
+    n, hkv, dh = 300, 4, 64
+    x = (r.standard_normal((n, hkv, dh)) * 3).astype(np.float32)
+    x[5, 1, 3] = np.nan
+    x[7, 2, 9] = np.inf
+    x[8, 2, 10] = -np.inf
+    x[:, 3, :] = 0.0          # an all-zero head -> scale 1
+    x[11, 0, 0] = -250.0      # a negative maximum
+    b = workloads.f32_to_bf16_bits(x)
+    wide = np.zeros((n, hkv * dh + 64), np.uint16)  # token stride beyond Hkv * dh
+    wide[:, : hkv * dh] = b.reshape(n, -1)
+    kd = to_dev(wide)
+    k = kd[:, : hkv * dh].view(n, hkv, dh)
+    ks, vs = _calib(kvq, k, k, workloads.PER_HEAD, workloads.E4M3, hkv, stride=hkv * dh + 64)
+    want = oracle.calibrate(b, workloads.PER_HEAD, workloads.E4M3)
+    np.testing.assert_array_equal(ks, want)
+    np.testing.assert_array_equal(vs, want)
+    assert want[3] == 1.0 and want[0] == np.float32(250) / np.float32(448)
+    e = torch.empty((0, hkv, dh), dtype=torch.bfloat16, device="cuda")
+    ks, vs = _calib(kvq, e, e, workloads.PER_TENSOR, workloads.E5M2, hkv)
+    assert ks[0] == 1.0 and vs[0] == 1.0
+
+
+def test_calibrate_then_write_uses_the_full_range(kvq):
+    """Scales from the calibration put every head's largest value on the
+    format's largest finite code and nothing beyond it."""
+    lay = workloads.make_layer(3, 0)
+    d = DeviceLayer(lay)
+    assert lay.gran == workloads.PER_HEAD
+    ks, vs = _calib(kvq, d.k, d.v, workloads.PER_HEAD, lay.fmt, lay.Hkv)
+    d.ks.copy_(torch.from_numpy(ks))
+    d.vs.copy_(torch.from_numpy(vs))
+    d.write()
+    assert d.status_word() == 0
+    top = 0x7E if lay.fmt == workloads.E4M3 else 0x7B
+    for cache in (d.kc, d.vc):
+        codes = to_np(cache)
+        per_head_max = (codes & 0x7F).transpose(1, 0, 2, 3).reshape(lay.Hkv, -1).max(axis=1)
+        np.testing.assert_array_equal(per_head_max, np.full(lay.Hkv, top))
