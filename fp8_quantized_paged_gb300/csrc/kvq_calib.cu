@@ -51,7 +51,7 @@ KVQ_DEVI uint32_t max_mag16(uint32_t acc, const uint4& a, const uint4& b) {
 }
 
 template <int DH>
-__global__ void __launch_bounds__(256) calib_kernel(const CalibParams p) {
+__global__ void __launch_bounds__(256, 4) calib_kernel(const CalibParams p) {
   constexpr int CH = DH / 16;  // chunks of a head row; divides 32
   pdl_allow_next();
   pdl_wait();  // k, v may come from the previous kernel
@@ -62,13 +62,28 @@ __global__ void __launch_bounds__(256) calib_kernel(const CalibParams p) {
   const int h = rem / CH;
   const int64_t tstride = nthreads / row_units;
   uint32_t mk = 0, mv = 0;  // two 16-bit magnitudes each
-  for (int64_t t = gtid / row_units; t < p.num_tokens; t += tstride) {
-    const int64_t src = t * p.token_stride + rem * 16;
-    if (!guard(src >= 0 && src + 16 <= p.in_elems, p.status, 9)) continue;
-    const uint4* ks = reinterpret_cast<const uint4*>(p.k + src);
-    const uint4* vs = reinterpret_cast<const uint4*>(p.v + src);
-    mk = max_mag16(mk, __ldcs(ks), __ldcs(ks + 1));
-    mv = max_mag16(mv, __ldcs(vs), __ldcs(vs + 1));
+  // two tokens per step, their eight 16-byte loads issued together
+  for (int64_t t = gtid / row_units; t < p.num_tokens; t += 2 * tstride) {
+    uint4 a[2][4];
+    bool ok[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int64_t tt = t + i * tstride;
+      const int64_t src = tt * p.token_stride + rem * 16;
+      ok[i] = tt < p.num_tokens && guard(src >= 0 && src + 16 <= p.in_elems, p.status, 9);
+      const uint4* ks = reinterpret_cast<const uint4*>(p.k + (ok[i] ? src : 0));
+      const uint4* vs = reinterpret_cast<const uint4*>(p.v + (ok[i] ? src : 0));
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      a[i][0] = ok[i] ? __ldcs(ks) : z;
+      a[i][1] = ok[i] ? __ldcs(ks + 1) : z;
+      a[i][2] = ok[i] ? __ldcs(vs) : z;
+      a[i][3] = ok[i] ? __ldcs(vs + 1) : z;
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mk = max_mag16(mk, a[i][0], a[i][1]);
+      mv = max_mag16(mv, a[i][2], a[i][3]);
+    }
   }
   // every thread takes part (those without tokens contribute 0): the CH
   // lanes of a head are consecutive, as the block is a multiple of Hkv * CH
@@ -137,7 +152,7 @@ extern "C" int kvq_calibrate_scales(const void* k, const void* v, int64_t token_
     p.in_elems = (num_tokens - 1) * token_stride + static_cast<int64_t>(num_kv_heads) * head_dim;
     p.status = dev_status;
     int grid = 0, block = 0;
-    token_row_shape(num_tokens, num_kv_heads * (head_dim / 16), 3, grid, block);
+    token_row_shape(num_tokens, num_kv_heads * (head_dim / 16), 4, grid, block);
     e = head_dim == 128 ? launch_pdl(calib_kernel<128>, dim3(grid), dim3(block), 0, s, p)
                         : launch_pdl(calib_kernel<64>, dim3(grid), dim3(block), 0, s, p);
     if (e != cudaSuccess) return KVQ_ERR_CUDA;

@@ -76,7 +76,7 @@ def lib():
                                      i32, i32, i32]
             L.kvqo_write.restype = i64
             L.kvqo_decode_attn.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, i32,
-                                           vp, vp, i32, i32, i32, vp, i64, vp, i32]
+                                           vp, vp, i32, i32, vp, i32, i32, vp, i64, vp, i32]
             L.kvqo_decode_attn.restype = i64
             L.kvqo_dequant.argtypes = [vp, vp, i64, i32, i32, i32, vp, i32, i32]
             L.kvqo_max_threads.restype = i32
@@ -169,11 +169,13 @@ def write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, granularity, f
 
 
 def decode_attn(q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale, granularity,
-                fmt, window=0, pairs=None, nthreads=0) -> np.ndarray:
+                fmt, window=0, pairs=None, nthreads=0, q_scale=None) -> np.ndarray:
     """Float64 decode attention over the dequantized paged cache.
 
     q: bf16 bits [B][Hq][dh]. Returns float64 [B][Hq][dh], or [len(pairs)][dh]
-    when ``pairs`` (int array [n][2] of (b, h)) is given.
+    when ``pairs`` (int array [n][2] of (b, h)) is given.  With ``q_scale``
+    ([1] or [Hq] fp32) the query is first quantized to E4M3 and restored,
+    dec(enc(fp32(q) / sQ)) * sQ (the FP8-domain mode).
     """
     q = np.ascontiguousarray(q, dtype=np.uint16)
     B, hq, dh = q.shape
@@ -190,9 +192,13 @@ def decode_attn(q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale, g
         pr = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
         npairs = pr.shape[0]
         out = np.empty((npairs, dh), dtype=np.float64)
+    qs = None if q_scale is None else np.ascontiguousarray(q_scale, dtype=np.float32).reshape(-1)
+    if qs is not None and qs.size not in (1, hq):
+        raise ValueError("q_scale must have 1 or num_q_heads entries")
     bad = lib().kvqo_decode_attn(_p(q), _p(np.ascontiguousarray(k_cache)),
                                  _p(np.ascontiguousarray(v_cache)), _p(bt), bt.shape[1], _p(sl),
                                  B, hq, hkv, dh, nb, bs, _p(ks), _p(vs), granularity, fmt,
+                                 _p(qs), 0 if qs is None else int(qs.size == hq and hq > 1),
                                  window, _p(pr), npairs, _p(out), nthreads)
     if bad:
         raise ValueError(f"oracle decode: {bad} (sequence, head) pairs had out-of-range inputs")

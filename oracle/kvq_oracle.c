@@ -249,11 +249,25 @@ static double cache_value(const void* cache, int64_t idx, int fmt, double s) {
  * O = sum_t p_t * V^_t.  Query head h reads KV head h / (Hq / Hkv).
  * q_scale is not applied: the stored-FP8 path leaves Q in its own dtype.
  * Returns 0, or -1 when the block table or length is out of range. */
+/* Query element d of head h as the attention uses it: the bf16 value, or --
+ * with a q scale (the FP8-domain mode) -- the query quantized to E4M3 with
+ * the head's scale and restored, dec(enc(fp32(q) / sQ)) * sQ, the division a
+ * binary32 one as for the cache write ("vLLM FP8 quantized KV cache guide",
+ * FlashAttention 3 note: the query is quantized to FP8 like K and V). */
+static double query_value(uint16_t qb, const float* q_scale, int q_per_head, int h) {
+  const float x = kvqo_bf16_to_f32(qb);
+  if (!q_scale) return (double)x;
+  const float sq = q_scale[q_per_head ? h : 0];
+  const float quotient = x / sq;
+  return kvqo_decode(KVQO_E4M3, kvqo_encode(KVQO_E4M3, quotient)) * (double)sq;
+}
+
 static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
                        const int32_t* block_tables, int max_blocks_per_seq,
                        const int32_t* seq_lens, int num_q_heads, int num_kv_heads,
                        int head_dim, int64_t num_blocks, int block_size,
                        const float* k_scale, const float* v_scale, int granularity, int fmt,
+                       const float* q_scale, int q_per_head,
                        int window, int b, int h, double* out, double* scores) {
   const int group = num_q_heads / num_kv_heads;
   const int g = h / group;
@@ -274,7 +288,7 @@ static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
     const int64_t base = (((int64_t)blk * num_kv_heads + g) * block_size + t % block_size) * head_dim;
     double dot = 0.0;
     for (int d = 0; d < head_dim; ++d)
-      dot += (double)kvqo_bf16_to_f32(qrow[d]) * cache_value(kc, base + d, fmt, sk);
+      dot += query_value(qrow[d], q_scale, q_per_head, h) * cache_value(kc, base + d, fmt, sk);
     const double x = dot * inv_sqrt_dh;
     scores[t - lo] = x;
     if (x > xmax) xmax = x;
@@ -303,6 +317,7 @@ int64_t kvqo_decode_attn(const uint16_t* q, const void* k_cache, const void* v_c
                          const int32_t* seq_lens, int num_seqs, int num_q_heads,
                          int num_kv_heads, int head_dim, int64_t num_blocks, int block_size,
                          const float* k_scale, const float* v_scale, int granularity, int fmt,
+                         const float* q_scale, int q_per_head,
                          int window, const int32_t* pairs, int64_t npairs, double* out,
                          int nthreads) {
   const int64_t n = pairs ? npairs : (int64_t)num_seqs * num_q_heads;
@@ -330,7 +345,8 @@ int64_t kvqo_decode_attn(const uint16_t* q, const void* k_cache, const void* v_c
       }
       if (decode_pair(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                       num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, k_scale,
-                      v_scale, granularity, fmt, window, b, h, out + i * head_dim, scores))
+                      v_scale, granularity, fmt, q_scale, q_per_head, window, b, h,
+                      out + i * head_dim, scores))
         bad += 1;
     }
     free(scores);

@@ -180,3 +180,66 @@ def test_bad_block_id_is_reported():
     bt[0, 1] = st.num_blocks + 5
     with pytest.raises(ValueError):
         oracle.decode_attn(q, K, V, bt, st.seq_lens, ks, vs, PER_TENSOR, E4M3)
+
+
+# ---------------------------------------------------------------- FP8-domain query mode
+
+def _q_hat(q_bits, q_scale, per_head):
+    """dec(enc(fp32(q) / sQ)) * sQ with the (separately pinned) codec, numpy
+    binary32 division."""
+    qf = (np.asarray(q_bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+    hq = qf.shape[1]
+    s = np.asarray(q_scale, np.float32)
+    s = (s if per_head else np.repeat(s, hq)).reshape(1, hq, 1)
+    codes = oracle.encode(E4M3, (qf / s).astype(np.float32))
+    return oracle.decode(E4M3, codes) * s.astype(np.float64)
+
+
+@pytest.mark.parametrize("fmt,per_head", [(E4M3, False), (E4M3, True), (E5M2, True)])
+def test_q_fp8_matches_sdpa_on_the_quantized_query(fmt, per_head):
+    r = np.random.default_rng(300 + fmt + per_head)
+    B, Hq, Hkv, dh = 2, 8, 2, 64
+    st, q, K, V, ks, vs = _case(r, B, Hq, Hkv, dh, [45, 17], fmt, PER_HEAD)
+    qs = (r.uniform(0.5, 2.0, Hq if per_head else 1) / 200).astype(np.float32)
+    out = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_HEAD, fmt,
+                             q_scale=qs)
+    qh = _q_hat(q, qs, per_head)
+    G = Hq // Hkv
+    for b in range(B):
+        Kh = torch.from_numpy(_gather(K, st, b, fmt, ks, PER_HEAD)).repeat_interleave(G, 0)
+        Vh = torch.from_numpy(_gather(V, st, b, fmt, vs, PER_HEAD)).repeat_interleave(G, 0)
+        qb = torch.from_numpy(qh[b])[:, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(qb, Kh, Vh)[:, 0, :].numpy()
+        np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-12)
+    # the quantized query differs from the bf16 one, so the outputs do too
+    plain = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_HEAD, fmt)
+    assert not np.array_equal(plain, out)
+
+
+def test_q_fp8_is_exact_for_representable_queries():
+    """Queries that are E4M3 values times a power-of-two scale come back
+    unchanged, so the FP8-domain mode equals the plain one."""
+    r = np.random.default_rng(9)
+    B, Hq, Hkv, dh = 2, 4, 2, 64
+    st, _, K, V, ks, vs = _case(r, B, Hq, Hkv, dh, [30, 64], E4M3, PER_TENSOR)
+    codes = r.integers(0, 0x7F, size=(B, Hq, dh)).astype(np.uint8)  # finite E4M3 codes (no NaN)
+    codes[codes == 0x7F] = 0x7E
+    sq = np.float32(2.0 ** -7)
+    q = bits_from(oracle.decode(E4M3, codes) * sq)  # exact in bf16 (at most 4 significant bits)
+    a = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_TENSOR, E4M3)
+    b = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_TENSOR, E4M3,
+                           q_scale=np.array([sq], np.float32))
+    np.testing.assert_array_equal(a, b)
+
+
+def test_q_fp8_per_head_scales_are_indexed_by_query_head():
+    r = np.random.default_rng(10)
+    B, Hq, Hkv, dh = 1, 4, 1, 64
+    st, q, K, V, ks, vs = _case(r, B, Hq, Hkv, dh, [20], E4M3, PER_TENSOR)
+    qs = np.array([0.01, 0.02, 0.003, 0.05], np.float32)
+    per_head = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_TENSOR, E4M3,
+                                  q_scale=qs)
+    for h in range(Hq):
+        one = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_TENSOR, E4M3,
+                                 q_scale=qs[h:h + 1])
+        np.testing.assert_array_equal(per_head[0, h], one[0, h])
