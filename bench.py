@@ -219,7 +219,7 @@ def run_gpu(args, rank, world, local_rank):
     sl = up(st.seq_lens)
     L = []
     for lay in layers:
-        L.append(dict(k=up(lay.k), v=up(lay.v), q=up(lay.q), ks=up(lay.k_scale),
+        L.append(dict(k=up(lay.k), v=up(lay.v), q=up(lay.q), qs=up(lay.q_scale), ks=up(lay.k_scale),
                       vs=up(lay.v_scale),
                       kc=kvq.new_cache(st.num_blocks, HKV, DH, kvq.KVQ_FMT_E4M3, dev),
                       vc=kvq.new_cache(st.num_blocks, HKV, DH, kvq.KVQ_FMT_E4M3, dev),
@@ -227,7 +227,7 @@ def run_gpu(args, rank, world, local_rank):
     ws = kvq.new_workspace(1, HQ, HKV, DH, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     E4, PH = kvq.KVQ_FMT_E4M3, kvq.KVQ_SCALE_PER_HEAD
-    launches_per_step = LAYERS * 3  # write kernel; decode + merge kernels
+    launches_per_step = LAYERS * 2  # one write and one decode kernel per layer
 
     def writes():
         for x in L:
@@ -236,8 +236,8 @@ def run_gpu(args, rank, world, local_rank):
 
     def decodes(flags=0):
         for x in L:
-            kvq.kvq_decode_attn(x["q"], x["kc"], x["vc"], bt, sl, None, x["ks"], x["vs"], PH, E4,
-                                0, ws, x["out"], dev_status=status, flags=flags)
+            kvq.kvq_decode_attn(x["q"], x["kc"], x["vc"], bt, sl, x["qs"], x["ks"], x["vs"], PH,
+                                E4, 0, ws, x["out"], dev_status=status, flags=flags)
 
     # eager warm-up (first calls configure the kernels), then one CUDA graph
     # for the 32 writes and one for the 32 decodes: the step replays both.
@@ -256,6 +256,12 @@ def run_gpu(args, rank, world, local_rank):
     # (the caches, tables and lengths are complete before the decode graph).
     with torch.cuda.graph(g_decode_ready):
         decodes(kvq.KVQ_CACHE_READY)
+    # The FP8-domain query mode: Q quantized with its per-head scale, QK^T on
+    # FP8 codes.
+    decodes(kvq.KVQ_Q_FP8)
+    g_decode_qf8 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_decode_qf8):
+        decodes(kvq.KVQ_Q_FP8)
     # Per-head scale calibration of every layer's K/V (into scratch scales).
     cal_k = torch.empty(HKV, dtype=torch.float32, device=dev)
     cal_v = torch.empty(HKV, dtype=torch.float32, device=dev)
@@ -303,6 +309,7 @@ def run_gpu(args, rank, world, local_rank):
         write_total = timed_replays(g_write.replay, args.steps)
         decode_total = timed_replays(g_decode.replay, args.steps)
         ready_total = timed_replays(g_decode_ready.replay, args.steps)
+        qf8_total = timed_replays(g_decode_qf8.replay, args.steps)
         calib_total = timed_replays(g_calib.replay, args.steps)
     barrier()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
@@ -310,6 +317,7 @@ def run_gpu(args, rank, world, local_rank):
     write_ms = rank_max(write_total) / args.steps
     decode_ms = rank_max(decode_total) / args.steps
     ready_ms = rank_max(ready_total) / args.steps
+    qf8_ms = rank_max(qf8_total) / args.steps
     calib_ms = rank_max(calib_total) / args.steps
 
     # ---- end to end through the public API with host buffers
@@ -323,6 +331,8 @@ def run_gpu(args, rank, world, local_rank):
     d_ach = decode_bytes(SEQ) / (decode_launch_us * 1e-6) / 1e9
     ready_launch_us = ready_ms * 1e3 / LAYERS
     r_ach = decode_bytes(SEQ) / (ready_launch_us * 1e-6) / 1e9
+    qf8_launch_us = qf8_ms * 1e3 / LAYERS
+    q_ach = decode_bytes(SEQ) / (qf8_launch_us * 1e-6) / 1e9
     calib_launch_us = calib_ms * 1e3 / LAYERS
     c_ach = SEQ * 2 * HKV * DH * 2 / (calib_launch_us * 1e-6) / 1e9  # bf16 K and V read once
 
@@ -353,6 +363,8 @@ def run_gpu(args, rank, world, local_rank):
         "decode_attn_cache_ready": {"gbs": round(r_ach, 1), "frac_of_peak": round(r_ach / peak, 4),
                                     "us_per_layer": round(ready_launch_us, 2),
                                     "flags": "KVQ_CACHE_READY"},
+        "decode_attn_q_fp8": {"gbs": round(q_ach, 1), "frac_of_peak": round(q_ach / peak, 4),
+                              "us_per_layer": round(qf8_launch_us, 2), "flags": "KVQ_Q_FP8"},
         "kv_calibrate": {"gbs": round(c_ach, 1), "frac_of_peak": round(c_ach / peak, 4),
                          "us_per_layer": round(calib_launch_us, 2),
                          "what": "per-head amax scales of one layer's 32768 bf16 K/V tokens"},
@@ -367,8 +379,8 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "timing": "CUDA graphs (32 writes, 32 decodes) replayed; events on the replay stream; "
                   "per-kernel figures from replaying each graph alone; decode_attn_cache_ready "
-                  "replays the 32 decodes with KVQ_CACHE_READY and kv_calibrate 32 scale "
-                  "calibrations (neither part of the step)",
+                  "replays the 32 decodes with KVQ_CACHE_READY, decode_attn_q_fp8 with "
+                  "KVQ_Q_FP8, and kv_calibrate 32 scale calibrations (none part of the step)",
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

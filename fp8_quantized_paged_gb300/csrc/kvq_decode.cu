@@ -132,6 +132,8 @@ struct DecodeParams {
   int per_head;
   int P;
   int early;  // KVQ_CACHE_READY: tables, lengths, scales and all but the last pages before the wait
+  const float* qs;  // KVQ_Q_FP8: query scales, [1] or [Hq]
+  int q_per_head;
   float logit_scale;  // log2(e) / sqrt(dh)
   uint32_t* ws_cnt;  // [B * Hkv] arrivals of the pieces of each segment (zero between calls)
   float* ws_ml;
@@ -507,22 +509,26 @@ KVQ_DEVI void load_page(uint32_t kp, uint32_t vp, int g, int t, int tok0, int lo
 //   converted to f16 exactly, or bf16 as is), the group's query heads the B
 //   operand; lane (g, t) covers dims t*(DH/4) + 4kk + {0..3} of step kk.
 //   PV: O^T += V^T P^T with m-tile mt, row r -> dim g*(DH/8) + 2mt + r/8.
-template <int FMT, int DH, int NP, bool PK>
+template <int FMT, int DH, int NP, bool PK, bool QF8>
 KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[NP],
                             const bool (&bad)[NP], int g, int t, int G,
                             const uint32_t (&qb)[DH / 16][2], float (&o)[DH / 16][4],
-                            SoftmaxState& st, float lscale, int lo, int L) {
+                            SoftmaxState& st, float lscale0, float lscale1, int lo, int L) {
   using R = PageRegs<FMT, DH>;
   constexpr bool BF = FMT == KVQ_FMT_BF16;
   float s[NP][4];
 #pragma unroll
   for (int i = 0; i < NP; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
 #pragma unroll
-  for (int kk = 0; kk < DH / 16; ++kk) {
+  for (int kk = 0; kk < (QF8 ? DH / 32 : DH / 16); ++kk) {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
       uint32_t a[4];
-      if (BF) {
+      if (QF8) {  // the FP8 codes themselves: dims 8kk .. 8kk + 7 of the lane's run
+        a[0] = r[i].k0[2 * kk]; a[1] = r[i].k1[2 * kk];
+        a[2] = r[i].k0[2 * kk + 1]; a[3] = r[i].k1[2 * kk + 1];
+        mma_fp8<FMT>(s[i], a, qb[kk][0], qb[kk][1]);
+      } else if (BF) {
         a[0] = r[i].k0[2 * kk]; a[1] = r[i].k1[2 * kk];
         a[2] = r[i].k0[2 * kk + 1]; a[3] = r[i].k1[2 * kk + 1];
         mma_bf16(s[i], a, qb[kk][0], qb[kk][1]);
@@ -538,10 +544,10 @@ KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[
   for (int i = 0; i < NP; ++i) {
     const int ta = tok0[i] + g, tb = ta + 8;
     const bool va = token_valid(ta, lo, L, bad[i]), vb = token_valid(tb, lo, L, bad[i]);
-    x[4 * i] = va ? s[i][0] * lscale : -INFINITY;
-    x[4 * i + 1] = va ? s[i][1] * lscale : -INFINITY;
-    x[4 * i + 2] = vb ? s[i][2] * lscale : -INFINITY;
-    x[4 * i + 3] = vb ? s[i][3] * lscale : -INFINITY;
+    x[4 * i] = va ? s[i][0] * lscale0 : -INFINITY;
+    x[4 * i + 1] = va ? s[i][1] * lscale1 : -INFINITY;
+    x[4 * i + 2] = vb ? s[i][2] * lscale0 : -INFINITY;
+    x[4 * i + 3] = vb ? s[i][3] * lscale1 : -INFINITY;
   }
   float pr[4 * NP];
   softmax_pages<NP, DH / 16>(x, pr, st, o);
@@ -615,6 +621,23 @@ KVQ_DEVI void q_fragments(const uint32_t (&w)[DH / 8], uint32_t (&qb)[DH / 16][2
       qb[kk][0] = f32x2_to_f16x2(bf16lo_to_f32(w[2 * kk]), bf16hi_to_f32(w[2 * kk]));
       qb[kk][1] = f32x2_to_f16x2(bf16lo_to_f32(w[2 * kk + 1]), bf16hi_to_f32(w[2 * kk + 1]));
     }
+  }
+}
+
+// Q of the FP8-domain mode: the lane's DH/4 query values divided by the
+// head's scale (binary32, round to nearest even) and encoded to the cache's
+// FP8 format (RNE, satfinite), four codes a word in dim order; MMA step kk
+// takes words 2kk and 2kk + 1 (dims 8kk .. 8kk + 7 of the run, as the K
+// words).
+template <int FMT, int DH>
+KVQ_DEVI void q_fragments_fp8(const uint32_t (&w)[DH / 8], float sq, uint32_t (&qb)[DH / 16][2]) {
+#pragma unroll
+  for (int j = 0; j < DH / 16; ++j) {  // output word j: bf16 words 2j, 2j + 1
+    const uint32_t lo = f32x2_to_fp8x2<FMT>(__fdiv_rn(bf16lo_to_f32(w[2 * j]), sq),
+                                            __fdiv_rn(bf16hi_to_f32(w[2 * j]), sq));
+    const uint32_t hi = f32x2_to_fp8x2<FMT>(__fdiv_rn(bf16lo_to_f32(w[2 * j + 1]), sq),
+                                            __fdiv_rn(bf16hi_to_f32(w[2 * j + 1]), sq));
+    qb[j >> 1][j & 1] = lo | (hi << 16);
   }
 }
 
@@ -722,7 +745,7 @@ KVQ_DEVI void merge_segment(const DecodeParams& p, int b, int gkv, int64_t sigma
 // Decode kernel
 // --------------------------------------------------------------------------
 
-template <int FMT, int DH, bool PK>
+template <int FMT, int DH, bool PK, bool QF8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSM)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
@@ -947,6 +970,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       const int fp = lo / kBS;
       const float sv = sv_s[gkv];
       const float lscale = sk_s[gkv] * p.logit_scale;
+      // FP8-domain query: this lane's query head scale, and the two MMA
+      // columns' (heads 2t, 2t + 1 of the group, or their P_lo copies) logit
+      // scales carry their heads' sQ
+      float lscale0 = lscale, lscale1 = lscale, sq = 1.f;
+      if (QF8) {
+        auto q_scale_of = [&](int hh) {
+          return hh < p.G ? __ldg(p.qs + (p.q_per_head ? gkv * p.G + hh : 0)) : 1.f;
+        };
+        sq = q_scale_of(qhead);
+        lscale0 = lscale * q_scale_of(PK ? ((2 * t) & 3) : 2 * t);
+        lscale1 = lscale * q_scale_of(PK ? ((2 * t + 1) & 3) : 2 * t + 1);
+      }
       const bool single = (p0 == 0 && n == pages);
       // A split segment's pieces are those of CTAs seg_lo .. seg_lo + seg_n - 1:
       // the CTAs holding the cost positions of its first and last pages.
@@ -956,7 +991,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         seg_lo = cost_split.cta_of(v_first);
         seg_n = cost_split.cta_of(v_first + pages - 1) - seg_lo + 1;
       }
-      q_fragments<FMT, DH>(qraw, qb);
+      if (QF8)
+        q_fragments_fp8<FMT, DH>(qraw, sq, qb);
+      else
+        q_fragments<FMT, DH>(qraw, qb);
       if (u + n < u1) {  // next piece's Q, in flight while this piece runs
         int nb, ng, npg, np0;
         piece_at(u + n, nb, ng, npg, np0);
@@ -1019,7 +1057,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
             for (int i = 0; i < NP; ++i)
               if (have[i]) mbar_arrive(&empty[slot[i]]);
           }
-          compute_pages<FMT, DH, NP, PK>(pr, tok0, bad, g, t, p.G, qb, o, st, lscale, lo, L);
+          compute_pages<FMT, DH, NP, PK, QF8>(pr, tok0, bad, g, t, p.G, qb, o, st, lscale0, lscale1,
+                                              lo, L);
         } else {
           __syncwarp();
           if (lane == 0) {
@@ -1208,22 +1247,33 @@ static int launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMa
   if (dev < 0 || dev >= 64 || !configured[dev]) {
     const int maxsmem = static_cast<int>(smem_bytes<FMT, DH>(kMaxGroup, kCtasPerSM * device_sm_count(), kMaxSeqs, kMaxKvHeads));
     // The largest shared-memory carveout, so that two CTAs fit on every SM.
-    if (cudaFuncSetAttribute(decode_kernel<FMT, DH, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, maxsmem) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_kernel<FMT, DH, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, maxsmem) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_kernel<FMT, DH, true>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-        cudaFuncSetAttribute(decode_kernel<FMT, DH, false>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-      return KVQ_ERR_CUDA;
+    auto configure = [&](auto kernel) {
+      return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxsmem) ==
+                 cudaSuccess &&
+             cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+    };
+    bool ok = configure(decode_kernel<FMT, DH, true, false>) &&
+              configure(decode_kernel<FMT, DH, false, false>);
+    if constexpr (FMT != KVQ_FMT_BF16)
+      ok = ok && configure(decode_kernel<FMT, DH, true, true>) &&
+           configure(decode_kernel<FMT, DH, false, true>);
+    if (!ok) return KVQ_ERR_CUDA;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  const cudaError_t e =
-      p.G <= 4 ? launch_pdl(decode_kernel<FMT, DH, true>, dim3(p.P), dim3(kThreads), smem, s, p, tk, tv)
-               : launch_pdl(decode_kernel<FMT, DH, false>, dim3(p.P), dim3(kThreads), smem, s, p, tk, tv);
+  const dim3 grid(p.P), block(kThreads);
+  cudaError_t e;
+  if constexpr (FMT != KVQ_FMT_BF16) {
+    if (p.qs)
+      e = p.G <= 4 ? launch_pdl(decode_kernel<FMT, DH, true, true>, grid, block, smem, s, p, tk, tv)
+                   : launch_pdl(decode_kernel<FMT, DH, false, true>, grid, block, smem, s, p, tk, tv);
+    else
+      e = p.G <= 4 ? launch_pdl(decode_kernel<FMT, DH, true, false>, grid, block, smem, s, p, tk, tv)
+                   : launch_pdl(decode_kernel<FMT, DH, false, false>, grid, block, smem, s, p, tk, tv);
+  } else {
+    e = p.G <= 4 ? launch_pdl(decode_kernel<FMT, DH, true, false>, grid, block, smem, s, p, tk, tv)
+                 : launch_pdl(decode_kernel<FMT, DH, false, false>, grid, block, smem, s, p, tk, tv);
+  }
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
@@ -1256,8 +1306,10 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   if (fmt < KVQ_FMT_BF16 || fmt > KVQ_FMT_E5M2) return KVQ_ERR_ARG;
   if (scale_granularity != KVQ_SCALE_PER_TENSOR && scale_granularity != KVQ_SCALE_PER_HEAD)
     return KVQ_ERR_ARG;
-  if (flags & KVQ_Q_FP8) return KVQ_ERR_UNSUPPORTED;
   if (flags & ~(KVQ_Q_FP8 | KVQ_CACHE_READY)) return KVQ_ERR_ARG;
+  const bool q_fp8 = (flags & KVQ_Q_FP8) != 0;
+  if (q_fp8 && fmt == KVQ_FMT_BF16) return KVQ_ERR_UNSUPPORTED;
+  if (q_fp8 && !q_scale) return KVQ_ERR_NULL;
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || sliding_window < 0)
     return KVQ_ERR_ARG;
@@ -1310,6 +1362,8 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   p.per_head = scale_granularity == KVQ_SCALE_PER_HEAD;
   p.P = P;
   p.early = (flags & KVQ_CACHE_READY) ? 1 : 0;
+  p.qs = q_fp8 ? q_scale : nullptr;
+  p.q_per_head = scale_granularity == KVQ_SCALE_PER_HEAD && num_q_heads > 1;
   p.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.ws_cnt = reinterpret_cast<uint32_t*>(ws + wl.cnt);

@@ -101,7 +101,7 @@ typedef enum {
 #define KVQ_WS_COUNTER_BYTES ((size_t)65536 * 4u)
 
 /* Flags of kvq_decode_attn. */
-#define KVQ_Q_FP8 1u /* reserved: FP8-domain attention with Q quantized; not built */
+#define KVQ_Q_FP8 1u /* FP8-domain attention: Q quantized with q_scale; see kvq_decode_attn */
 #define KVQ_CACHE_READY 2u /* start before the preceding kernel ends; see kvq_decode_attn */
 
 /*
@@ -184,13 +184,22 @@ KVQ_API size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_
  *   block_tables    int32 [num_seqs][max_blocks_per_seq]; entries past
  *                   ceil(L_b / block_size) are never read.
  *   seq_lens        int32 [num_seqs]; 0 gives a zero output row.
- *   q_scale         optional; accepted and shape-checked (q_scale_len 1 or
- *                   num_q_heads) but not applied: the stored-FP8 path keeps
- *                   Q in bf16 (see KVQ_Q_FP8).
+ *   q_scale         fp32, q_scale_len 1 (KVQ_SCALE_PER_TENSOR) or
+ *                   num_q_heads (KVQ_SCALE_PER_HEAD).  Used only with
+ *                   KVQ_Q_FP8; otherwise optional and only shape-checked.
  *   k_scale,v_scale as for kvq_write (ignored and may be NULL for BF16).
  *   sliding_window  0 = none.
- *   flags           0, or KVQ_CACHE_READY (KVQ_Q_FP8 returns
- *                   KVQ_ERR_UNSUPPORTED).  The kernel is launched as a
+ *   flags           KVQ_Q_FP8: the FP8-domain mode ("vLLM FP8 quantized KV
+ *                   cache guide", FlashAttention 3 note: the query is
+ *                   quantized to FP8 like K and V).  Each query value is
+ *                   divided by its head's q_scale (binary32) and encoded in
+ *                   the cache's FP8 format as kvq_write encodes K; QK^T then
+ *                   runs on the FP8 codes (m16n8k32 FP8 MMA), the logits
+ *                   scaled by sQ sK / sqrt(dh).  Needs an FP8 cache
+ *                   (KVQ_ERR_UNSUPPORTED for BF16) and q_scale
+ *                   (KVQ_ERR_NULL).
+ *                   KVQ_CACHE_READY (combinable with KVQ_Q_FP8): the kernel
+ *                   is launched as a
  *                   programmatic dependent of the kernel before it on the
  *                   stream.  Without the flag it waits for that kernel to
  *                   complete before reading anything.  With KVQ_CACHE_READY

@@ -174,8 +174,8 @@ def decode_attn(q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale, g
 
     q: bf16 bits [B][Hq][dh]. Returns float64 [B][Hq][dh], or [len(pairs)][dh]
     when ``pairs`` (int array [n][2] of (b, h)) is given.  With ``q_scale``
-    ([1] or [Hq] fp32) the query is first quantized to E4M3 and restored,
-    dec(enc(fp32(q) / sQ)) * sQ (the FP8-domain mode).
+    ([1] or [Hq] fp32) the query is first quantized to the cache's FP8 format
+    and restored, dec(enc(fp32(q) / sQ)) * sQ (the FP8-domain mode).
     """
     q = np.ascontiguousarray(q, dtype=np.uint16)
     B, hq, dh = q.shape

@@ -250,16 +250,17 @@ static double cache_value(const void* cache, int64_t idx, int fmt, double s) {
  * q_scale is not applied: the stored-FP8 path leaves Q in its own dtype.
  * Returns 0, or -1 when the block table or length is out of range. */
 /* Query element d of head h as the attention uses it: the bf16 value, or --
- * with a q scale (the FP8-domain mode) -- the query quantized to E4M3 with
- * the head's scale and restored, dec(enc(fp32(q) / sQ)) * sQ, the division a
- * binary32 one as for the cache write ("vLLM FP8 quantized KV cache guide",
- * FlashAttention 3 note: the query is quantized to FP8 like K and V). */
-static double query_value(uint16_t qb, const float* q_scale, int q_per_head, int h) {
+ * with a q scale (the FP8-domain mode) -- the query quantized to the cache's
+ * FP8 format with the head's scale and restored, dec(enc(fp32(q) / sQ)) * sQ,
+ * the division a binary32 one as for the cache write ("vLLM FP8 quantized KV
+ * cache guide", FlashAttention 3 note: the query is quantized to FP8 like K
+ * and V). */
+static double query_value(uint16_t qb, int fmt, const float* q_scale, int q_per_head, int h) {
   const float x = kvqo_bf16_to_f32(qb);
   if (!q_scale) return (double)x;
   const float sq = q_scale[q_per_head ? h : 0];
   const float quotient = x / sq;
-  return kvqo_decode(KVQO_E4M3, kvqo_encode(KVQO_E4M3, quotient)) * (double)sq;
+  return kvqo_decode(fmt, kvqo_encode(fmt, quotient)) * (double)sq;
 }
 
 static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
@@ -288,7 +289,7 @@ static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
     const int64_t base = (((int64_t)blk * num_kv_heads + g) * block_size + t % block_size) * head_dim;
     double dot = 0.0;
     for (int d = 0; d < head_dim; ++d)
-      dot += query_value(qrow[d], q_scale, q_per_head, h) * cache_value(kc, base + d, fmt, sk);
+      dot += query_value(qrow[d], fmt, q_scale, q_per_head, h) * cache_value(kc, base + d, fmt, sk);
     const double x = dot * inv_sqrt_dh;
     scores[t - lo] = x;
     if (x > xmax) xmax = x;

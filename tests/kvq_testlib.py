@@ -115,9 +115,11 @@ def oracle_caches(lay: workloads.Layer, token_idx=None, fill=0):
     return K, V
 
 
-def oracle_decode(lay, K, V, pairs=None, window=None, seq_lens=None, block_tables=None):
+def oracle_decode(lay, K, V, pairs=None, window=None, seq_lens=None, block_tables=None,
+                  q_fp8=False):
     st = lay.st
     return oracle.decode_attn(lay.q, K, V, st.block_tables if block_tables is None else block_tables,
                               st.seq_lens if seq_lens is None else seq_lens, lay.k_scale,
                               lay.v_scale, lay.gran, lay.fmt,
-                              lay.window if window is None else window, pairs=pairs)
+                              lay.window if window is None else window, pairs=pairs,
+                              q_scale=lay.q_scale if q_fp8 else None)

@@ -142,7 +142,9 @@ def test_decode_validation(kvq):
     assert _decode(kvq, fmt=-1) == kvq.KVQ_ERR_ARG
     assert _decode(kvq, B=0) == kvq.KVQ_ERR_ARG
     assert _decode(kvq, win=-1) == kvq.KVQ_ERR_ARG
-    assert _decode(kvq, flags=kvq.KVQ_Q_FP8) == kvq.KVQ_ERR_UNSUPPORTED
+    assert _decode(kvq, flags=kvq.KVQ_Q_FP8) == kvq.KVQ_ERR_NULL  # the mode needs q_scale
+    assert _decode(kvq, flags=kvq.KVQ_Q_FP8, fmt=0, qs=A, qsl=1) == kvq.KVQ_ERR_UNSUPPORTED
+    assert _decode(kvq, flags=kvq.KVQ_Q_FP8, qs=A, qsl=32) == kvq.KVQ_ERR_SHAPE
     assert _decode(kvq, flags=4) == kvq.KVQ_ERR_ARG
     assert _decode(kvq, dh=80) == kvq.KVQ_ERR_UNSUPPORTED
     assert _decode(kvq, bs=8) == kvq.KVQ_ERR_UNSUPPORTED

@@ -7,6 +7,8 @@ the same dequantized cache.  Inputs are the seeded workloads of
 scales in E4M3 and E5M2, one long-context layer, a FP8 and a bf16 layer of the
 mixed skip-layer batch) plus hand-made edge cases.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -485,3 +487,78 @@ def test_calibrate_then_write_uses_the_full_range(kvq):
         codes = to_np(cache)
         per_head_max = (codes & 0x7F).transpose(1, 0, 2, 3).reshape(lay.Hkv, -1).max(axis=1)
         np.testing.assert_array_equal(per_head_max, np.full(lay.Hkv, top))
+
+
+# ---------------------------------------------------------------- FP8-domain query mode
+
+def _q_fp8_layer(lay, scale=None):
+    """The layer with q_scale set from the query's own amax (per tensor or per
+    query head, as the layer's granularity), or to ``scale``."""
+    qs = oracle.calibrate(lay.q, lay.gran, lay.fmt) if scale is None else scale
+    return dataclasses.replace(lay, q_scale=np.asarray(qs, np.float32))
+
+
+@pytest.mark.parametrize("cfg,layer,fmt3", [(1, 0, workloads.E4M3), (2, 0, workloads.E4M3),
+                                           (3, 0, workloads.E4M3), (3, 0, workloads.E5M2),
+                                           (5, 2, workloads.E4M3)],
+                         ids=["tiny", "llama8b_layer", "perhead_e4m3", "perhead_e5m2",
+                              "mixed_fp8_layer2"])
+def test_decode_q_fp8(kvq, cfg, layer, fmt3):
+    """Q quantized to the cache format with the workload's q scale, QK^T on
+    FP8 codes: same output as the oracle's dec(enc(q / sQ)) sQ query."""
+    lay = workloads.make_layer(cfg, layer, fmt3)
+    d = DeviceLayer(lay)
+    d.write()
+    out = d.decode(flags=kvq.KVQ_Q_FP8)
+    assert d.status_word() == 0
+    K, V = oracle_caches(lay)
+    pairs = _pairs_for(lay)
+    ref = oracle_decode(lay, K, V, pairs=pairs, q_fp8=True)
+    got = bf16_out_to_f64(out)
+    if pairs is not None:
+        got = got[pairs[:, 0], pairs[:, 1]]
+    check_attention(got, ref, f"q fp8 config {cfg} layer {layer}")
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2])
+@pytest.mark.parametrize("G,dh", [(1, 128), (2, 64), (4, 128), (8, 64), (8, 128)])
+@pytest.mark.parametrize("gran", [workloads.PER_TENSOR, workloads.PER_HEAD])
+def test_decode_q_fp8_shapes(kvq, fmt, G, dh, gran):
+    lay = _q_fp8_layer(_custom_layer([1, 15, 0, 250, 33, 1000], Hq=2 * G, Hkv=2, dh=dh, fmt=fmt,
+                                     gran=gran, seed=110 + G + dh))
+    d = DeviceLayer(lay)
+    d.write()
+    got = bf16_out_to_f64(d.decode(flags=kvq.KVQ_Q_FP8))
+    assert d.status_word() == 0
+    K, V = oracle_caches(lay)
+    check_attention(got, oracle_decode(lay, K, V, q_fp8=True), f"q fp8 G={G} dh={dh}")
+    assert np.all(got[2] == 0)
+
+
+def test_decode_q_fp8_saturating_and_split(kvq):
+    """A q scale small enough that most query codes saturate to the format's
+    largest finite value, on segments split over many CTAs, with the
+    cache-ready flag."""
+    lay = _q_fp8_layer(_custom_layer([20000, 3], Hq=32, Hkv=8, dh=128, seed=120),
+                       scale=np.full(32, 1.0 / 1024, np.float32))
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    ref = oracle_decode(lay, K, V, q_fp8=True)
+    for flags in (kvq.KVQ_Q_FP8, kvq.KVQ_Q_FP8 | kvq.KVQ_CACHE_READY):
+        got = bf16_out_to_f64(d.decode(flags=flags))
+        assert d.status_word() == 0
+        check_attention(got, ref, f"q fp8 saturating flags={flags}")
+        d.poison_workspace()
+
+
+def test_decode_q_fp8_rejected_without_fp8_cache_or_scale(kvq):
+    lay = _custom_layer([40], Hq=4, Hkv=2, dh=64, fmt=workloads.BF16)
+    d = DeviceLayer(lay)
+    with pytest.raises(RuntimeError):
+        d.decode(flags=kvq.KVQ_Q_FP8)
+    lay8 = _custom_layer([40], Hq=4, Hkv=2, dh=64)
+    d8 = DeviceLayer(lay8)
+    d8.qs = None
+    with pytest.raises(RuntimeError):
+        d8.decode(flags=kvq.KVQ_Q_FP8)

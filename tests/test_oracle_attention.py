@@ -184,15 +184,15 @@ def test_bad_block_id_is_reported():
 
 # ---------------------------------------------------------------- FP8-domain query mode
 
-def _q_hat(q_bits, q_scale, per_head):
-    """dec(enc(fp32(q) / sQ)) * sQ with the (separately pinned) codec, numpy
-    binary32 division."""
+def _q_hat(q_bits, q_scale, per_head, fmt):
+    """dec(enc(fp32(q) / sQ)) * sQ in the cache's format with the (separately
+    pinned) codec, numpy binary32 division."""
     qf = (np.asarray(q_bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
     hq = qf.shape[1]
     s = np.asarray(q_scale, np.float32)
     s = (s if per_head else np.repeat(s, hq)).reshape(1, hq, 1)
-    codes = oracle.encode(E4M3, (qf / s).astype(np.float32))
-    return oracle.decode(E4M3, codes) * s.astype(np.float64)
+    codes = oracle.encode(fmt, (qf / s).astype(np.float32))
+    return oracle.decode(fmt, codes) * s.astype(np.float64)
 
 
 @pytest.mark.parametrize("fmt,per_head", [(E4M3, False), (E4M3, True), (E5M2, True)])
@@ -203,7 +203,7 @@ def test_q_fp8_matches_sdpa_on_the_quantized_query(fmt, per_head):
     qs = (r.uniform(0.5, 2.0, Hq if per_head else 1) / 200).astype(np.float32)
     out = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_HEAD, fmt,
                              q_scale=qs)
-    qh = _q_hat(q, qs, per_head)
+    qh = _q_hat(q, qs, per_head, fmt)
     G = Hq // Hkv
     for b in range(B):
         Kh = torch.from_numpy(_gather(K, st, b, fmt, ks, PER_HEAD)).repeat_interleave(G, 0)
@@ -216,18 +216,20 @@ def test_q_fp8_matches_sdpa_on_the_quantized_query(fmt, per_head):
     assert not np.array_equal(plain, out)
 
 
-def test_q_fp8_is_exact_for_representable_queries():
-    """Queries that are E4M3 values times a power-of-two scale come back
-    unchanged, so the FP8-domain mode equals the plain one."""
-    r = np.random.default_rng(9)
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_q_fp8_is_exact_for_representable_queries(fmt):
+    """Queries that are codes of the cache's format times a power-of-two
+    scale come back unchanged, so the FP8-domain mode equals the plain one."""
+    r = np.random.default_rng(9 + fmt)
     B, Hq, Hkv, dh = 2, 4, 2, 64
-    st, _, K, V, ks, vs = _case(r, B, Hq, Hkv, dh, [30, 64], E4M3, PER_TENSOR)
-    codes = r.integers(0, 0x7F, size=(B, Hq, dh)).astype(np.uint8)  # finite E4M3 codes (no NaN)
-    codes[codes == 0x7F] = 0x7E
+    st, _, K, V, ks, vs = _case(r, B, Hq, Hkv, dh, [30, 64], fmt, PER_TENSOR)
+    top = 0x7E if fmt == E4M3 else 0x7B  # largest finite code
+    codes = r.integers(0, top + 1, size=(B, Hq, dh)).astype(np.uint8)
+    codes |= (r.integers(0, 2, size=codes.shape) << 7).astype(np.uint8)  # both signs
     sq = np.float32(2.0 ** -7)
-    q = bits_from(oracle.decode(E4M3, codes) * sq)  # exact in bf16 (at most 4 significant bits)
-    a = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_TENSOR, E4M3)
-    b = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_TENSOR, E4M3,
+    q = bits_from(oracle.decode(fmt, codes) * sq)  # exact in bf16 (at most 4 significant bits)
+    a = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_TENSOR, fmt)
+    b = oracle.decode_attn(q, K, V, st.block_tables, st.seq_lens, ks, vs, PER_TENSOR, fmt,
                            q_scale=np.array([sq], np.float32))
     np.testing.assert_array_equal(a, b)
 
