@@ -10,7 +10,8 @@ wraps it with ctypes over numpy arrays.
 Sources (page titles and sections):
   * "10.4 KV Cache quantization: INT8, KIVI 2-bit, FP8 KV", sections 10.4.1
     (KV size formula), 10.4.2 (write / read / attention over the dequantized
-    cache), 10.4.5 (FP8 path: cast_fp8(K/sK) then cast_float(K_fp8) * sK).
+    cache), 10.4.3 (per-token scales and their metadata bytes), 10.4.5 (FP8
+    path: cast_fp8(K/sK) then cast_float(K_fp8) * sK).
   * "vLLM FP8 quantized KV cache guide": scale shapes [1] (per tensor) and
     [num_kv_heads] (per attention head), ``fp8`` as an alias of ``fp8_e4m3``,
     uint8 storage with FP8 bit semantics; scale calibration, way two (scales
@@ -28,7 +29,7 @@ import threading
 import numpy as np
 
 BF16, E4M3, E5M2 = 0, 1, 2
-PER_TENSOR, PER_HEAD = 0, 1
+PER_TENSOR, PER_HEAD, PER_TOKEN_HEAD = 0, 1, 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvq_oracle.c")
@@ -75,6 +76,9 @@ def lib():
             L.kvqo_write.argtypes = [vp, vp, i64, vp, i64, i32, i32, vp, vp, i64, i32, vp, vp,
                                      i32, i32, i32]
             L.kvqo_write.restype = i64
+            L.kvqo_write_token_head.argtypes = [vp, vp, i64, vp, i64, i32, i32, vp, vp, i64,
+                                                i32, vp, vp, i32, i32]
+            L.kvqo_write_token_head.restype = i64
             L.kvqo_decode_attn.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, i32,
                                            vp, vp, i32, i32, vp, i32, i32, vp, i64, vp, i32]
             L.kvqo_decode_attn.restype = i64
@@ -133,9 +137,11 @@ def bf16_to_f64(bits) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def kv_bytes(layers: int, batch: int, kv_heads: int, seq: int, head_dim: int,
-             bytes_per_element: float) -> float:
-    """M_KV = 2 * L * B * Hkv * S * dh * bytes (2 = K and V; Hkv, not Hq)."""
-    return 2 * layers * batch * kv_heads * seq * head_dim * bytes_per_element
+             bytes_per_element: float, scale_bytes_per_row: float = 0) -> float:
+    """M_KV = 2 * L * B * Hkv * S * dh * bytes (2 = K and V; Hkv, not Hq),
+    plus, with per-(token, head) scales (section 10.4.3), the scale bytes of
+    each K row and each V row."""
+    return 2 * layers * batch * kv_heads * seq * (head_dim * bytes_per_element + scale_bytes_per_row)
 
 
 # --------------------------------------------------------------------------
@@ -151,14 +157,33 @@ def new_cache(num_blocks, num_kv_heads, block_size, head_dim, fmt, fill=0):
     return np.full(shape, fill, dtype=_cache_dtype(fmt))
 
 
+def new_scale_cache(num_blocks, num_kv_heads, block_size, fill=0.0):
+    """Per-(token, KV head) scales beside the pages: float32 [blocks][Hkv][bs]."""
+    return np.full((num_blocks, num_kv_heads, block_size), fill, dtype=np.float32)
+
+
 def write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, granularity, fmt,
           token_stride=None, nthreads=0) -> int:
-    """Quantize-and-scatter (in place on k_cache / v_cache). Returns bad-slot count."""
+    """Quantize-and-scatter (in place on k_cache / v_cache). Returns bad-slot count.
+
+    With ``granularity == PER_TOKEN_HEAD`` k_scale / v_scale are the scale
+    caches (float32 [blocks][Hkv][bs], from ``new_scale_cache``): every
+    written row's scale amax / fmt_max (1 if 0) is stored there, in place."""
     k = np.ascontiguousarray(k, dtype=np.uint16)
     v = np.ascontiguousarray(v, dtype=np.uint16)
     n, hkv, dh = k.shape
     stride = hkv * dh if token_stride is None else token_stride
     slot = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    if granularity == PER_TOKEN_HEAD:
+        nb, hkv2, bs, dh2 = k_cache.shape
+        assert fmt in (E4M3, E5M2) and hkv2 == hkv and dh2 == dh
+        for a in (k_scale, v_scale):
+            assert a.dtype == np.float32 and a.shape == (nb, hkv, bs) and a.flags.c_contiguous
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+        return int(lib().kvqo_write_token_head(_p(k), _p(v), stride, _p(slot), n, hkv, dh,
+                                               _p(k_cache), _p(v_cache), nb, bs, _p(k_scale),
+                                               _p(v_scale), fmt, nthreads))
     ks = np.ascontiguousarray(k_scale, dtype=np.float32)
     vs = np.ascontiguousarray(v_scale, dtype=np.float32)
     nb, hkv2, bs, dh2 = k_cache.shape

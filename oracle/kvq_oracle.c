@@ -13,9 +13,11 @@
  *                     P = softmax(Q K^T / sqrt(dh) + mask), O = P V^
  *     section 10.4.5  FP8 path: store cast_fp8(K / sK), compute with
  *                     cast_float(K_fp8) * sK
+ *     section 10.4.3  per-token scales: one scale per token along dh, so a
+ *                     new token is quantized on its own and appended
  *   "vLLM FP8 quantized KV cache guide" (per-tensor scales of shape [1],
  *     per-head k/v scales of shape [num_kv_heads]; fp8 = fp8_e4m3;
- *     cache storage is uint8 with FP8 bit semantics)
+ *     cache storage is uint8 with FP8 bit semantics; fp8_per_token_head)
  *
  * FP8 bit layouts are not printed on the pages; the oracle takes the OCP
  * 8-bit floating point formats: E4M3 (bias 7, no infinities, NaN = S.1111.111,
@@ -37,7 +39,7 @@
 #endif
 
 enum { KVQO_BF16 = 0, KVQO_E4M3 = 1, KVQO_E5M2 = 2 };
-enum { KVQO_PER_TENSOR = 0, KVQO_PER_HEAD = 1 };
+enum { KVQO_PER_TENSOR = 0, KVQO_PER_HEAD = 1, KVQO_PER_TOKEN_HEAD = 2 };
 
 /* ------------------------------------------------------------------------ */
 /* bf16 <-> f32 (bf16 is the top half of an IEEE binary32)                   */
@@ -231,6 +233,62 @@ int64_t kvqo_write(const uint16_t* k, const uint16_t* v, int64_t token_stride,
   return bad;
 }
 
+/* Per-(token, KV head) scale of one row of head_dim bf16 values: the largest
+ * magnitude among its finite values over the format's largest finite value
+ * (binary32 division), or 1 when that is 0 -- the row's largest value then
+ * lands on the format's largest code. */
+static float token_head_scale(const uint16_t* x, int head_dim, int fmt) {
+  float amax = 0.0f;
+  for (int d = 0; d < head_dim; ++d) {
+    const float a = fabsf(kvqo_bf16_to_f32(x[d]));
+    if (isfinite(a) && a > amax) amax = a;
+  }
+  const float fmt_max = (fmt == KVQO_E4M3) ? 448.0f : 57344.0f;
+  const float s = amax / fmt_max;
+  return s > 0.0f ? s : 1.0f;
+}
+
+/* Write with per-(token, KV head) scales ("10.4 KV Cache quantization",
+ * section 10.4.3, per-token granularity; vLLM's fp8_per_token_head): every
+ * row gets its own scale from its own values, stored beside the page in
+ * k_scale_cache / v_scale_cache [num_blocks][num_kv_heads][block_size]
+ * (binary32), and its codes are cast_fp8(x / s) as for the other
+ * granularities.  FP8 formats only.  Returns the bad-slot count. */
+int64_t kvqo_write_token_head(const uint16_t* k, const uint16_t* v, int64_t token_stride,
+                              const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                              int head_dim, uint8_t* k_cache, uint8_t* v_cache,
+                              int64_t num_blocks, int block_size, float* k_scale_cache,
+                              float* v_scale_cache, int fmt, int nthreads) {
+  int64_t bad = 0;
+  const int64_t capacity = num_blocks * (int64_t)block_size;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(static) reduction(+ : bad) num_threads(nthreads)
+#endif
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= capacity) {
+      bad += 1;
+      continue;
+    }
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const int64_t src = t * token_stride + (int64_t)h * head_dim;
+      const int64_t row = (blk * num_kv_heads + h) * block_size + off;
+      const float sk = token_head_scale(k + src, head_dim, fmt);
+      const float sv = token_head_scale(v + src, head_dim, fmt);
+      k_scale_cache[row] = sk;
+      v_scale_cache[row] = sv;
+      for (int d = 0; d < head_dim; ++d) {
+        k_cache[row * head_dim + d] = quantize_bf16(fmt, k[src + d], sk);
+        v_cache[row * head_dim + d] = quantize_bf16(fmt, v[src + d], sv);
+      }
+    }
+  }
+  return bad;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Decode attention over the dequantized cache, float64                      */
 /* ------------------------------------------------------------------------ */
@@ -242,13 +300,16 @@ static double cache_value(const void* cache, int64_t idx, int fmt, double s) {
   return kvqo_decode(fmt, ((const uint8_t*)cache)[idx]) * s;
 }
 
-/* One (sequence b, query head h) pair: the query attends to tokens
- * [lo, L) where L = seq_lens[b] and lo = L - window when a positive window
- * is shorter than L (the window keeps the newest tokens, the current one
- * included).  x_t = (sum_d q_d * K^_{t,d}) / sqrt(dh); p = softmax(x);
- * O = sum_t p_t * V^_t.  Query head h reads KV head h / (Hq / Hkv).
- * q_scale is not applied: the stored-FP8 path leaves Q in its own dtype.
- * Returns 0, or -1 when the block table or length is out of range. */
+/* Scale of KV head g for the token in block blk at offset off: one per
+ * tensor, one per KV head, or -- per (token, KV head) -- the one stored
+ * beside the page, [num_blocks][num_kv_heads][block_size]. */
+static double scale_at(const float* s, int granularity, int num_kv_heads, int block_size,
+                       int64_t blk, int g, int off) {
+  if (granularity == KVQO_PER_TOKEN_HEAD)
+    return (double)s[(blk * num_kv_heads + g) * block_size + off];
+  return (double)s[granularity == KVQO_PER_HEAD ? g : 0];
+}
+
 /* Query element d of head h as the attention uses it: the bf16 value, or --
  * with a q scale (the FP8-domain mode) -- the query quantized to the cache's
  * FP8 format with the head's scale and restored, dec(enc(fp32(q) / sQ)) * sQ,
@@ -263,6 +324,12 @@ static double query_value(uint16_t qb, int fmt, const float* q_scale, int q_per_
   return kvqo_decode(fmt, kvqo_encode(fmt, quotient)) * (double)sq;
 }
 
+/* One (sequence b, query head h) pair: the query attends to tokens
+ * [lo, L) where L = seq_lens[b] and lo = L - window when a positive window
+ * is shorter than L (the window keeps the newest tokens, the current one
+ * included).  x_t = (sum_d q_d * K^_{t,d}) / sqrt(dh); p = softmax(x);
+ * O = sum_t p_t * V^_t.  Query head h reads KV head h / (Hq / Hkv).
+ * Returns 0, or -1 when the block table or length is out of range. */
 static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
                        const int32_t* block_tables, int max_blocks_per_seq,
                        const int32_t* seq_lens, int num_q_heads, int num_kv_heads,
@@ -277,8 +344,6 @@ static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
   if (L <= 0) return L < 0 ? -1 : 0;
   if (L > max_blocks_per_seq * block_size) return -1;
   const int lo = (window > 0 && L > window) ? L - window : 0;
-  const double sk = (fmt == KVQO_BF16) ? 1.0 : (double)k_scale[granularity == KVQO_PER_HEAD ? g : 0];
-  const double sv = (fmt == KVQO_BF16) ? 1.0 : (double)v_scale[granularity == KVQO_PER_HEAD ? g : 0];
   const uint16_t* qrow = q + ((int64_t)b * num_q_heads + h) * head_dim;
   const double inv_sqrt_dh = 1.0 / sqrt((double)head_dim);
 
@@ -287,6 +352,10 @@ static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
     const int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
     if (blk < 0 || blk >= num_blocks) return -1;
     const int64_t base = (((int64_t)blk * num_kv_heads + g) * block_size + t % block_size) * head_dim;
+    const double sk = (fmt == KVQO_BF16)
+                          ? 1.0
+                          : scale_at(k_scale, granularity, num_kv_heads, block_size, blk, g,
+                                     t % block_size);
     double dot = 0.0;
     for (int d = 0; d < head_dim; ++d)
       dot += query_value(qrow[d], fmt, q_scale, q_per_head, h) * cache_value(kc, base + d, fmt, sk);
@@ -303,6 +372,10 @@ static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
   for (int t = lo; t < L; ++t) {
     const int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
     const int64_t base = (((int64_t)blk * num_kv_heads + g) * block_size + t % block_size) * head_dim;
+    const double sv = (fmt == KVQO_BF16)
+                          ? 1.0
+                          : scale_at(v_scale, granularity, num_kv_heads, block_size, blk, g,
+                                     t % block_size);
     const double p = scores[t - lo];
     for (int d = 0; d < head_dim; ++d) out[d] += p * cache_value(vc, base + d, fmt, sv);
   }
@@ -360,7 +433,8 @@ int64_t kvqo_decode_attn(const uint16_t* q, const void* k_cache, const void* v_c
 /* ------------------------------------------------------------------------ */
 
 /* The "independent dequant kernel" of the unfused path: every code c of KV
- * head h becomes bf16(fp32(cast_float(c) * s_h)).  The product of an FP8
+ * head h becomes bf16(fp32(cast_float(c) * s_h)), s_h the tensor's, the
+ * head's or the (token, head)'s scale.  The product of an FP8
  * value (at most 4 significant bits) and a binary32 scale is exact in
  * float64, so the float cast below is the single binary32 rounding of the
  * product, followed by RNE to bf16. */
@@ -369,9 +443,10 @@ void kvqo_dequant(const uint8_t* src, uint16_t* dst, int64_t num_blocks, int num
   const int64_t per_head = (int64_t)block_size * head_dim;
   for (int64_t blk = 0; blk < num_blocks; ++blk) {
     for (int h = 0; h < num_kv_heads; ++h) {
-      const double s = (double)scale[granularity == KVQO_PER_HEAD ? h : 0];
       const int64_t base = (blk * num_kv_heads + h) * per_head;
       for (int64_t i = 0; i < per_head; ++i) {
+        const double s = scale_at(scale, granularity, num_kv_heads, block_size, blk, h,
+                                  (int)(i / head_dim));
         const float prod = (float)(kvqo_decode(fmt, src[base + i]) * s);
         dst[base + i] = kvqo_f32_to_bf16(prod);
       }
