@@ -82,6 +82,9 @@ def lib():
             L.kvqo_decode_attn.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, i32,
                                            vp, vp, i32, i32, vp, i32, i32, vp, i64, vp, i32]
             L.kvqo_decode_attn.restype = i64
+            L.kvqo_prefill_attn.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64,
+                                            i32, vp, vp, i32, i32, vp, i32, i32, vp, i64, vp, i32]
+            L.kvqo_prefill_attn.restype = i64
             L.kvqo_dequant.argtypes = [vp, vp, i64, i32, i32, i32, vp, i32, i32]
             L.kvqo_max_threads.restype = i32
             _lib = L
@@ -227,6 +230,46 @@ def decode_attn(q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale, g
                                  window, _p(pr), npairs, _p(out), nthreads)
     if bad:
         raise ValueError(f"oracle decode: {bad} (sequence, head) pairs had out-of-range inputs")
+    return out
+
+
+def prefill_attn(q, cu_q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
+                 granularity, fmt, window=0, pairs=None, nthreads=0, q_scale=None) -> np.ndarray:
+    """Float64 prefill / prefix-hit attention over the dequantized paged cache.
+
+    q: bf16 bits [total_q][Hq][dh]; cu_q int [B+1] query row offsets.  The
+    n_b = cu_q[b+1] - cu_q[b] queries of sequence b are its last n_b tokens
+    (positions L_b - n_b .. L_b - 1, L_b = seq_lens[b]); each attends causally
+    to the cached tokens up to its own position.  Returns float64
+    [total_q][Hq][dh], or [len(pairs)][dh] for pairs of (query row, head)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    total_q, hq, dh = q.shape
+    cu = np.ascontiguousarray(cu_q, dtype=np.int32)
+    B = cu.size - 1
+    assert cu[0] == 0 and cu[-1] == total_q
+    nb, hkv, bs, dh2 = k_cache.shape
+    assert dh2 == dh
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    ks = np.ascontiguousarray(k_scale if k_scale is not None else [1.0], dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale if v_scale is not None else [1.0], dtype=np.float32)
+    if pairs is None:
+        out = np.empty((total_q, hq, dh), dtype=np.float64)
+        pr, npairs = None, 0
+    else:
+        pr = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+        npairs = pr.shape[0]
+        out = np.empty((npairs, dh), dtype=np.float64)
+    qs = None if q_scale is None else np.ascontiguousarray(q_scale, dtype=np.float32).reshape(-1)
+    if qs is not None and qs.size not in (1, hq):
+        raise ValueError("q_scale must have 1 or num_q_heads entries")
+    bad = lib().kvqo_prefill_attn(_p(q), _p(cu), _p(np.ascontiguousarray(k_cache)),
+                                  _p(np.ascontiguousarray(v_cache)), _p(bt), bt.shape[1], _p(sl),
+                                  B, hq, hkv, dh, nb, bs, _p(ks), _p(vs), granularity, fmt,
+                                  _p(qs), 0 if qs is None else int(qs.size == hq and hq > 1),
+                                  window, _p(pr), npairs, _p(out), nthreads)
+    if bad:
+        raise ValueError(f"oracle prefill: {bad} (row, head) pairs had out-of-range inputs")
     return out
 
 

@@ -324,27 +324,24 @@ static double query_value(uint16_t qb, int fmt, const float* q_scale, int q_per_
   return kvqo_decode(fmt, kvqo_encode(fmt, quotient)) * (double)sq;
 }
 
-/* One (sequence b, query head h) pair: the query attends to tokens
- * [lo, L) where L = seq_lens[b] and lo = L - window when a positive window
- * is shorter than L (the window keeps the newest tokens, the current one
- * included).  x_t = (sum_d q_d * K^_{t,d}) / sqrt(dh); p = softmax(x);
- * O = sum_t p_t * V^_t.  Query head h reads KV head h / (Hq / Hkv).
- * Returns 0, or -1 when the block table or length is out of range. */
-static int decode_pair(const uint16_t* q, const void* kc, const void* vc,
-                       const int32_t* block_tables, int max_blocks_per_seq,
-                       const int32_t* seq_lens, int num_q_heads, int num_kv_heads,
-                       int head_dim, int64_t num_blocks, int block_size,
-                       const float* k_scale, const float* v_scale, int granularity, int fmt,
-                       const float* q_scale, int q_per_head,
-                       int window, int b, int h, double* out, double* scores) {
+/* One query row qrow of head h of sequence b that attends to the tokens
+ * [lo, L) of the sequence, lo = L - window when a positive window is shorter
+ * than L (the window keeps the newest tokens, the query's own included).
+ * x_t = (sum_d q_d * K^_{t,d}) / sqrt(dh); p = softmax(x); O = sum_t p_t V^_t.
+ * Query head h reads KV head h / (Hq / Hkv).  Returns 0, or -1 when the
+ * block table or length is out of range. */
+static int attend_row(const uint16_t* qrow, int L, const void* kc, const void* vc,
+                      const int32_t* block_tables, int max_blocks_per_seq, int num_q_heads,
+                      int num_kv_heads, int head_dim, int64_t num_blocks, int block_size,
+                      const float* k_scale, const float* v_scale, int granularity, int fmt,
+                      const float* q_scale, int q_per_head, int window, int b, int h,
+                      double* out, double* scores) {
   const int group = num_q_heads / num_kv_heads;
   const int g = h / group;
-  const int L = seq_lens[b];
   for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
   if (L <= 0) return L < 0 ? -1 : 0;
   if (L > max_blocks_per_seq * block_size) return -1;
   const int lo = (window > 0 && L > window) ? L - window : 0;
-  const uint16_t* qrow = q + ((int64_t)b * num_q_heads + h) * head_dim;
   const double inv_sqrt_dh = 1.0 / sqrt((double)head_dim);
 
   double xmax = -INFINITY;
@@ -417,10 +414,79 @@ int64_t kvqo_decode_attn(const uint16_t* q, const void* k_cache, const void* v_c
         b = (int)(i / num_q_heads);
         h = (int)(i % num_q_heads);
       }
-      if (decode_pair(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
-                      num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, k_scale,
-                      v_scale, granularity, fmt, q_scale, q_per_head, window, b, h,
-                      out + i * head_dim, scores))
+      /* the decode query is the sequence's last token: it attends to [lo, L) */
+      if (attend_row(q + ((int64_t)b * num_q_heads + h) * head_dim, seq_lens[b], k_cache,
+                     v_cache, block_tables, max_blocks_per_seq, num_q_heads, num_kv_heads,
+                     head_dim, num_blocks, block_size, k_scale, v_scale, granularity, fmt,
+                     q_scale, q_per_head, window, b, h, out + i * head_dim, scores))
+        bad += 1;
+    }
+    free(scores);
+  }
+  return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Prefill / prefix-hit attention: several new query tokens per sequence      */
+/* ------------------------------------------------------------------------ */
+
+/* "10.4 KV Cache quantization", section 10.4.2: the prefill and prefix-hit
+ * paths read the same quantized cache as the decode.  Sequence b holds
+ * L_b = seq_lens[b] tokens in the cache, the last n_b = cu_q[b+1] - cu_q[b]
+ * of them new; query row cu_q[b] + j (j < n_b) is the token at position
+ * pos = L_b - n_b + j and attends causally to the tokens [lo, pos], lo as
+ * for the decode with L = pos + 1 (a sliding window keeps the newest
+ * `window` of them).  With n_b = 1 this is the decode.  q and out are
+ * [total_q][Hq][dh].  pairs (int32 [npairs][2] of (query row, head)) picks
+ * rows; NULL takes all.  Returns the number of rows with out-of-range
+ * inputs (n_b > L_b, a bad length or block id). */
+int64_t kvqo_prefill_attn(const uint16_t* q, const int32_t* cu_q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_tables,
+                          int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int64_t num_blocks,
+                          int block_size, const float* k_scale, const float* v_scale,
+                          int granularity, int fmt, const float* q_scale, int q_per_head,
+                          int window, const int32_t* pairs, int64_t npairs, double* out,
+                          int nthreads) {
+  const int64_t total_q = cu_q[num_seqs];
+  const int64_t n = pairs ? npairs : total_q * num_q_heads;
+  int max_len = 0;
+  for (int b = 0; b < num_seqs; ++b)
+    if (seq_lens[b] > max_len) max_len = seq_lens[b];
+  int64_t bad = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(+ : bad)
+#endif
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 16)
+#endif
+    for (int64_t i = 0; i < n; ++i) {
+      int64_t row;
+      int h;
+      if (pairs) {
+        row = pairs[2 * i];
+        h = pairs[2 * i + 1];
+      } else {
+        row = i / num_q_heads;
+        h = (int)(i % num_q_heads);
+      }
+      int b = 0; /* the sequence holding query row `row` */
+      while (b + 1 < num_seqs && cu_q[b + 1] <= row) ++b;
+      const int64_t nb_q = cu_q[b + 1] - cu_q[b];
+      const int64_t pos = (int64_t)seq_lens[b] - nb_q + (row - cu_q[b]);
+      double* o = out + i * head_dim;
+      if (nb_q > seq_lens[b] || pos < 0) {
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        bad += 1;
+        continue;
+      }
+      if (attend_row(q + (row * num_q_heads + h) * head_dim, (int)(pos + 1), k_cache, v_cache,
+                     block_tables, max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim,
+                     num_blocks, block_size, k_scale, v_scale, granularity, fmt, q_scale,
+                     q_per_head, window, b, h, o, scores))
         bad += 1;
     }
     free(scores);
