@@ -60,6 +60,19 @@ def decode_bytes(n_tokens: int, n_heads: int = HQ) -> int:
             + ((n_tokens + BS - 1) // BS) * 4 + 4 + 2 * HKV * 4)
 
 
+def write_bytes_token_head(n_tokens: int) -> int:
+    """The write with per-(token, head) scales: the same, plus the fp32 scale
+    of every K and V row."""
+    return write_bytes(n_tokens) + n_tokens * 2 * HKV * 4
+
+
+def decode_bytes_token_head(n_tokens: int) -> int:
+    """The decode with per-(token, head) scales: the 16 K and 16 V fp32 scales
+    of every page read beside it instead of the per-head scales."""
+    pages = (n_tokens + BS - 1) // BS
+    return decode_bytes(n_tokens) - 2 * HKV * 4 + pages * HKV * 2 * BS * 4
+
+
 STEP_WRITE_BYTES = LAYERS * write_bytes(SEQ)
 STEP_DECODE_BYTES = LAYERS * decode_bytes(SEQ)
 STEP_BYTES = STEP_WRITE_BYTES + STEP_DECODE_BYTES
@@ -274,6 +287,29 @@ def run_gpu(args, rank, world, local_rank):
     g_calib = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_calib):
         calibrations()
+    # Per-(token, head) scales: every layer's write into the same caches with
+    # its scale caches beside them, then the decodes reading them.  Timed
+    # after the per-head graphs (it rewrites the caches).
+    for x in L:
+        x["ksc"] = kvq.new_scale_cache(st.num_blocks, HKV, dev)
+        x["vsc"] = kvq.new_scale_cache(st.num_blocks, HKV, dev)
+
+    def writes_th():
+        for x in L:
+            kvq.kvq_write_token_head(x["k"], x["v"], slots, x["kc"], x["vc"], x["ksc"], x["vsc"],
+                                     E4, dev_status=status)
+
+    def decodes_th():
+        for x in L:
+            kvq.kvq_decode_attn(x["q"], x["kc"], x["vc"], bt, sl, None, x["ksc"], x["vsc"],
+                                kvq.KVQ_SCALE_PER_TOKEN_HEAD, E4, 0, ws, x["out"],
+                                dev_status=status)
+
+    g_write_th, g_decode_th = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_write_th):
+        writes_th()
+    with torch.cuda.graph(g_decode_th):
+        decodes_th()
     stream = torch.cuda.current_stream()
 
     def step(_timed=False):
@@ -311,6 +347,10 @@ def run_gpu(args, rank, world, local_rank):
         ready_total = timed_replays(g_decode_ready.replay, args.steps)
         qf8_total = timed_replays(g_decode_qf8.replay, args.steps)
         calib_total = timed_replays(g_calib.replay, args.steps)
+        g_write_th.replay()  # the caches now hold per-token-head codes
+        g_decode_th.replay()
+        write_th_total = timed_replays(g_write_th.replay, args.steps)
+        decode_th_total = timed_replays(g_decode_th.replay, args.steps)
     barrier()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     ms_step = rank_max(total_ms) / args.steps
@@ -319,6 +359,8 @@ def run_gpu(args, rank, world, local_rank):
     ready_ms = rank_max(ready_total) / args.steps
     qf8_ms = rank_max(qf8_total) / args.steps
     calib_ms = rank_max(calib_total) / args.steps
+    write_th_us = rank_max(write_th_total) / args.steps * 1e3 / LAYERS
+    decode_th_us = rank_max(decode_th_total) / args.steps * 1e3 / LAYERS
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barrier,
@@ -368,6 +410,16 @@ def run_gpu(args, rank, world, local_rank):
         "kv_calibrate": {"gbs": round(c_ach, 1), "frac_of_peak": round(c_ach / peak, 4),
                          "us_per_layer": round(calib_launch_us, 2),
                          "what": "per-head amax scales of one layer's 32768 bf16 K/V tokens"},
+        "kv_write_token_head": {
+            "gbs": round(write_bytes_token_head(SEQ) / (write_th_us * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(write_bytes_token_head(SEQ) / (write_th_us * 1e-6) / 1e9 / peak, 4),
+            "us_per_layer": round(write_th_us, 2),
+            "what": "kvq_write_token_head: per-(token, head) amax scales stored beside the pages"},
+        "decode_attn_token_head": {
+            "gbs": round(decode_bytes_token_head(SEQ) / (decode_th_us * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(decode_bytes_token_head(SEQ) / (decode_th_us * 1e-6) / 1e9 / peak, 4),
+            "us_per_layer": round(decode_th_us, 2),
+            "what": "decode reading the per-(token, head) scale caches"},
         "kv_write": {"gbs": round(w_ach, 1), "frac_of_peak": round(w_ach / peak, 4),
                      "us_per_layer": round(write_launch_us, 2),
                      "tok_s": round(SEQ / (write_launch_us * 1e-6), 0)},
@@ -380,7 +432,9 @@ def run_gpu(args, rank, world, local_rank):
         "timing": "CUDA graphs (32 writes, 32 decodes) replayed; events on the replay stream; "
                   "per-kernel figures from replaying each graph alone; decode_attn_cache_ready "
                   "replays the 32 decodes with KVQ_CACHE_READY, decode_attn_q_fp8 with "
-                  "KVQ_Q_FP8, and kv_calibrate 32 scale calibrations (none part of the step)",
+                  "KVQ_Q_FP8, kv_calibrate 32 scale calibrations, kv_write_token_head and "
+                  "decode_attn_token_head the per-(token, head) scale mode (none part of the "
+                  "step)",
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

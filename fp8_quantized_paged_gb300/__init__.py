@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
 
 KVQ_FMT_BF16, KVQ_FMT_E4M3, KVQ_FMT_E5M2 = 0, 1, 2
-KVQ_SCALE_PER_TENSOR, KVQ_SCALE_PER_HEAD = 0, 1
+KVQ_SCALE_PER_TENSOR, KVQ_SCALE_PER_HEAD, KVQ_SCALE_PER_TOKEN_HEAD = 0, 1, 2
 KVQ_OK, KVQ_ERR_NULL, KVQ_ERR_SHAPE, KVQ_ERR_ALIGN = 0, -1, -2, -3
 KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA, KVQ_ERR_ARG = -4, -5, -6, -7
 KVQ_DEV_BAD_SLOT, KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
@@ -32,6 +32,8 @@ _vp, _i32, _i64, _u32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctyp
 SIGNATURES = {
     "kvq_write": (_i32, [_vp, _vp, _i64, _vp, _i64, _i32, _i32, _vp, _vp, _i64, _i32, _vp, _i32,
                          _vp, _i32, _i32, _i32, _vp, _vp]),
+    "kvq_write_token_head": (_i32, [_vp, _vp, _i64, _vp, _i64, _i32, _i32, _vp, _vp, _i64, _i32,
+                                    _vp, _vp, _i32, _vp, _vp]),
     "kvq_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "kvq_decode_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
                                _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _u32, _vp, _sz,
@@ -115,6 +117,27 @@ def kvq_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, scale_gran
                         _ptr(v_cache), nb, bs, _ptr(k_scale), _len(k_scale), _ptr(v_scale),
                         _len(v_scale), scale_granularity, fmt, _ptr(dev_status), _stream(stream))
     _check(st, "kvq_write")
+
+
+def kvq_write_token_head(k, v, slot_mapping, k_cache, v_cache, k_scale_cache, v_scale_cache,
+                         fmt, dev_status=None, stream=None, token_stride=None) -> None:
+    """Quantize-and-scatter with per-(token, KV head) scales: every written
+    row's scale amax / fmt_max goes to the scale caches fp32
+    [num_blocks][Hkv][16] (see ``new_scale_cache``)."""
+    n, hkv, dh = k.shape
+    stride = k.stride(0) if token_stride is None else token_stride
+    if v.stride(0) != stride or k.stride(1) != dh or k.stride(2) != 1 or v.stride(1) != dh:
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_write_token_head")
+    nb, hkv2, bs, dh2 = k_cache.shape
+    if (hkv2, dh2) != (hkv, dh) or v_cache.shape != k_cache.shape or tuple(v.shape) != (n, hkv, dh):
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_write_token_head")
+    for sc in (k_scale_cache, v_scale_cache):
+        if tuple(sc.shape) != (nb, hkv, bs) or not sc.is_contiguous():
+            raise KvqError(KVQ_ERR_SHAPE, "kvq_write_token_head")
+    st = _lib.kvq_write_token_head(_ptr(k), _ptr(v), stride, _ptr(slot_mapping), n, hkv, dh,
+                                   _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(k_scale_cache),
+                                   _ptr(v_scale_cache), fmt, _ptr(dev_status), _stream(stream))
+    _check(st, "kvq_write_token_head")
 
 
 def kvq_calibrate_scales(k, v, k_scale, v_scale, scale_granularity, fmt, dev_status=None,
@@ -212,6 +235,12 @@ def new_cache(num_blocks, num_kv_heads, head_dim, fmt, device="cuda"):
     import torch
     dt = torch.bfloat16 if fmt == KVQ_FMT_BF16 else torch.uint8
     return torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE, head_dim), dtype=dt, device=device)
+
+
+def new_scale_cache(num_blocks, num_kv_heads, device="cuda"):
+    """Per-(token, KV head) scales beside the pages: fp32 [num_blocks][Hkv][16]."""
+    import torch
+    return torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE), dtype=torch.float32, device=device)
 
 
 KVQ_WS_COUNTER_BYTES = 65536 * 4  # leading workspace bytes that must start at zero

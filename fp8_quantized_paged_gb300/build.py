@@ -1,6 +1,7 @@
 """Build libkvq.so in-tree with nvcc for sm_103a (GB300).
 
-Each CUDA source compiles to an object in parallel, then nvcc links the
+Each CUDA source compiles to an object in parallel (the decode kernels once
+per cache format and head size), then nvcc links the
 shared library (static CUDA runtime, no libcuda link: the tensor-map encoder
 is looked up through the runtime's driver entry-point query).
 """
@@ -16,8 +17,15 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
-SOURCES = ["kvq_host.cu", "kvq_write.cu", "kvq_decode.cu", "kvq_static.cu", "kvq_calib.cu"]
-HEADERS = ["kvq_common.cuh", "kvq_host.h"]
+SOURCES = ["kvq_host.cu", "kvq_write.cu", "kvq_decode.cu", "kvq_static.cu", "kvq_calib.cu",
+           "kvq_decode_variant.cu"]
+HEADERS = ["kvq_common.cuh", "kvq_host.h", "kvq_decode.cuh"]
+# (object, source, defines): one object per translation unit, the decode
+# variants once per (format, head size); kvq_fmt 0 = BF16, 1 = E4M3, 2 = E5M2
+UNITS = [(os.path.splitext(s)[0], s, []) for s in SOURCES if s != "kvq_decode_variant.cu"] + [
+    (f"kvq_decode_f{fmt}_d{dh}", "kvq_decode_variant.cu",
+     [f"-DKVQ_VARIANT_FMT={fmt}", f"-DKVQ_VARIANT_DH={dh}"])
+    for fmt in (1, 2, 0) for dh in (128, 64)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]
@@ -49,9 +57,10 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     nvcc = _nvcc()
     extra = list(extra or [])
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(unit):
+        name, src, defines = unit
+        obj = os.path.join(BUILD, name + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *defines, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -61,8 +70,8 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
             print(r.stderr, file=sys.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+    with cf.ThreadPoolExecutor(max_workers=min(len(UNITS), max(2, os.cpu_count() or 2))) as ex:
+        objs = list(ex.map(compile_one, UNITS))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -31,25 +31,6 @@ struct CalibParams {
   uint32_t* status;
 };
 
-// Magnitudes of the finite values of two bf16 (one word); NaN and +-inf
-// count as 0.
-KVQ_DEVI uint32_t finite_mag2(uint32_t w) {
-  const uint32_t m = w & 0x7FFF7FFFu;
-  return m & __vcmpltu2(m, 0x7F807F80u);
-}
-
-KVQ_DEVI uint32_t max_mag16(uint32_t acc, const uint4& a, const uint4& b) {
-  acc = __vmaxu2(acc, finite_mag2(a.x));
-  acc = __vmaxu2(acc, finite_mag2(a.y));
-  acc = __vmaxu2(acc, finite_mag2(a.z));
-  acc = __vmaxu2(acc, finite_mag2(a.w));
-  acc = __vmaxu2(acc, finite_mag2(b.x));
-  acc = __vmaxu2(acc, finite_mag2(b.y));
-  acc = __vmaxu2(acc, finite_mag2(b.z));
-  acc = __vmaxu2(acc, finite_mag2(b.w));
-  return acc;
-}
-
 template <int DH>
 __global__ void __launch_bounds__(256, 4) calib_kernel(const CalibParams p) {
   constexpr int CH = DH / 16;  // chunks of a head row; divides 32

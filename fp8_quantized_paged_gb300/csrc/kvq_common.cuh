@@ -268,4 +268,25 @@ KVQ_DEVI float fast_exp2(float x) {
   return r;
 }
 
+// Largest finite magnitude among bf16 values, two at a time: the magnitudes
+// of the finite values of one word (NaN and +-inf count as 0), and the
+// running per-half maxima over sixteen values (non-negative bf16 order like
+// their unsigned bit patterns).
+KVQ_DEVI uint32_t finite_mag2(uint32_t w) {
+  const uint32_t m = w & 0x7FFF7FFFu;
+  return m & __vcmpltu2(m, 0x7F807F80u);
+}
+
+KVQ_DEVI uint32_t max_mag16(uint32_t acc, const uint4& a, const uint4& b) {
+  acc = __vmaxu2(acc, finite_mag2(a.x));
+  acc = __vmaxu2(acc, finite_mag2(a.y));
+  acc = __vmaxu2(acc, finite_mag2(a.z));
+  acc = __vmaxu2(acc, finite_mag2(a.w));
+  acc = __vmaxu2(acc, finite_mag2(b.x));
+  acc = __vmaxu2(acc, finite_mag2(b.y));
+  acc = __vmaxu2(acc, finite_mag2(b.z));
+  acc = __vmaxu2(acc, finite_mag2(b.w));
+  return acc;
+}
+
 }  // namespace kvq

@@ -5,6 +5,12 @@
 // the cache stores cast_fp8(K / sK); section 10.4.2: the inefficient path
 // runs an independent dequant kernel that writes a 16-bit KV back to HBM.
 //
+// With per-(token, KV head) scales ("10.4 KV Cache quantization", section
+// 10.4.3, per-token granularity) the write derives each row's scale from the
+// row itself, s = amax / fmt_max over its finite values (1 if 0), stores it
+// in a binary32 scale cache [num_blocks][Hkv][16] beside the pages and
+// quantizes the row with it.
+//
 // Both kernels are HBM streams.  One thread owns 16 contiguous elements of
 // one (token, KV head) row: two 16-byte bf16 loads per tensor, one 16-byte
 // FP8 store (or two 16-byte bf16 stores), so a warp moves whole 128-byte
@@ -30,6 +36,8 @@ struct WriteParams {
   const float* ks;
   const float* vs;
   int per_head;
+  float* ksc;  // per-(token, head) scale caches [num_blocks][Hkv][16] (token-head mode)
+  float* vsc;
   uint32_t* status;
   int64_t in_elems;     // extent of k / v in elements
   int64_t cache_elems;  // elements of one cache tensor
@@ -106,12 +114,27 @@ KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, const HeadScale& h) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Scale of one (token, KV head) row held by CH consecutive lanes (aligned to
+// CH in the warp; mask = those lanes): the largest finite magnitude of the
+// row over the format's largest finite value (binary32 division), or 1 when
+// that is 0.
+template <int FMT, int CH>
+KVQ_DEVI float row_scale(const uint4& a, const uint4& b, uint32_t mask) {
+  const uint32_t m2 = max_mag16(0u, a, b);
+  uint32_t am = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+#pragma unroll
+  for (int off = 1; off < CH; off <<= 1) am = max(am, __shfl_xor_sync(mask, am, off));
+  const float q = __fdiv_rn(__uint_as_float(am), FMT == KVQ_FMT_E4M3 ? 448.f : 57344.f);
+  return q > 0.f ? q : 1.f;
+}
+
 // One thread per 16-element chunk (h, c) of the (token, KV head) rows.  The
 // grid's thread count is a multiple of the Hkv * DH/16 chunks of a token, so
 // a thread keeps its chunk (and its head's scales) and strides over tokens;
 // the next token's K/V and slot loads are issued before the current token is
 // converted.
-template <int FMT, int DH>
+// TS: per-(token, head) scales, computed by the CH lanes of each row.
+template <int FMT, int DH, bool TS>
 __global__ void __launch_bounds__(256, 3) write_kernel(const WriteParams p) {
   constexpr int CH = DH / 16;
   pdl_allow_next();
@@ -125,7 +148,10 @@ __global__ void __launch_bounds__(256, 3) write_kernel(const WriteParams p) {
   int64_t t = gtid / row_units;
   if (t >= p.num_tokens) return;
   HeadScale hk, hv;
-  if (FMT != KVQ_FMT_BF16) {
+  // the CH lanes of this thread's row (a token's rows are whole, aligned
+  // lane groups: the block is a multiple of Hkv * CH threads, or of 256)
+  const uint32_t row_mask = (CH == 8 ? 0xFFu : 0xFu) << (threadIdx.x & 31 & ~(CH - 1));
+  if (FMT != KVQ_FMT_BF16 && !TS) {
     hk = head_scale(__ldg(p.ks + (p.per_head ? h : 0)));
     hv = head_scale(__ldg(p.vs + (p.per_head ? h : 0)));
   }
@@ -151,6 +177,10 @@ __global__ void __launch_bounds__(256, 3) write_kernel(const WriteParams p) {
     uint4 kn[2], vn[2];
     int64_t sn = -1;
     if (tn < p.num_tokens) load(tn, kn, vn, sn);
+    if (TS) {  // every lane of the row takes part, whatever its slot
+      hk = head_scale(row_scale<FMT, CH>(k[0], k[1], row_mask));
+      hv = head_scale(row_scale<FMT, CH>(v[0], v[1], row_mask));
+    }
     if (slot >= p.capacity) {
       if (rem == 0) flag_status(p.status, KVQ_DEV_BAD_SLOT);
     } else if (slot >= 0) {  // a negative slot is a padding token
@@ -166,6 +196,11 @@ __global__ void __launch_bounds__(256, 3) write_kernel(const WriteParams p) {
         } else {
           *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.kc) + dst) = quantize16<FMT>(k[0], k[1], hk);
           *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.vc) + dst) = quantize16<FMT>(v[0], v[1], hv);
+          if (TS && rem % CH == 0) {
+            const int64_t row = ((slot >> 4) * p.hkv + h) * 16 + (slot & 15);
+            p.ksc[row] = hk.s;
+            p.vsc[row] = hv.s;
+          }
         }
       }
     }
@@ -186,7 +221,7 @@ struct DequantParams {
   int chunks_per_head;  // block_size * head_dim / 16
   int hkv;
   const float* scale;
-  int per_head;
+  int gran;  // kvq_gran: [1], [Hkv] or [num_blocks][Hkv][16] scales
 };
 
 // Sixteen FP8 codes -> sixteen bf16: exact FP8 -> f16 -> f32, one binary32
@@ -199,7 +234,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < p.units;
        u += stride) {
     const int h = static_cast<int>((u / p.chunks_per_head) % p.hkv);
-    const float s = __ldg(p.scale + (p.per_head ? h : 0));
+    // the token row of chunk u is u / (chunks per row), chunks_per_head / 16
+    const int64_t si = p.gran == KVQ_SCALE_PER_TOKEN_HEAD ? u / (p.chunks_per_head / 16)
+                                                          : (p.gran == KVQ_SCALE_PER_HEAD ? h : 0);
+    const float s = __ldg(p.scale + si);
     const uint4 c = __ldcs(reinterpret_cast<const uint4*>(p.src) + u);
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
     uint32_t o[8];
@@ -225,6 +263,65 @@ static int grid_for(int64_t units, int threads) {
   return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
+// Shape checks and launch shared by the two write entry points.
+static int write_common(const void* k, const void* v, int64_t token_stride,
+                        const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                        int head_dim, void* k_cache, void* v_cache, int64_t num_blocks,
+                        int block_size, int fmt, WriteParams& p, bool token_scales,
+                        uint32_t* dev_status, kvq_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return KVQ_ERR_ARG;
+  if (!k_cache || !v_cache) return KVQ_ERR_NULL;
+  if (num_tokens > 0 && (!k || !v || !slot_mapping)) return KVQ_ERR_NULL;
+  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
+  if (token_stride < static_cast<int64_t>(num_kv_heads) * head_dim) return KVQ_ERR_SHAPE;
+  if (token_stride % 8 != 0) return KVQ_ERR_ALIGN;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return KVQ_ERR_ALIGN;
+  if (num_blocks > (INT64_MAX / 16) / (static_cast<int64_t>(num_kv_heads) * head_dim))
+    return KVQ_ERR_SHAPE;
+  if (num_tokens == 0) return KVQ_OK;
+
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.token_stride = token_stride;
+  p.slots = slot_mapping;
+  p.num_tokens = num_tokens;
+  p.hkv = num_kv_heads;
+  p.dh = head_dim;
+  p.kc = k_cache;
+  p.vc = v_cache;
+  p.capacity = num_blocks * block_size;
+  p.status = dev_status;
+  p.in_elems = (num_tokens - 1) * token_stride + static_cast<int64_t>(num_kv_heads) * head_dim;
+  p.cache_elems = num_blocks * num_kv_heads * block_size * head_dim;
+  int grid = 0, block = 0;
+  token_row_shape(num_tokens, num_kv_heads * (head_dim / 16), 3, grid, block);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const dim3 gd(grid), bd(block);
+#define KVQ_WRITE_LAUNCH(F, D)                                                              \
+  (token_scales ? launch_pdl(write_kernel<F, D, true>, gd, bd, 0, s, p)                     \
+                : launch_pdl(write_kernel<F, D, false>, gd, bd, 0, s, p))
+  if (head_dim == 128) {
+    switch (fmt) {
+      case KVQ_FMT_E4M3: e = KVQ_WRITE_LAUNCH(KVQ_FMT_E4M3, 128); break;
+      case KVQ_FMT_E5M2: e = KVQ_WRITE_LAUNCH(KVQ_FMT_E5M2, 128); break;
+      default: e = launch_pdl(write_kernel<KVQ_FMT_BF16, 128, false>, gd, bd, 0, s, p); break;
+    }
+  } else {
+    switch (fmt) {
+      case KVQ_FMT_E4M3: e = KVQ_WRITE_LAUNCH(KVQ_FMT_E4M3, 64); break;
+      case KVQ_FMT_E5M2: e = KVQ_WRITE_LAUNCH(KVQ_FMT_E5M2, 64); break;
+      default: e = launch_pdl(write_kernel<KVQ_FMT_BF16, 64, false>, gd, bd, 0, s, p); break;
+    }
+  }
+#undef KVQ_WRITE_LAUNCH
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 }  // namespace kvq
 
 using namespace kvq;
@@ -238,62 +335,37 @@ extern "C" int kvq_write(const void* k, const void* v, int64_t token_stride,
   if (fmt < KVQ_FMT_BF16 || fmt > KVQ_FMT_E5M2) return KVQ_ERR_ARG;
   if (scale_granularity != KVQ_SCALE_PER_TENSOR && scale_granularity != KVQ_SCALE_PER_HEAD)
     return KVQ_ERR_ARG;
-  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return KVQ_ERR_ARG;
-  if (!k_cache || !v_cache) return KVQ_ERR_NULL;
-  if (num_tokens > 0 && (!k || !v || !slot_mapping)) return KVQ_ERR_NULL;
-  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
-  if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
-  if (token_stride < static_cast<int64_t>(num_kv_heads) * head_dim) return KVQ_ERR_SHAPE;
-  if (token_stride % 8 != 0) return KVQ_ERR_ALIGN;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
-    return KVQ_ERR_ALIGN;
-  if (fmt != KVQ_FMT_BF16) {
+  if (fmt != KVQ_FMT_BF16 && num_kv_heads > 0) {
     if (!k_scale || !v_scale) return KVQ_ERR_NULL;
     const int want = scale_granularity == KVQ_SCALE_PER_HEAD ? num_kv_heads : 1;
     if (k_scale_len != want || v_scale_len != want) return KVQ_ERR_SHAPE;
   }
-  if (num_blocks > (INT64_MAX / 16) / (static_cast<int64_t>(num_kv_heads) * head_dim))
-    return KVQ_ERR_SHAPE;
-  if (num_tokens == 0) return KVQ_OK;
-
-  WriteParams p;
-  p.k = static_cast<const uint16_t*>(k);
-  p.v = static_cast<const uint16_t*>(v);
-  p.token_stride = token_stride;
-  p.slots = slot_mapping;
-  p.num_tokens = num_tokens;
-  p.hkv = num_kv_heads;
-  p.dh = head_dim;
-  p.kc = k_cache;
-  p.vc = v_cache;
-  p.capacity = num_blocks * block_size;
+  WriteParams p = {};
   p.ks = k_scale;
   p.vs = v_scale;
   p.per_head = scale_granularity == KVQ_SCALE_PER_HEAD;
-  p.status = dev_status;
-  p.in_elems = (num_tokens - 1) * token_stride + static_cast<int64_t>(num_kv_heads) * head_dim;
-  p.cache_elems = num_blocks * num_kv_heads * block_size * head_dim;
-  int grid = 0, block = 0;
-  token_row_shape(num_tokens, num_kv_heads * (head_dim / 16), 3, grid, block);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  const dim3 gd(grid), bd(block);
-  if (head_dim == 128) {
-    switch (fmt) {
-      case KVQ_FMT_E4M3: e = launch_pdl(write_kernel<KVQ_FMT_E4M3, 128>, gd, bd, 0, s, p); break;
-      case KVQ_FMT_E5M2: e = launch_pdl(write_kernel<KVQ_FMT_E5M2, 128>, gd, bd, 0, s, p); break;
-      default: e = launch_pdl(write_kernel<KVQ_FMT_BF16, 128>, gd, bd, 0, s, p); break;
-    }
-  } else {
-    switch (fmt) {
-      case KVQ_FMT_E4M3: e = launch_pdl(write_kernel<KVQ_FMT_E4M3, 64>, gd, bd, 0, s, p); break;
-      case KVQ_FMT_E5M2: e = launch_pdl(write_kernel<KVQ_FMT_E5M2, 64>, gd, bd, 0, s, p); break;
-      default: e = launch_pdl(write_kernel<KVQ_FMT_BF16, 64>, gd, bd, 0, s, p); break;
-    }
-  }
-  if (e != cudaSuccess) return KVQ_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  return write_common(k, v, token_stride, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                      k_cache, v_cache, num_blocks, block_size, fmt, p, false, dev_status,
+                      stream);
+}
+
+extern "C" int kvq_write_token_head(const void* k, const void* v, int64_t token_stride,
+                                    const int64_t* slot_mapping, int64_t num_tokens,
+                                    int num_kv_heads, int head_dim, void* k_cache, void* v_cache,
+                                    int64_t num_blocks, int block_size, float* k_scale_cache,
+                                    float* v_scale_cache, int fmt, uint32_t* dev_status,
+                                    kvq_stream_t stream) {
+  if (fmt < KVQ_FMT_BF16 || fmt > KVQ_FMT_E5M2) return KVQ_ERR_ARG;
+  if (fmt == KVQ_FMT_BF16) return KVQ_ERR_UNSUPPORTED;
+  if (!k_scale_cache || !v_scale_cache) return KVQ_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(k_scale_cache) & 15u) ||
+      (reinterpret_cast<uintptr_t>(v_scale_cache) & 15u))
+    return KVQ_ERR_ALIGN;
+  WriteParams p = {};
+  p.ksc = k_scale_cache;
+  p.vsc = v_scale_cache;
+  return write_common(k, v, token_stride, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                      k_cache, v_cache, num_blocks, block_size, fmt, p, true, dev_status, stream);
 }
 
 extern "C" int kvq_dequant_cache(const void* src, void* dst_bf16, int64_t num_blocks,
@@ -301,14 +373,17 @@ extern "C" int kvq_dequant_cache(const void* src, void* dst_bf16, int64_t num_bl
                                  const float* scale, int scale_len, int scale_granularity,
                                  int fmt, kvq_stream_t stream) {
   if (fmt != KVQ_FMT_E4M3 && fmt != KVQ_FMT_E5M2) return KVQ_ERR_UNSUPPORTED;
-  if (scale_granularity != KVQ_SCALE_PER_TENSOR && scale_granularity != KVQ_SCALE_PER_HEAD)
+  if (scale_granularity != KVQ_SCALE_PER_TENSOR && scale_granularity != KVQ_SCALE_PER_HEAD &&
+      scale_granularity != KVQ_SCALE_PER_TOKEN_HEAD)
     return KVQ_ERR_ARG;
   if (num_blocks < 0 || num_kv_heads <= 0) return KVQ_ERR_ARG;
   if (!src || !dst_bf16 || !scale) return KVQ_ERR_NULL;
   if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
   if (block_size != 16) return KVQ_ERR_UNSUPPORTED;
   if (!aligned16(src) || !aligned16(dst_bf16)) return KVQ_ERR_ALIGN;
-  const int want = scale_granularity == KVQ_SCALE_PER_HEAD ? num_kv_heads : 1;
+  const int64_t want = scale_granularity == KVQ_SCALE_PER_TOKEN_HEAD
+                           ? num_blocks * num_kv_heads * block_size
+                           : (scale_granularity == KVQ_SCALE_PER_HEAD ? num_kv_heads : 1);
   if (scale_len != want) return KVQ_ERR_SHAPE;
   if (num_blocks == 0) return KVQ_OK;
   DequantParams p;
@@ -318,7 +393,7 @@ extern "C" int kvq_dequant_cache(const void* src, void* dst_bf16, int64_t num_bl
   p.units = num_blocks * num_kv_heads * p.chunks_per_head;
   p.hkv = num_kv_heads;
   p.scale = scale;
-  p.per_head = scale_granularity == KVQ_SCALE_PER_HEAD;
+  p.gran = scale_granularity;
   const int grid = grid_for(p.units, 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e =

@@ -72,9 +72,16 @@ typedef enum {
   KVQ_FMT_E5M2 = 2  /* FP8 E5M2 (OCP, max 57344)                            */
 } kvq_fmt;
 
-/* Scale granularity: per tensor (shape [1]) or per attention head
- * (k/v scale shape [num_kv_heads], q scale shape [num_q_heads]). */
-typedef enum { KVQ_SCALE_PER_TENSOR = 0, KVQ_SCALE_PER_HEAD = 1 } kvq_gran;
+/* Scale granularity: per tensor (shape [1]), per attention head (k/v scale
+ * shape [num_kv_heads], q scale shape [num_q_heads]), or per (token, KV head)
+ * ("10.4 KV Cache quantization", section 10.4.3, per-token granularity):
+ * k/v scale caches [num_blocks][num_kv_heads][block_size] fp32 beside the
+ * pages, written by kvq_write_token_head. */
+typedef enum {
+  KVQ_SCALE_PER_TENSOR = 0,
+  KVQ_SCALE_PER_HEAD = 1,
+  KVQ_SCALE_PER_TOKEN_HEAD = 2
+} kvq_gran;
 
 typedef enum {
   KVQ_OK = 0,
@@ -135,6 +142,35 @@ KVQ_API int kvq_write(const void* k, const void* v, int64_t token_stride, const 
               uint32_t* dev_status, kvq_stream_t stream);
 
 /*
+ * kvq_write_token_head -- quantize and scatter with per-(token, KV head)
+ * scales ("10.4 KV Cache quantization", section 10.4.3: one scale per token
+ * along dh, so every new token is quantized on its own and appended; vLLM's
+ * fp8_per_token_head).  Each written row k[t][h][:] gets
+ *   s = amax / fmt_max   (amax = largest magnitude among the row's finite
+ *                         values, NaN and +-inf ignored; binary32 division;
+ *                         fmt_max = 448 for E4M3, 57344 for E5M2),
+ * s = 1 where that quotient is 0, stored at
+ *   k_scale_cache[slot / bs][h][slot % bs],
+ * and its codes are cast_fp8(float(x) / s) exactly as kvq_write forms them
+ * (V likewise).  The row's largest finite value thus lands on the format's
+ * largest code.  kvq_decode_attn and kvq_dequant_cache read the scale caches
+ * with scale_granularity KVQ_SCALE_PER_TOKEN_HEAD.
+ *
+ *   k, v, slot_mapping, caches   as for kvq_write.
+ *   k_scale_cache, v_scale_cache fp32 [num_blocks][num_kv_heads][block_size],
+ *                   16-byte aligned; only the written rows' entries change.
+ *   fmt             KVQ_FMT_E4M3 or KVQ_FMT_E5M2 (BF16: KVQ_ERR_UNSUPPORTED).
+ * Cache metadata: 4 bytes per row beside dh code bytes (264 bytes per
+ * (token, KV head) at dh = 128 for K and V together, against 512 in bf16).
+ */
+KVQ_API int kvq_write_token_head(const void* k, const void* v, int64_t token_stride,
+                                 const int64_t* slot_mapping, int64_t num_tokens,
+                                 int num_kv_heads, int head_dim, void* k_cache, void* v_cache,
+                                 int64_t num_blocks, int block_size, float* k_scale_cache,
+                                 float* v_scale_cache, int fmt, uint32_t* dev_status,
+                                 kvq_stream_t stream);
+
+/*
  * kvq_calibrate_scales -- per-tensor or per-KV-head scales from the data
  * ("vLLM FP8 quantized KV cache guide", scale calibration, way two: scales
  * estimated from statistics of the K/V activations).  The statistic is the
@@ -185,9 +221,15 @@ KVQ_API size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_
  *                   ceil(L_b / block_size) are never read.
  *   seq_lens        int32 [num_seqs]; 0 gives a zero output row.
  *   q_scale         fp32, q_scale_len 1 (KVQ_SCALE_PER_TENSOR) or
- *                   num_q_heads (KVQ_SCALE_PER_HEAD).  Used only with
+ *                   num_q_heads (KVQ_SCALE_PER_HEAD); 1 or num_q_heads
+ *                   with KVQ_SCALE_PER_TOKEN_HEAD.  Used only with
  *                   KVQ_Q_FP8; otherwise optional and only shape-checked.
- *   k_scale,v_scale as for kvq_write (ignored and may be NULL for BF16).
+ *   k_scale,v_scale as for kvq_write (ignored and may be NULL for BF16);
+ *                   with KVQ_SCALE_PER_TOKEN_HEAD the scale caches of
+ *                   kvq_write_token_head (k/v_scale_len = num_blocks *
+ *                   num_kv_heads * block_size, 16-byte aligned): token t of
+ *                   head g uses the scale stored beside its row, the logit
+ *                   x_t = q . K_codes_t * sK_t / sqrt(dh) and V^_t = V_t sV_t.
  *   sliding_window  0 = none.
  *   flags           KVQ_Q_FP8: the FP8-domain mode ("vLLM FP8 quantized KV
  *                   cache guide", FlashAttention 3 note: the query is
@@ -204,8 +246,9 @@ KVQ_API size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_
  *                   stream.  Without the flag it waits for that kernel to
  *                   complete before reading anything.  With KVQ_CACHE_READY
  *                   it reads block_tables, seq_lens, k_scale, v_scale and
- *                   every cache page except the one holding each sequence's
- *                   last token (L_b - 1) while that kernel may still run,
+ *                   every cache page (with its per-token scales) except the
+ *                   one holding each sequence's last token (L_b - 1) while
+ *                   that kernel may still run,
  *                   and waits only before reading q or those last pages and
  *                   before writing anything: the caller promises that the
  *                   preceding kernel writes none of the early inputs (true
@@ -288,7 +331,10 @@ KVQ_API int kvq_decode_attn_static(const void* q, const void* k_cache, const voi
  * [num_blocks][num_kv_heads][block_size][head_dim]; the product is rounded to
  * binary32 (exact whenever s_h is a power of two), then to bf16 (nearest
  * even).  kvq_decode_attn with fmt KVQ_FMT_BF16 then reads the result.
- * fmt must be E4M3 or E5M2; scale as for kvq_write.
+ * fmt must be E4M3 or E5M2; scale as for kvq_write, or with
+ * KVQ_SCALE_PER_TOKEN_HEAD the scale cache of kvq_write_token_head
+ * (scale_len = num_blocks * num_kv_heads * block_size; row r of the cache
+ * uses scale[r]).
  */
 KVQ_API int kvq_dequant_cache(const void* src, void* dst_bf16, int64_t num_blocks, int num_kv_heads,
                       int block_size, int head_dim, const float* scale, int scale_len,

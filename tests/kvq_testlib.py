@@ -47,7 +47,7 @@ def check_attention(got, ref, what=""):
 class DeviceLayer:
     """One workload layer resident on the GPU, with its paged caches."""
 
-    def __init__(self, lay: workloads.Layer, dev="cuda", fill=0):
+    def __init__(self, lay: workloads.Layer, dev="cuda", fill=0, token_head=False):
         import fp8_quantized_paged_gb300 as kvq
         self.kvq = kvq
         self.lay = lay
@@ -66,6 +66,14 @@ class DeviceLayer:
         self.vc = kvq.new_cache(st.num_blocks, lay.Hkv, lay.dh, lay.fmt, dev)
         self.kc.view(torch.uint8).fill_(fill)
         self.vc.view(torch.uint8).fill_(fill)
+        # per-(token, head) scales: caches beside the pages, NaN bytes until written
+        self.token_head = token_head
+        self.ksc = self.vsc = None
+        if token_head:
+            self.ksc = kvq.new_scale_cache(st.num_blocks, lay.Hkv, dev)
+            self.vsc = kvq.new_scale_cache(st.num_blocks, lay.Hkv, dev)
+            self.ksc.view(torch.int32).fill_(-1)
+            self.vsc.view(torch.int32).fill_(-1)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.ws = kvq.new_workspace(lay.B, lay.Hq, lay.Hkv, lay.dh, dev)
         self.poison_workspace()
@@ -84,15 +92,21 @@ class DeviceLayer:
         else:
             idx = torch.as_tensor(np.asarray(token_idx, np.int64), device=self.dev)
             k, v, s = self.k[idx], self.v[idx], self.slots[idx]
+        if self.token_head:
+            self.kvq.kvq_write_token_head(k, v, s, self.kc, self.vc, self.ksc, self.vsc, lay.fmt,
+                                          dev_status=self.status)
+            return
         self.kvq.kvq_write(k, v, s, self.kc, self.vc, self.ks, self.vs, lay.gran, lay.fmt,
                            dev_status=self.status)
 
     def decode(self, window=None, seq_lens=None, block_tables=None, flags=0):
         lay = self.lay
+        th = self.token_head
         self.kvq.kvq_decode_attn(self.q, self.kc, self.vc,
                                  self.bt if block_tables is None else block_tables,
-                                 self.sl if seq_lens is None else seq_lens, self.qs, self.ks,
-                                 self.vs, lay.gran, lay.fmt,
+                                 self.sl if seq_lens is None else seq_lens, self.qs,
+                                 self.ksc if th else self.ks, self.vsc if th else self.vs,
+                                 self.kvq.KVQ_SCALE_PER_TOKEN_HEAD if th else lay.gran, lay.fmt,
                                  lay.window if window is None else window, self.ws, self.out,
                                  dev_status=self.status, flags=flags)
         return self.out
@@ -102,7 +116,9 @@ class DeviceLayer:
         return int(self.status.item())
 
 
-def oracle_caches(lay: workloads.Layer, token_idx=None, fill=0):
+def oracle_caches(lay: workloads.Layer, token_idx=None, fill=0, token_head=False):
+    """The oracle's caches; with token_head also its scale caches (NaN where
+    unwritten, like the device ones): returns K, V or K, V, sK, sV."""
     st = lay.st
     K = oracle.new_cache(st.num_blocks, lay.Hkv, lay.bs, lay.dh, lay.fmt, fill)
     V = oracle.new_cache(st.num_blocks, lay.Hkv, lay.bs, lay.dh, lay.fmt, fill)
@@ -110,16 +126,26 @@ def oracle_caches(lay: workloads.Layer, token_idx=None, fill=0):
         k, v, s = lay.k, lay.v, st.slot_mapping
     else:
         k, v, s = lay.k[token_idx], lay.v[token_idx], st.slot_mapping[token_idx]
+    if token_head:
+        nan = np.frombuffer(np.uint32(0xFFFFFFFF).tobytes(), np.float32)[0]
+        sK = oracle.new_scale_cache(st.num_blocks, lay.Hkv, lay.bs, nan)
+        sV = oracle.new_scale_cache(st.num_blocks, lay.Hkv, lay.bs, nan)
+        assert oracle.write(k, v, s, K, V, sK, sV, oracle.PER_TOKEN_HEAD, lay.fmt) == 0
+        return K, V, sK, sV
     bad = oracle.write(k, v, s, K, V, lay.k_scale, lay.v_scale, lay.gran, lay.fmt)
     assert bad == 0
     return K, V
 
 
 def oracle_decode(lay, K, V, pairs=None, window=None, seq_lens=None, block_tables=None,
-                  q_fp8=False):
+                  q_fp8=False, scale_caches=None):
+    """Oracle attention; scale_caches = (sK, sV) selects per-(token, head) scales."""
     st = lay.st
+    ks, vs, gran = lay.k_scale, lay.v_scale, lay.gran
+    if scale_caches is not None:
+        ks, vs, gran = scale_caches[0], scale_caches[1], oracle.PER_TOKEN_HEAD
     return oracle.decode_attn(lay.q, K, V, st.block_tables if block_tables is None else block_tables,
-                              st.seq_lens if seq_lens is None else seq_lens, lay.k_scale,
-                              lay.v_scale, lay.gran, lay.fmt,
+                              st.seq_lens if seq_lens is None else seq_lens, ks, vs, gran,
+                              lay.fmt,
                               lay.window if window is None else window, pairs=pairs,
                               q_scale=lay.q_scale if q_fp8 else None)

@@ -28,7 +28,8 @@ def test_exports_every_declared_symbol(kvq):
     declared = header_functions()
     assert declared == {"kvq_write", "kvq_decode_workspace_size", "kvq_decode_attn",
                         "kvq_decode_attn_static", "kvq_dequant_cache", "kvq_parse_dtype",
-                        "kvq_layer_fmt", "kvq_status_string", "kvq_version", "kvq_calibrate_scales"}
+                        "kvq_layer_fmt", "kvq_status_string", "kvq_version", "kvq_calibrate_scales",
+                        "kvq_write_token_head"}
     raw = ctypes.CDLL(kvq.LIB_PATH)
     for name in declared:
         assert getattr(raw, name) is not None
@@ -122,6 +123,31 @@ def test_write_validation(kvq):
     assert _write(kvq, n=0, fmt=0, ks=None, vs=None, ksl=0, vsl=0) == kvq.KVQ_OK
 
 
+def _write_th(kvq, **kw):
+    args = dict(k=A, v=A, token_stride=1024, slots=A, n=4, hkv=8, dh=128, kc=A, vc=A, nb=10,
+                bs=16, ksc=A, vsc=A, fmt=1, status=None)
+    args.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return kvq.lib().kvq_write_token_head(
+        p(args["k"]), p(args["v"]), args["token_stride"], p(args["slots"]), args["n"],
+        args["hkv"], args["dh"], p(args["kc"]), p(args["vc"]), args["nb"], args["bs"],
+        p(args["ksc"]), p(args["vsc"]), args["fmt"], p(args["status"]), None)
+
+
+def test_write_token_head_validation(kvq):
+    assert _write_th(kvq, ksc=None) == kvq.KVQ_ERR_NULL
+    assert _write_th(kvq, vsc=None) == kvq.KVQ_ERR_NULL
+    assert _write_th(kvq, fmt=0) == kvq.KVQ_ERR_UNSUPPORTED  # bf16 has no scales
+    assert _write_th(kvq, fmt=5) == kvq.KVQ_ERR_ARG
+    assert _write_th(kvq, ksc=A + 4) == kvq.KVQ_ERR_ALIGN
+    assert _write_th(kvq, kc=None) == kvq.KVQ_ERR_NULL
+    assert _write_th(kvq, n=-1) == kvq.KVQ_ERR_ARG
+    assert _write_th(kvq, dh=96) == kvq.KVQ_ERR_UNSUPPORTED
+    assert _write_th(kvq, token_stride=512) == kvq.KVQ_ERR_SHAPE
+    assert _write_th(kvq, k=A + 2) == kvq.KVQ_ERR_ALIGN
+    assert _write_th(kvq, n=0) == kvq.KVQ_OK
+
+
 def _decode(kvq, **kw):
     args = dict(q=A, kc=A, vc=A, bt=A, maxb=4, sl=A, B=2, hq=32, hkv=8, dh=128, nb=8, bs=16,
                 qs=None, qsl=0, ks=A, ksl=1, vs=A, vsl=1, gran=0, fmt=1, win=0, flags=0, ws=A,
@@ -157,6 +183,13 @@ def test_decode_validation(kvq):
     assert _decode(kvq, gran=1) == kvq.KVQ_ERR_SHAPE            # k/v scale must be [Hkv]
     assert _decode(kvq, gran=1, ksl=8, vsl=8, qs=A, qsl=8) == kvq.KVQ_ERR_SHAPE  # q scale [Hq]
     assert _decode(kvq, qs=A, qsl=32) == kvq.KVQ_ERR_SHAPE      # per tensor q scale is [1]
+    # per-(token, head) scales: the scale caches [num_blocks][Hkv][16]
+    th = dict(gran=2, ksl=8 * 8 * 16, vsl=8 * 8 * 16)
+    assert _decode(kvq, gran=3) == kvq.KVQ_ERR_ARG
+    assert _decode(kvq, gran=2) == kvq.KVQ_ERR_SHAPE
+    assert _decode(kvq, **dict(th, vsl=8)) == kvq.KVQ_ERR_SHAPE
+    assert _decode(kvq, **dict(th, ks=A + 4)) == kvq.KVQ_ERR_ALIGN
+    assert _decode(kvq, **dict(th, qs=A, qsl=8)) == kvq.KVQ_ERR_SHAPE  # q scale: [1] or [Hq]
 
 
 def test_python_constants_mirror_the_header():

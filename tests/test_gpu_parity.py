@@ -562,3 +562,131 @@ def test_decode_q_fp8_rejected_without_fp8_cache_or_scale(kvq):
     d8.qs = None
     with pytest.raises(RuntimeError):
         d8.decode(flags=kvq.KVQ_Q_FP8)
+
+
+# ---------------------------------------------------------------- per-(token, KV head) scales
+
+def _f32_bits(a):
+    return np.ascontiguousarray(a, np.float32).view(np.uint32)
+
+
+def _check_token_head_caches(d, K, V, sK, sV):
+    np.testing.assert_array_equal(to_np(d.kc), K)
+    np.testing.assert_array_equal(to_np(d.vc), V)
+    np.testing.assert_array_equal(_f32_bits(to_np(d.ksc)), _f32_bits(sK))
+    np.testing.assert_array_equal(_f32_bits(to_np(d.vsc)), _f32_bits(sV))
+
+
+@pytest.mark.parametrize("cfg,layer,fmt3", [(1, 0, workloads.E4M3), (2, 0, workloads.E4M3),
+                                           (3, 0, workloads.E4M3), (3, 0, workloads.E5M2),
+                                           (5, 2, workloads.E4M3)],
+                         ids=["tiny", "llama8b_layer", "perhead_e4m3", "perhead_e5m2",
+                              "mixed_fp8_layer2"])
+def test_token_head_write_and_decode(kvq, cfg, layer, fmt3):
+    """Each row's scale from its own amax, stored beside the page; the decode
+    reads the row scales: caches and scales bit-exact, attention within
+    tolerance, in both query modes."""
+    lay = workloads.make_layer(cfg, layer, fmt3)
+    d = DeviceLayer(lay, token_head=True)
+    if cfg == 2:
+        new = np.flatnonzero(lay.new_token_mask)
+        d.write(np.flatnonzero(~lay.new_token_mask))
+        d.write(new)
+    else:
+        d.write()
+    out = bf16_out_to_f64(d.decode())
+    assert d.status_word() == 0
+    K, V, sK, sV = oracle_caches(lay, token_head=True)
+    _check_token_head_caches(d, K, V, sK, sV)
+    pairs = _pairs_for(lay)
+    ref = oracle_decode(lay, K, V, pairs=pairs, scale_caches=(sK, sV))
+    got = out if pairs is None else out[pairs[:, 0], pairs[:, 1]]
+    check_attention(got, ref, f"token-head config {cfg}")
+    qf = bf16_out_to_f64(d.decode(flags=kvq.KVQ_Q_FP8))
+    assert d.status_word() == 0
+    ref8 = oracle_decode(lay, K, V, pairs=pairs, scale_caches=(sK, sV), q_fp8=True)
+    check_attention(qf if pairs is None else qf[pairs[:, 0], pairs[:, 1]], ref8,
+                    f"token-head q fp8 config {cfg}")
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2])
+def test_token_head_special_rows(kvq, fmt):
+    """Rows of zeros, NaN / inf among finite values, subnormal-only rows, rows
+    at the bf16 range's top (scales outside the fast division's range) and
+    rows whose magnitudes span the whole format."""
+    lay = _custom_layer([40, 17], Hq=4, Hkv=2, dh=128, fmt=fmt, seed=130)
+    k = lay.k.copy()
+    one = lambda x: workloads.f32_to_bf16_bits(np.asarray(x, np.float32))  # noqa: E731
+    k[0] = 0                                        # zero rows -> scale 1
+    k[1, 0, :3] = one([np.nan, np.inf, -np.inf])    # specials ignored by amax
+    k[2, 1, :] = np.arange(1, 129, dtype=np.uint16)  # bf16 subnormals only
+    k[3, 0, :] = one(np.linspace(-3e38, 3e38, 128))  # huge: s > 2^80
+    k[4, 1, :] = one(np.geomspace(1e-30, 1e30, 128))
+    k[5, :, :] = 0x8000                              # -0 everywhere
+    lay = dataclasses.replace(lay, k=k)
+    d = DeviceLayer(lay, token_head=True)
+    d.write()
+    assert d.status_word() == 0
+    K, V, sK, sV = oracle_caches(lay, token_head=True)
+    nan_k = np.isnan(oracle.decode(fmt, K))
+    np.testing.assert_array_equal(np.isnan(oracle.decode(fmt, to_np(d.kc))), nan_k)
+    np.testing.assert_array_equal(np.where(nan_k, 0, to_np(d.kc)), np.where(nan_k, 0, K))
+    np.testing.assert_array_equal(to_np(d.vc), V)
+    np.testing.assert_array_equal(_f32_bits(to_np(d.ksc)), _f32_bits(sK))
+    np.testing.assert_array_equal(_f32_bits(to_np(d.vsc)), _f32_bits(sV))
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2])
+@pytest.mark.parametrize("G,dh", [(1, 64), (2, 128), (4, 64), (8, 128)])
+def test_token_head_shapes(kvq, fmt, G, dh):
+    """Ragged lengths (an empty sequence, partial last pages whose unwritten
+    rows hold NaN scales), widely varying row magnitudes."""
+    lay = _custom_layer([1, 15, 0, 250, 33, 1000], Hq=2 * G, Hkv=2, dh=dh, fmt=fmt,
+                        seed=140 + G + dh)
+    r = np.random.default_rng(141 + G)
+    mag = 10.0 ** r.uniform(-3, 3, (lay.k.shape[0], 2, 1))
+    kf = (lay.k.astype(np.uint32) << 16).view(np.float32) * mag
+    vf = (lay.v.astype(np.uint32) << 16).view(np.float32) / mag
+    lay = dataclasses.replace(lay, k=workloads.f32_to_bf16_bits(kf.astype(np.float32)),
+                              v=workloads.f32_to_bf16_bits(vf.astype(np.float32)))
+    d = DeviceLayer(lay, token_head=True)
+    d.write()
+    got = bf16_out_to_f64(d.decode())
+    assert d.status_word() == 0
+    K, V, sK, sV = oracle_caches(lay, token_head=True)
+    _check_token_head_caches(d, K, V, sK, sV)
+    check_attention(got, oracle_decode(lay, K, V, scale_caches=(sK, sV)), f"token-head G={G}")
+    assert np.all(got[2] == 0)
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,dh,fmt,window", [
+    ([20000, 3], 32, 8, 128, workloads.E4M3, 0),
+    ([3000] * 4, 32, 8, 128, workloads.E5M2, 0),
+    ([7000, 40], 16, 4, 64, workloads.E4M3, 1000),
+])
+def test_token_head_split_segments_and_cache_ready(kvq, lens, Hq, Hkv, dh, fmt, window):
+    lay = _custom_layer(lens, Hq=Hq, Hkv=Hkv, dh=dh, fmt=fmt, seed=150 + dh, window=window)
+    d = DeviceLayer(lay, token_head=True)
+    d.write()
+    K, V, sK, sV = oracle_caches(lay, token_head=True)
+    ref = oracle_decode(lay, K, V, scale_caches=(sK, sV))
+    for flags in (0, kvq.KVQ_CACHE_READY):
+        got = bf16_out_to_f64(d.decode(flags=flags))
+        assert d.status_word() == 0
+        check_attention(got, ref, f"token-head lens={lens} flags={flags}")
+        d.poison_workspace()
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2])
+def test_token_head_dequant_then_bf16_decode(kvq, fmt):
+    lay = _custom_layer([300, 77], Hq=8, Hkv=2, dh=128, fmt=fmt, seed=160)
+    d = DeviceLayer(lay, token_head=True)
+    d.write()
+    K, V, sK, sV = oracle_caches(lay, token_head=True)
+    kb = torch.empty(d.kc.shape, dtype=torch.bfloat16, device="cuda")
+    kvq.kvq_dequant_cache(d.kc, kb, d.ksc, kvq.KVQ_SCALE_PER_TOKEN_HEAD, fmt)
+    torch.cuda.synchronize()
+    # rows nobody wrote hold NaN scales: compare the written rows
+    want = oracle.dequant(K, sK, oracle.PER_TOKEN_HEAD, fmt)
+    written = ~np.isnan(sK)
+    np.testing.assert_array_equal(to_np(kb)[written], want[written])
