@@ -73,6 +73,17 @@ def decode_bytes_token_head(n_tokens: int) -> int:
     return decode_bytes(n_tokens) - 2 * HKV * 4 + pages * HKV * 2 * BS * 4
 
 
+PREFILL_Q = 2048  # prefix-hit prefill: the last 2048 tokens of the 32768 are queries
+
+
+def prefill_flops(n_q: int, seq: int) -> int:
+    """QK^T and PV multiply-adds of the causal prefill of the last n_q of seq
+    tokens: query j attends to seq - n_q + j + 1 tokens, 4 dh flops each per
+    query head."""
+    keys = n_q * (seq - n_q) + n_q * (n_q + 1) // 2
+    return keys * HQ * DH * 4
+
+
 STEP_WRITE_BYTES = LAYERS * write_bytes(SEQ)
 STEP_DECODE_BYTES = LAYERS * decode_bytes(SEQ)
 STEP_BYTES = STEP_WRITE_BYTES + STEP_DECODE_BYTES
@@ -85,6 +96,15 @@ WORKLOAD = {
     "head_dim": DH, "block_size": BS, "kv_cache_dtype": "fp8_e4m3", "scales": "per-head amax/448",
     "l2": "inputs larger than L2 (about 6.3 GB moved per step)",
 }
+
+
+def measured_tflops() -> float:
+    """Dense bf16 tensor peak measured on this GPU model (burst), TFLOP/s."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
 
 
 def measured_peaks():
@@ -287,6 +307,21 @@ def run_gpu(args, rank, world, local_rank):
     g_calib = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_calib):
         calibrations()
+    # Prefix-hit prefill on layer 0's cache: the last PREFILL_Q tokens are
+    # queries over the 32768 cached ones (4 calls per graph replay).
+    pf_q = torch.randn((PREFILL_Q, HQ, DH), device=dev).to(torch.bfloat16)
+    pf_out = torch.empty_like(pf_q)
+    pf_cu = torch.tensor([0, PREFILL_Q], dtype=torch.int32, device=dev)
+
+    def prefills():
+        for _ in range(4):
+            kvq.kvq_prefill_attn(pf_q, pf_cu, PREFILL_Q, L[0]["kc"], L[0]["vc"], bt, sl,
+                                 L[0]["ks"], L[0]["vs"], PH, E4, 0, pf_out, dev_status=status)
+
+    prefills()
+    g_prefill = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_prefill):
+        prefills()
     # Per-(token, head) scales: every layer's write into the same caches with
     # its scale caches beside them, then the decodes reading them.  Timed
     # after the per-head graphs (it rewrites the caches).
@@ -347,6 +382,7 @@ def run_gpu(args, rank, world, local_rank):
         ready_total = timed_replays(g_decode_ready.replay, args.steps)
         qf8_total = timed_replays(g_decode_qf8.replay, args.steps)
         calib_total = timed_replays(g_calib.replay, args.steps)
+        prefill_total = timed_replays(g_prefill.replay, args.steps)
         g_write_th.replay()  # the caches now hold per-token-head codes
         g_decode_th.replay()
         write_th_total = timed_replays(g_write_th.replay, args.steps)
@@ -360,6 +396,7 @@ def run_gpu(args, rank, world, local_rank):
     qf8_ms = rank_max(qf8_total) / args.steps
     calib_ms = rank_max(calib_total) / args.steps
     write_th_us = rank_max(write_th_total) / args.steps * 1e3 / LAYERS
+    prefill_us = rank_max(prefill_total) / args.steps * 1e3 / 4
     decode_th_us = rank_max(decode_th_total) / args.steps * 1e3 / LAYERS
 
     # ---- end to end through the public API with host buffers
@@ -410,6 +447,13 @@ def run_gpu(args, rank, world, local_rank):
         "kv_calibrate": {"gbs": round(c_ach, 1), "frac_of_peak": round(c_ach / peak, 4),
                          "us_per_layer": round(calib_launch_us, 2),
                          "what": "per-head amax scales of one layer's 32768 bf16 K/V tokens"},
+        "prefill_attn": {
+            "tflops": round(prefill_flops(PREFILL_Q, SEQ) / (prefill_us * 1e-6) / 1e12, 1),
+            "us_per_call": round(prefill_us, 1),
+            "frac_of_bf16_peak": round(prefill_flops(PREFILL_Q, SEQ) / (prefill_us * 1e-6) / 1e12
+                                       / measured_tflops(), 4),
+            "what": "prefix-hit prefill of layer 0: last 2048 of 32768 tokens as causal queries "
+                    "(Hq=32, Hkv=8, dh=128, FP8 E4M3), mma.sync f16"},
         "kv_write_token_head": {
             "gbs": round(write_bytes_token_head(SEQ) / (write_th_us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(write_bytes_token_head(SEQ) / (write_th_us * 1e-6) / 1e9 / peak, 4),

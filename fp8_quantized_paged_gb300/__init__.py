@@ -41,6 +41,9 @@ SIGNATURES = {
     "kvq_decode_attn_static": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i64,
                                       _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                       _u32, _vp, _vp, _vp]),
+    "kvq_prefill_attn": (_i32, [_vp, _vp, _i64, _i32, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                _i32, _i64, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _vp,
+                                _vp, _vp]),
     "kvq_dequant_cache": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
     "kvq_calibrate_scales": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                     _vp]),
@@ -195,6 +198,26 @@ def kvq_decode_attn_static(q, k_cache, v_cache, block_tables, seq_lens, q_scale,
                                      scale_granularity, fmt, sliding_window, flags, _ptr(out),
                                      _ptr(dev_status), _stream(stream))
     _check(st, "kvq_decode_attn_static")
+
+
+def kvq_prefill_attn(q, cu_q_lens, max_q_len, k_cache, v_cache, block_tables, seq_lens,
+                     k_scale, v_scale, scale_granularity, fmt, sliding_window, out,
+                     dev_status=None, stream=None) -> None:
+    """Prefill / prefix-hit attention: q bf16 [total_q][Hq][dh], cu_q_lens int32
+    [B+1] (device), max_q_len a host bound of the per-sequence query counts;
+    the queries are each sequence's last tokens, attending causally."""
+    total_q, hq, dh = q.shape
+    nb, hkv, bs, dh2 = k_cache.shape
+    B = seq_lens.shape[0]
+    if dh2 != dh or tuple(out.shape) != (total_q, hq, dh) or cu_q_lens.shape[0] != B + 1 or \
+            block_tables.shape[0] != B:
+        raise KvqError(KVQ_ERR_SHAPE, "kvq_prefill_attn")
+    st = _lib.kvq_prefill_attn(_ptr(q), _ptr(cu_q_lens), total_q, int(max_q_len), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                               _ptr(seq_lens), B, hq, hkv, dh, nb, bs, _ptr(k_scale),
+                               _len(k_scale), _ptr(v_scale), _len(v_scale), scale_granularity,
+                               fmt, sliding_window, _ptr(out), _ptr(dev_status), _stream(stream))
+    _check(st, "kvq_prefill_attn")
 
 
 def kvq_dequant_cache(src, dst_bf16, scale, scale_granularity, fmt, stream=None) -> None:

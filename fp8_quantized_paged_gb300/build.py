@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
 SOURCES = ["kvq_host.cu", "kvq_write.cu", "kvq_decode.cu", "kvq_static.cu", "kvq_calib.cu",
-           "kvq_decode_variant.cu"]
+           "kvq_prefill.cu", "kvq_decode_variant.cu"]
 HEADERS = ["kvq_common.cuh", "kvq_host.h", "kvq_decode.cuh"]
 # (object, source, defines): one object per translation unit, the decode
 # variants once per (format, head size); kvq_fmt 0 = BF16, 1 = E4M3, 2 = E5M2

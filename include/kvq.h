@@ -324,6 +324,46 @@ KVQ_API int kvq_decode_attn_static(const void* q, const void* k_cache, const voi
                                    uint32_t* dev_status, kvq_stream_t stream);
 
 /*
+ * kvq_prefill_attn -- prefill, chunked-prefill and prefix-hit attention over
+ * the paged cache, dequantization fused ("10.4 KV Cache quantization",
+ * section 10.4.2: prefill, decode and prefix-hit paths all read the same
+ * compressed cache).  Sequence b holds L_b = seq_lens[b] tokens in the cache
+ * (write the chunk's K/V first, on the same stream); its last
+ * n_b = cu_q_lens[b+1] - cu_q_lens[b] tokens are the queries.  Query row
+ * cu_q_lens[b] + j is the token at position pos = L_b - n_b + j and attends
+ * to the tokens [lo, pos] of its sequence, lo = pos + 1 - sliding_window when
+ * 0 < sliding_window <= pos, else 0:
+ *   O = softmax(q K^T / sqrt(dh) over [lo, pos]) V^,  K^ = cast_float(K) sK.
+ * The tokens before the chunk are a cached prefix (a prefix hit, or the
+ * earlier chunks of a chunked prefill); n_b = 1 is the decode.
+ *
+ *   q               bf16 [num_q_tokens][num_q_heads][head_dim].
+ *   cu_q_lens       int32 [num_seqs + 1], device: 0 = cu_q_lens[0] <= ... <=
+ *                   cu_q_lens[num_seqs] = num_q_tokens.
+ *   max_q_len       host: an upper bound of every n_b (sets the grid; rows
+ *                   of a longer chunk would be left unwritten).
+ *   block_tables, seq_lens, caches, scales, fmt   as for kvq_decode_attn
+ *                   (KVQ_SCALE_PER_TENSOR or KVQ_SCALE_PER_HEAD).
+ *   out             bf16 [num_q_tokens][num_q_heads][head_dim].
+ *   dev_status      optional; KVQ_DEV_BAD_BLOCK (page masked out),
+ *                   KVQ_DEV_BAD_SEQLEN (L_b < n_b or L_b > max_blocks_per_seq
+ *                   * block_size: the sequence's rows are zero),
+ *                   KVQ_DEV_WAIT_TIMEOUT.
+ * Group size num_q_heads / num_kv_heads in {1, 2, 4, 8}; num_seqs <= 65535.
+ * No workspace: one CTA per (sequence, KV head, 64 query rows), so a short
+ * chunk over a long prefix keeps few SMs busy.
+ */
+KVQ_API int kvq_prefill_attn(const void* q, const int32_t* cu_q_lens, int64_t num_q_tokens,
+                             int max_q_len, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int head_dim, int64_t num_blocks,
+                             int block_size, const float* k_scale, int k_scale_len,
+                             const float* v_scale, int v_scale_len, int scale_granularity,
+                             int fmt, int sliding_window, void* out, uint32_t* dev_status,
+                             kvq_stream_t stream);
+
+/*
  * kvq_dequant_cache -- the unfused path's separate dequant kernel
  * ("10.4 KV Cache quantization", section 10.4.2: read the quantized KV,
  * dequantize in an independent kernel, write a 16-bit KV back to HBM).

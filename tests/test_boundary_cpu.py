@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol(kvq):
     assert declared == {"kvq_write", "kvq_decode_workspace_size", "kvq_decode_attn",
                         "kvq_decode_attn_static", "kvq_dequant_cache", "kvq_parse_dtype",
                         "kvq_layer_fmt", "kvq_status_string", "kvq_version", "kvq_calibrate_scales",
-                        "kvq_write_token_head"}
+                        "kvq_write_token_head", "kvq_prefill_attn"}
     raw = ctypes.CDLL(kvq.LIB_PATH)
     for name in declared:
         assert getattr(raw, name) is not None
@@ -146,6 +146,40 @@ def test_write_token_head_validation(kvq):
     assert _write_th(kvq, token_stride=512) == kvq.KVQ_ERR_SHAPE
     assert _write_th(kvq, k=A + 2) == kvq.KVQ_ERR_ALIGN
     assert _write_th(kvq, n=0) == kvq.KVQ_OK
+
+
+def _prefill(kvq, **kw):
+    args = dict(q=A, cu=A, nq=64, maxq=32, kc=A, vc=A, bt=A, maxb=4, sl=A, B=2, hq=32, hkv=8,
+                dh=128, nb=8, bs=16, ks=A, ksl=1, vs=A, vsl=1, gran=0, fmt=1, win=0, out=A)
+    args.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return kvq.lib().kvq_prefill_attn(
+        p(args["q"]), p(args["cu"]), args["nq"], args["maxq"], p(args["kc"]), p(args["vc"]),
+        p(args["bt"]), args["maxb"], p(args["sl"]), args["B"], args["hq"], args["hkv"], args["dh"],
+        args["nb"], args["bs"], p(args["ks"]), args["ksl"], p(args["vs"]), args["vsl"],
+        args["gran"], args["fmt"], args["win"], p(args["out"]), None, None)
+
+
+def test_prefill_validation(kvq):
+    assert _prefill(kvq, q=None) == kvq.KVQ_ERR_NULL
+    assert _prefill(kvq, cu=None) == kvq.KVQ_ERR_NULL
+    assert _prefill(kvq, fmt=3) == kvq.KVQ_ERR_ARG
+    assert _prefill(kvq, gran=2) == kvq.KVQ_ERR_ARG   # per-token scales: decode only
+    assert _prefill(kvq, B=0) == kvq.KVQ_ERR_ARG
+    assert _prefill(kvq, nq=-1) == kvq.KVQ_ERR_ARG
+    assert _prefill(kvq, win=-2) == kvq.KVQ_ERR_ARG
+    assert _prefill(kvq, dh=96) == kvq.KVQ_ERR_UNSUPPORTED
+    assert _prefill(kvq, bs=32) == kvq.KVQ_ERR_UNSUPPORTED
+    assert _prefill(kvq, hq=30) == kvq.KVQ_ERR_SHAPE
+    assert _prefill(kvq, hq=48) == kvq.KVQ_ERR_UNSUPPORTED  # group of 6
+    assert _prefill(kvq, hq=128) == kvq.KVQ_ERR_UNSUPPORTED  # group of 16
+    assert _prefill(kvq, out=A + 4) == kvq.KVQ_ERR_ALIGN
+    assert _prefill(kvq, cu=A + 2) == kvq.KVQ_ERR_ALIGN
+    assert _prefill(kvq, ks=None) == kvq.KVQ_ERR_NULL
+    assert _prefill(kvq, gran=1) == kvq.KVQ_ERR_SHAPE
+    assert _prefill(kvq, nq=0) == kvq.KVQ_OK
+    assert _prefill(kvq, maxq=0) == kvq.KVQ_OK
+    assert _prefill(kvq, fmt=0, ks=None, vs=None, nq=0) == kvq.KVQ_OK
 
 
 def _decode(kvq, **kw):

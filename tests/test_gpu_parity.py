@@ -690,3 +690,101 @@ def test_token_head_dequant_then_bf16_decode(kvq, fmt):
     want = oracle.dequant(K, sK, oracle.PER_TOKEN_HEAD, fmt)
     written = ~np.isnan(sK)
     np.testing.assert_array_equal(to_np(kb)[written], want[written])
+
+
+# ---------------------------------------------------------------- prefill / prefix-hit attention
+
+def _prefill_case(kvq, lay, nq, seed, window=None):
+    """Write the layer's tokens, then attend with the last nq[b] tokens of each
+    sequence as queries; returns (gpu float64 [total_q][Hq][dh], oracle inputs)."""
+    r = np.random.default_rng(seed)
+    cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = workloads.f32_to_bf16_bits(r.standard_normal((int(cu[-1]), lay.Hq, lay.dh)).astype(np.float32))
+    d = DeviceLayer(lay)
+    d.write()
+    out = torch.empty((int(cu[-1]), lay.Hq, lay.dh), dtype=torch.bfloat16, device="cuda")
+    out.fill_(float("nan"))
+    win = lay.window if window is None else window
+    kvq.kvq_prefill_attn(to_dev(q), to_dev(cu), int(max(nq)) if len(nq) else 0, d.kc, d.vc, d.bt,
+                         d.sl, d.ks, d.vs, lay.gran, lay.fmt, win, out, dev_status=d.status)
+    assert d.status_word() == 0
+    return bf16_out_to_f64(out), q, cu, win
+
+
+def _prefill_ref(lay, q, cu, win, pairs=None):
+    K, V = oracle_caches(lay)
+    st = lay.st
+    return oracle.prefill_attn(q, cu, K, V, st.block_tables, st.seq_lens, lay.k_scale,
+                               lay.v_scale, lay.gran, lay.fmt, window=win, pairs=pairs)
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2, workloads.BF16])
+@pytest.mark.parametrize("G,dh", [(1, 64), (2, 128), (4, 128), (8, 64)])
+def test_prefill_full_and_prefix_hit(kvq, fmt, G, dh):
+    """Whole-sequence prefills, prefix hits of a few tokens and a single
+    query (the decode) in one ragged batch."""
+    lens = [70, 33, 300, 16, 129]
+    nq = [70, 5, 37, 1, 0]
+    lay = _custom_layer(lens, Hq=2 * G, Hkv=2, dh=dh, fmt=fmt, seed=170 + G + dh)
+    got, q, cu, win = _prefill_case(kvq, lay, nq, seed=171)
+    check_attention(got, _prefill_ref(lay, q, cu, win), f"prefill G={G} dh={dh}")
+
+
+@pytest.mark.parametrize("window", [1, 16, 100, 1000])
+def test_prefill_sliding_window(kvq, window):
+    lay = _custom_layer([600, 40], Hq=8, Hkv=2, dh=128, seed=180)
+    got, q, cu, win = _prefill_case(kvq, lay, [150, 40], seed=181, window=window)
+    check_attention(got, _prefill_ref(lay, q, cu, win), f"prefill window={window}")
+    layb = _custom_layer([600, 40], Hq=8, Hkv=2, dh=128, fmt=workloads.BF16, seed=182)
+    got, q, cu, win = _prefill_case(kvq, layb, [100, 3], seed=183, window=window)
+    check_attention(got, _prefill_ref(layb, q, cu, win), f"bf16 prefill window={window}")
+
+
+def test_prefill_one_query_matches_decode(kvq):
+    lay = _custom_layer([300, 1, 45, 1000], Hq=32, Hkv=8, dh=128, seed=190)
+    got, q, cu, win = _prefill_case(kvq, lay, [1, 1, 1, 1], seed=191)
+    lay_q = dataclasses.replace(lay, q=q)
+    K, V = oracle_caches(lay)
+    check_attention(got, oracle_decode(lay_q, K, V), "prefill n=1 vs decode")
+
+
+@pytest.mark.parametrize("cfg,layer,fmt3,nq", [
+    (2, 0, workloads.E4M3, 64),    # Llama-3.1-8B-shaped layer: 64-token prefix hits
+    (3, 0, workloads.E5M2, 200),   # per-head scales, long prefixes
+    (5, 2, workloads.E4M3, 16),    # mixed batch FP8 layer
+    (5, 3, workloads.E4M3, 16),    # mixed batch bf16 layer with window 4096
+])
+def test_prefill_workloads(kvq, cfg, layer, fmt3, nq):
+    """The workloads' caches with each sequence's last nq tokens as queries
+    (all of them when shorter), on sampled (row, head) pairs."""
+    lay = workloads.make_layer(cfg, layer, fmt3)
+    lens = lay.st.seq_lens
+    n = np.minimum(lens, nq).astype(np.int64)
+    got, q, cu, win = _prefill_case(kvq, lay, list(n), seed=200 + cfg)
+    r = np.random.default_rng(201)
+    rows = r.integers(0, int(cu[-1]), 256)
+    heads = r.integers(0, lay.Hq, 256)
+    pairs = np.stack([rows, heads], 1).astype(np.int32)
+    ref = _prefill_ref(lay, q, cu, win, pairs=pairs)
+    check_attention(got[rows, heads], ref, f"prefill workload {cfg}")
+
+
+def test_prefill_bad_lengths_and_empty(kvq):
+    """A sequence with fewer cached tokens than queries gets zero rows and
+    the length flag; the others are unaffected."""
+    lay = _custom_layer([50, 40], Hq=4, Hkv=2, dh=64, seed=210)
+    r = np.random.default_rng(211)
+    cu = np.array([0, 10, 60], np.int32)  # sequence 1 asks for 50 queries of 40 tokens
+    q = workloads.f32_to_bf16_bits(r.standard_normal((60, 4, 64)).astype(np.float32))
+    d = DeviceLayer(lay)
+    d.write()
+    out = torch.full((60, 4, 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kvq.kvq_prefill_attn(to_dev(q), to_dev(cu), 50, d.kc, d.vc, d.bt, d.sl, d.ks, d.vs, lay.gran,
+                         lay.fmt, 0, out, dev_status=d.status)
+    assert d.status_word() & kvq.KVQ_DEV_BAD_SEQLEN
+    got = bf16_out_to_f64(out)
+    assert np.all(got[10:] == 0)
+    K, V = oracle_caches(lay)
+    ref = oracle.prefill_attn(q[:10], cu[:2], K, V, lay.st.block_tables[:1], lay.st.seq_lens[:1],
+                              lay.k_scale, lay.v_scale, lay.gran, lay.fmt)
+    check_attention(got[:10], ref, "prefill valid sequence")
