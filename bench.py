@@ -453,7 +453,7 @@ def run_gpu(args, rank, world, local_rank):
             "frac_of_bf16_peak": round(prefill_flops(PREFILL_Q, SEQ) / (prefill_us * 1e-6) / 1e12
                                        / measured_tflops(), 4),
             "what": "prefix-hit prefill of layer 0: last 2048 of 32768 tokens as causal queries "
-                    "(Hq=32, Hkv=8, dh=128, FP8 E4M3), mma.sync f16"},
+                    "(Hq=32, Hkv=8, dh=128, FP8 E4M3), tcgen05 f16 MMA, accumulators in TMEM"},
         "kv_write_token_head": {
             "gbs": round(write_bytes_token_head(SEQ) / (write_th_us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(write_bytes_token_head(SEQ) / (write_th_us * 1e-6) / 1e9 / peak, 4),
@@ -625,7 +625,10 @@ def run_ncu_case(case: str):
     before each captured launch): 'decode' and 'write' run one FP8 layer of
     the mixed skip-layer batch (128 sequences, about 0.9 GB of FP8 cache),
     'decode_long' and 'write_long' one layer of the long-context workload
-    (32768 tokens: 128 MiB of bf16 K/V in, 64 MiB of FP8 cache)."""
+    (32768 tokens: 128 MiB of bf16 K/V in, 64 MiB of FP8 cache); on that
+    layer 'write_th_long' / 'decode_th_long' use per-(token, head) scales,
+    'calib_long' calibrates per-head scales and 'prefill_long' runs a
+    prefix-hit prefill of the last 512 tokens."""
     import torch
 
     import fp8_quantized_paged_gb300 as kvq
@@ -647,11 +650,32 @@ def run_ncu_case(case: str):
     vc = kvq.new_cache(st.num_blocks, lay.Hkv, lay.dh, lay.fmt, dev)
     ws = kvq.new_workspace(lay.B, lay.Hq, lay.Hkv, lay.dh, dev)
     out = torch.empty((lay.B, lay.Hq, lay.dh), dtype=torch.bfloat16, device=dev)
+    token_head = "_th" in case
     n_write = 3 if case.startswith("write") else 1
-    for _ in range(n_write):
-        kvq.kvq_write(k, v, slots, kc, vc, ks, vs, lay.gran, lay.fmt)
+    if token_head:
+        ksc = kvq.new_scale_cache(st.num_blocks, lay.Hkv, dev)
+        vsc = kvq.new_scale_cache(st.num_blocks, lay.Hkv, dev)
+        for _ in range(n_write):
+            kvq.kvq_write_token_head(k, v, slots, kc, vc, ksc, vsc, lay.fmt)
+        ks, vs, gran = ksc, vsc, kvq.KVQ_SCALE_PER_TOKEN_HEAD
+    else:
+        gran = lay.gran
+        for _ in range(n_write):
+            kvq.kvq_write(k, v, slots, kc, vc, ks, vs, lay.gran, lay.fmt)
     for _ in range(3 if case.startswith("decode") else 0):
-        kvq.kvq_decode_attn(q, kc, vc, bt, sl, None, ks, vs, lay.gran, lay.fmt, lay.window, ws, out)
+        kvq.kvq_decode_attn(q, kc, vc, bt, sl, None, ks, vs, gran, lay.fmt, lay.window, ws, out)
+    if case == "calib_long":
+        cal_k = torch.empty(lay.Hkv, dtype=torch.float32, device=dev)
+        cal_v = torch.empty(lay.Hkv, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            kvq.kvq_calibrate_scales(k, v, cal_k, cal_v, kvq.KVQ_SCALE_PER_HEAD, lay.fmt)
+    if case == "prefill_long":
+        nq = 512
+        pq = torch.randn((nq, lay.Hq, lay.dh), device=dev).to(torch.bfloat16)
+        pout = torch.empty_like(pq)
+        cu = torch.tensor([0, nq], dtype=torch.int32, device=dev)
+        for _ in range(2):
+            kvq.kvq_prefill_attn(pq, cu, nq, kc, vc, bt, sl, ks, vs, lay.gran, lay.fmt, 0, pout)
     torch.cuda.synchronize()
     print(json.dumps({"ncu_case": case, "workload": cfg, "layer": layer,
                       "kv_tokens": int(st.seq_lens.sum()), "decode_bytes": int(st.seq_lens.sum()) * 2048}))
@@ -666,7 +690,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "write", "decode_long", "write_long"], default=None,
+    ap.add_argument("--ncu-case", choices=["decode", "write", "decode_long", "write_long",
+                                           "write_th_long", "decode_th_long", "calib_long",
+                                           "prefill_long"], default=None,
                     help="run a few launches of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.ncu_case:

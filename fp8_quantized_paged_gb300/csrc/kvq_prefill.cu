@@ -391,6 +391,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+}  // namespace kvq
+
+#include "kvq_prefill_tc.cuh"
+
+namespace kvq {
+
 static PFN_cuTensorMapEncodeTiled_v12000 pf_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -440,6 +446,29 @@ static int prefill_launch(const PrefillParams& p, const CUtensorMap& tk, const C
   }
   const dim3 grid(p.tiles, p.Hkv, p.B), block(kThreads);
   if (launch_pdl(prefill_kernel<FMT, DH>, grid, block, smem, s, p, tk, tv) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+// The FP8 caches' prefill on the tcgen05 tensor cores (128 query rows a CTA).
+template <int FMT, int DH>
+static int prefill_tc_launch(PrefillParams p, int max_q_len, const CUtensorMap& tk,
+                             const CUtensorMap& tv, cudaStream_t s) {
+  constexpr size_t smem = tc::Layout<DH>::total;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (cudaFuncSetAttribute(tc::prefill_tc_kernel<FMT, DH>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  const int TQ = tc::kRows / p.G;
+  p.tiles = (max_q_len + TQ - 1) / TQ;
+  const dim3 grid(p.tiles, p.Hkv, p.B), block(tc::kThreadsTc);
+  if (launch_pdl(tc::prefill_tc_kernel<FMT, DH>, grid, block, smem, s, p, tk, tv) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
@@ -519,11 +548,11 @@ extern "C" int kvq_prefill_attn(const void* q, const int32_t* cu_q_lens, int64_t
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (fmt) {
     case KVQ_FMT_E4M3:
-      return head_dim == 128 ? prefill_launch<KVQ_FMT_E4M3, 128>(p, tk, tv, s)
-                             : prefill_launch<KVQ_FMT_E4M3, 64>(p, tk, tv, s);
+      return head_dim == 128 ? prefill_tc_launch<KVQ_FMT_E4M3, 128>(p, max_q_len, tk, tv, s)
+                             : prefill_tc_launch<KVQ_FMT_E4M3, 64>(p, max_q_len, tk, tv, s);
     case KVQ_FMT_E5M2:
-      return head_dim == 128 ? prefill_launch<KVQ_FMT_E5M2, 128>(p, tk, tv, s)
-                             : prefill_launch<KVQ_FMT_E5M2, 64>(p, tk, tv, s);
+      return head_dim == 128 ? prefill_tc_launch<KVQ_FMT_E5M2, 128>(p, max_q_len, tk, tv, s)
+                             : prefill_tc_launch<KVQ_FMT_E5M2, 64>(p, max_q_len, tk, tv, s);
     default:
       return head_dim == 128 ? prefill_launch<KVQ_FMT_BF16, 128>(p, tk, tv, s)
                              : prefill_launch<KVQ_FMT_BF16, 64>(p, tk, tv, s);

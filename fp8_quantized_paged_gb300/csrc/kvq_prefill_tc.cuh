@@ -1,0 +1,530 @@
+// kvq_prefill_tc.cuh -- the prefill kernel of the FP8 caches on the 5th-
+// generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// One CTA per (sequence, KV head, tile of 128 query rows); a row is a (query
+// token, query head of the group) pair, so a tile holds 128 / G tokens.  The
+// keys stream in blocks of 64 tokens (4 pages):
+//   warp 4 (producer): TMA loads of the block's 4 K and 4 V FP8 pages into a
+//     3-stage ring (the decode's 128-byte-swizzled page boxes).
+//   warp 5 (MMA): allocates 256 TMEM columns (two 64-column S buffers and
+//     the dh-column O accumulator); one elected lane issues, per block,
+//     S = Q K^T (M = 128, N = 64, K = dh in steps of 16) and, once the block's
+//     probabilities are in shared memory, O += P V (N = dh, K = 64 tokens),
+//     each completion signalled to an mbarrier by tcgen05.commit.
+//   warps 0-3 (128 threads, thread r = row r = TMEM lane r): convert the next
+//     block's pages to f16 in shared memory (K as the B operand of QK^T,
+//     token-major; V transposed, dim-major, as the B operand of PV), then
+//     run the softmax of the current block: S row from TMEM, causal / window
+//     mask, online max with a lazy rescale of the O row in TMEM, P = 2^(x-m)
+//     as f16 into shared memory (the A operand of PV).
+// Every shared-memory operand is in the K-major 128-byte-swizzle layout:
+// 8-row groups of 1024 bytes, 128-byte rows of 64 f16, 16-byte chunk c of
+// row r at chunk c ^ (r % 8); wider K in further 64-column blocks of the
+// tile.  All waits are bounded; a timeout sets KVQ_DEV_WAIT_TIMEOUT, the
+// roles stop, and the CTA waits (bounded) for its copies and MMAs in flight
+// before it frees the tensor memory.
+#pragma once
+
+namespace kvq {
+namespace tc {
+
+constexpr int kRows = 128;      // query rows per CTA (MMA M)
+constexpr int kKeys = 64;       // tokens per key block (QK^T N, PV K)
+constexpr int kStagesTc = 3;    // FP8 page stages
+constexpr int kThreadsTc = 192; // warps 0-3 softmax/convert, 4 producer, 5 MMA
+constexpr uint32_t kTmemCols = 256;
+
+template <int DH>
+struct Layout {
+  static constexpr int kPage8 = kBS * DH;                  // bytes of one FP8 page
+  static constexpr int kStage = 8 * kPage8;                // 4 K pages + 4 V pages
+  static constexpr size_t q = 0;                           // Q   [128][DH] f16
+  static constexpr size_t qBytes = static_cast<size_t>(kRows) * DH * 2;
+  static constexpr size_t k = q + qBytes;                  // K   2 x [64][DH] f16
+  static constexpr size_t kBytes = static_cast<size_t>(kKeys) * DH * 2;
+  static constexpr size_t vt = k + 2 * kBytes;             // V^T 2 x [DH][64] f16
+  static constexpr size_t vtBytes = static_cast<size_t>(DH) * kKeys * 2;
+  static constexpr size_t p = vt + 2 * vtBytes;            // P   [128][64] f16
+  static constexpr size_t pBytes = static_cast<size_t>(kRows) * kKeys * 2;
+  static constexpr size_t stage = p + pBytes;              // FP8 pages, kStagesTc stages
+  static constexpr size_t bars = stage + static_cast<size_t>(kStagesTc) * kStage;
+  // barriers: full[3], empty[3], conv[2], sfull[2], pfull, odone, fin
+  static constexpr int kBars = 2 * kStagesTc + 2 + 2 + 3;
+  static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
+  // misc: tmem address, abort flag, page flags [3 stages][4 pages], issued[3]
+  static constexpr size_t total = misc + 128 + 1024;
+};
+
+// Byte offset of f16 element (row, col) in a K-major 128-byte-swizzled tile
+// of `rows` rows (col = K index).
+KVQ_DEVI uint32_t sw128_off(int row, int col, int rows) {
+  const int blk = col >> 6, c16 = (col & 63) >> 3;
+  return static_cast<uint32_t>(blk * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
+                               ((c16 ^ (row & 7)) << 4) + ((col & 7) << 1));
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), leading byte offset unused (1).
+KVQ_DEVI uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator, f16 A and B, both
+// K-major, N and M as given.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+KVQ_DEVI void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+KVQ_DEVI void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+
+KVQ_DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+KVQ_DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of this thread's lane (warp-collective).
+KVQ_DEVI void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  __syncwarp();
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+KVQ_DEVI void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  __syncwarp();
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+        "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+        "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+        "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+        "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
+        "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+        "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
+        "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+        "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
+        "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+KVQ_DEVI void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+KVQ_DEVI uint32_t lds32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
+  return r;
+}
+
+template <int FMT, int DH>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillParams p,
+                      const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv) {
+  using Lo = Layout<DH>;
+  using C = Cfg<FMT, DH>;
+  constexpr int S = kStagesTc;
+  constexpr int KSTEPS = DH / 16;  // QK^T MMAs per block
+  static_assert(C::kRow == DH && C::kPage == Lo::kPage8, "FP8 pages");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lo::bars);
+  uint64_t* full = bars;               // [S] FP8 stage landed
+  uint64_t* empty = bars + S;          // [S] FP8 stage converted (128 arrivals)
+  uint64_t* conv = bars + 2 * S;       // [2] f16 K / V^T buffer b ready (128 arrivals)
+  uint64_t* sfull = bars + 2 * S + 2;  // [2] S buffer b written (commit)
+  uint64_t* pfull = bars + 2 * S + 4;  // P of the block written (128 arrivals)
+  uint64_t* odone = bars + 2 * S + 5;  // PV of the block done (commit)
+  uint64_t* fin = bars + 2 * S + 6;    // every MMA done (commit)
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lo::misc);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  uint32_t* pg_bad = const_cast<uint32_t*>(tmem_slot + 2);    // [S][4] page masked out
+  int32_t* issued = reinterpret_cast<int32_t*>(pg_bad + S * 4);  // [S] last block issued
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.z, gkv = blockIdx.y;
+  const int tile = p.tiles - 1 - static_cast<int>(blockIdx.x);  // longest tiles first
+  const int TQ = kRows / p.G;
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 128);
+      issued[i] = -1;
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&conv[i], 128);
+      mbar_init(&sfull[i], 1);
+    }
+    mbar_init(pfull, 128);
+    mbar_init(odone, 1);
+    mbar_init(fin, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  pdl_wait();
+  pdl_allow_next();
+
+  const int q0 = __ldg(p.cu_q + b);
+  const int n = __ldg(p.cu_q + b + 1) - q0;
+  const int j0 = tile * TQ;
+  if (n <= 0 || j0 >= n) return;  // the whole CTA, before any tensor memory is taken
+  const int j1 = min(n, j0 + TQ);
+  const int L = __ldg(p.seq_lens + b);
+  if (!(L >= n && L <= p.max_blocks * kBS)) {
+    if (tile == 0 && gkv == 0 && tid == 0) flag_status(p.status, KVQ_DEV_BAD_SEQLEN);
+    for (int i = tid; i < (j1 - j0) * p.G * DH; i += kThreadsTc) {
+      const int r = i / DH, d = i - r * DH;
+      const int64_t orow = static_cast<int64_t>(q0 + j0 + r / p.G) * p.Hq + gkv * p.G + r % p.G;
+      if (guard(orow >= 0 && orow < p.total_q * p.Hq, p.status, 20)) p.out[orow * DH + d] = 0;
+    }
+    return;
+  }
+  const int base = L - n;  // position of query token 0
+  const int pos_first = base + j0, pos_last = base + j1 - 1;
+  const int p_begin = window_lo(p.window, pos_first + 1) / kBS;  // first page
+  const int p_end = pos_last / kBS;                              // last page
+  const int nblk = (p_end - p_begin) / 4 + 1;                    // key blocks of 4 pages
+
+  if (warp == 5) {  // tensor memory for S (2 x 64 columns) and O (DH columns)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(const_cast<uint32_t*>(tmem_slot))), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_o = tmem + 128;  // O: columns 128 .. 128 + DH - 1
+
+  auto fail = [&](void) {
+    if (!*abort_flag) {
+      *abort_flag = 1u;
+      flag_status(p.status, KVQ_DEV_WAIT_TIMEOUT);
+    }
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int j = 0; j < nblk && !*abort_flag; ++j) {
+        const int s = j % S;
+        if (j >= S && !wait_or_abort(&empty[s], static_cast<uint32_t>(((j / S) - 1) & 1), abort_flag)) {
+          fail();
+          break;
+        }
+        uint32_t bytes = 0;
+        int rows[4];
+        for (int i = 0; i < 4; ++i) {
+          const int col = p_begin + 4 * j + i;
+          int blk = -1;
+          if (col <= p_end && guard(col >= 0 && col < p.max_blocks, p.status, 21))
+            blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + col);
+          bool bad = blk < 0 || blk >= p.num_blocks;
+          if (bad && col <= p_end) flag_status(p.status, KVQ_DEV_BAD_BLOCK);
+          int32_t row = ((bad ? 0 : blk) * p.Hkv + gkv) * kBS;
+          if (!bad && !guard(row >= 0 && row + kBS <= p.rows, p.status, 22)) bad = true;
+          rows[i] = bad ? -1 : row;
+          pg_bad[s * 4 + i] = bad ? 1u : 0u;
+          if (!bad) bytes += 2 * Lo::kPage8;
+        }
+        issued[s] = j;
+        if (bytes == 0) {  // nothing to load: complete the phase by hand
+          mbar_arrive(&full[s]);
+          continue;
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        uint8_t* dst = smem + Lo::stage + static_cast<size_t>(s) * Lo::kStage;
+        for (int i = 0; i < 4; ++i) {
+          if (rows[i] < 0) continue;
+          tma_load_2d(dst + i * Lo::kPage8, &tmk, 0, rows[i], &full[s]);
+          tma_load_2d(dst + (4 + i) * Lo::kPage8, &tmv, 0, rows[i], &full[s]);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_f16(kRows, kKeys), id_pv = idesc_f16(kRows, DH);
+      const uint32_t a_q = sbase + Lo::q, a_p = sbase + Lo::p;
+      bool ok = true;
+      for (int j = 0; j <= nblk && ok; ++j) {
+        if (j < nblk) {  // S[j % 2] = Q K_j^T
+          ok = wait_or_abort(&conv[j & 1], static_cast<uint32_t>((j >> 1) & 1), abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t b_k = sbase + Lo::k + (j & 1) * Lo::kBytes;
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const uint32_t off_a = (ks >> 2) * (kRows * 128) + (ks & 3) * 32;
+            const uint32_t off_b = (ks >> 2) * (kKeys * 128) + (ks & 3) * 32;
+            mma_f16_ss(tmem + (j & 1) * kKeys, sw128_desc(a_q + off_a), sw128_desc(b_k + off_b),
+                       id_qk, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&sfull[j & 1]);
+        }
+        if (j >= 1) {  // O += P_{j-1} V_{j-1}
+          const int jp = j - 1;
+          ok = wait_or_abort(pfull, static_cast<uint32_t>(jp & 1), abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t b_v = sbase + Lo::vt + (jp & 1) * Lo::vtBytes;
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            mma_f16_ss(tm_o, sw128_desc(a_p + kk * 32), sw128_desc(b_v + kk * 32), id_pv,
+                       (jp > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(odone);
+        }
+      }
+      if (!ok) fail();
+      mma_commit(fin);  // completes when every MMA issued above has
+      if (!mbar_wait(fin, 0u)) fail();
+    }
+  } else {
+    // ------------------------------------------------------------ convert + softmax
+    const int r = tid;  // row = TMEM lane
+    const int jr = j0 + r / p.G;
+    const bool live = jr < j1;
+    const int pos = live ? base + jr : -1;
+    const int lo = live ? window_lo(p.window, pos + 1) : 0;
+    const int64_t qrow = live ? static_cast<int64_t>(q0 + jr) * p.Hq + gkv * p.G + r % p.G : -1;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    // Q row r -> f16 into the A tile
+    {
+      const bool ok = live && guard(qrow < p.total_q * p.Hq, p.status, 23);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (ok ? qrow : 0) * DH);
+#pragma unroll
+      for (int c = 0; c < DH / 8; ++c) {
+        const uint4 v = ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = f32x2_to_f16x2(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]));
+        sts128(sbase + Lo::q + sw128_off(r, 8 * c, kRows), h[0], h[1], h[2], h[3]);
+      }
+    }
+    const float sk = __ldg(p.ks + (p.per_head ? gkv : 0));
+    const float sv = __ldg(p.vs + (p.per_head ? gkv : 0));
+    const float lscale = sk * p.logit_scale;
+
+    // Waits of this role are warp-uniform (the TMEM accesses after them are
+    // warp-collective).
+    auto wait_w = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(kFull, wait_or_abort(bar, parity, abort_flag));
+    };
+    uint32_t badmask[2] = {0u, 0u};  // masked-out pages of the block in buffer 0 / 1
+    // Block j's FP8 pages -> f16 K (token rows) and V^T (dim rows), buffer j % 2.
+    auto convert = [&](int j) -> bool {
+      const int s = j % S;
+      if (!wait_w(&full[s], static_cast<uint32_t>((j / S) & 1))) return false;
+      if (j >= 2 && !wait_w(odone, static_cast<uint32_t>((j - 2) & 1)))
+        return false;  // PV of block j - 2 (the buffer's last reader) is done
+      // the stage's page flags, kept for the softmax of block j (the
+      // producer rewrites the stage's flags once the stage is released)
+      badmask[j & 1] = (pg_bad[s * 4] ? 1u : 0u) | (pg_bad[s * 4 + 1] ? 2u : 0u) |
+                       (pg_bad[s * 4 + 2] ? 4u : 0u) | (pg_bad[s * 4 + 3] ? 8u : 0u);
+      const uint32_t stg = sbase + Lo::stage + s * Lo::kStage;
+      const uint32_t kb = sbase + Lo::k + (j & 1) * Lo::kBytes;
+      const uint32_t vb = sbase + Lo::vt + (j & 1) * Lo::vtBytes;
+      const int tok_base = (p_begin + 4 * j) * kBS;
+      // K: 16-byte chunk (token t, dims 16c .. 16c + 15) -> 32 bytes of f16
+      constexpr int KCH = DH / 16;  // chunks per token row
+      for (int e = tid; e < kKeys * KCH; e += 128) {
+        const int t = e / KCH, c = e - t * KCH;
+        const int pg = t >> 4, tr = t & 15;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (!(badmask[j & 1] >> pg & 1u))
+          w = lds128(stg + pg * Lo::kPage8 + swz(page_off<C::kRow>(tr, 16 * c), C::kSwz));
+        uint32_t h[8];
+        fp8x4_to_f16x2x2<FMT>(w.x, h[0], h[1]);
+        fp8x4_to_f16x2x2<FMT>(w.y, h[2], h[3]);
+        fp8x4_to_f16x2x2<FMT>(w.z, h[4], h[5]);
+        fp8x4_to_f16x2x2<FMT>(w.w, h[6], h[7]);
+        sts128(kb + sw128_off(t, 16 * c, kKeys), h[0], h[1], h[2], h[3]);
+        sts128(kb + sw128_off(t, 16 * c + 8, kKeys), h[4], h[5], h[6], h[7]);
+      }
+      // V^T: tokens 8g .. 8g + 7 x dims 4a .. 4a + 3 -> four 16-byte chunks;
+      // tokens past the sequence or in masked pages are zero (p = 0 would
+      // not clear a NaN)
+      for (int e = tid; e < (kKeys / 8) * (DH / 4); e += 128) {
+        const int g8 = e / (DH / 4), a = e - g8 * (DH / 4);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int t = 8 * g8 + i, pg = t >> 4, tr = t & 15;
+          const bool ok = !(badmask[j & 1] >> pg & 1u) && tok_base + t < L;
+          w[i] = ok ? lds32(stg + (4 + pg) * Lo::kPage8 + swz(page_off<C::kRow>(tr, 4 * a), C::kSwz))
+                    : 0u;
+        }
+#pragma unroll
+        for (int d = 0; d < 4; d += 2) {  // dims 4a + d, 4a + d + 1
+          uint32_t lo_d[4], hi_d[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {  // tokens 2m, 2m + 1 of the 8
+            const uint32_t sel = static_cast<uint32_t>(d | ((4 + d) << 4) | ((d + 1) << 8) | ((5 + d) << 12));
+            fp8x4_to_f16x2x2<FMT>(prmt(w[2 * m], w[2 * m + 1], sel), lo_d[m], hi_d[m]);
+          }
+          sts128(vb + sw128_off(4 * a + d, 8 * g8, DH), lo_d[0], lo_d[1], lo_d[2], lo_d[3]);
+          sts128(vb + sw128_off(4 * a + d + 1, 8 * g8, DH), hi_d[0], hi_d[1], hi_d[2], hi_d[3]);
+        }
+      }
+      fence_proxy_async_smem();  // generic writes -> the tensor core's reads
+      mbar_arrive(&conv[j & 1]);
+      mbar_arrive(&empty[s]);
+      return true;
+    };
+
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    fence_proxy_async_smem();  // the Q tile
+    ok = convert(0);
+    for (int j = 0; j < nblk && ok; ++j) {
+      if (j + 1 < nblk) {
+        ok = convert(j + 1);
+        if (!ok) break;
+      }
+      // ---- softmax of block j
+      if (!wait_w(&sfull[j & 1], static_cast<uint32_t>((j >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[kKeys];
+      {
+        float t0[32], t1[32];
+        tmem_ld32(tmem + lane_base + (j & 1) * kKeys, t0);
+        tmem_ld32(tmem + lane_base + (j & 1) * kKeys + 32, t1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = t0[i];
+          x[32 + i] = t1[i];
+        }
+      }
+      const int kb0 = (p_begin + 4 * j) * kBS;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kKeys; ++i) {
+        const int kp = kb0 + i;
+        const bool valid = live && kp >= lo && kp <= pos && !(badmask[j & 1] >> (i >> 4) & 1u);
+        x[i] = valid ? x[i] * lscale : -INFINITY;
+        mx = fmaxf(mx, x[i]);
+      }
+      // PV of block j - 1 must be done before P is rewritten and O touched
+      if (j >= 1 && !wait_w(odone, static_cast<uint32_t>((j - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool grow = mx > m + kRescaleThreshold;
+      if (__any_sync(kFull, grow)) {  // rescale O rows (warp-collective TMEM access)
+        const float nm = grow ? mx : m;
+        const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - nm);
+        if (j >= 1) {
+#pragma unroll
+          for (int c = 0; c < DH; c += 32) {
+            float o[32];
+            tmem_ld32(tm_o + lane_base + c, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= a;
+            tmem_st32(tm_o + lane_base + c, o);
+          }
+        }
+        l *= a;
+        m = nm;
+      }
+      // P row -> f16 into the A tile of PV
+      uint32_t ph[kKeys / 2];
+#pragma unroll
+      for (int i = 0; i < kKeys; i += 2) {
+        const float p0 = (x[i] == -INFINITY) ? 0.f : fast_exp2(x[i] - m);
+        const float p1 = (x[i + 1] == -INFINITY) ? 0.f : fast_exp2(x[i + 1] - m);
+        l += p0 + p1;
+        ph[i / 2] = f32x2_to_f16x2(p0, p1);
+      }
+#pragma unroll
+      for (int c = 0; c < kKeys / 8; ++c)
+        sts128(sbase + Lo::p + sw128_off(r, 8 * c, kRows), ph[4 * c], ph[4 * c + 1], ph[4 * c + 2],
+               ph[4 * c + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(pfull);
+    }
+    if (!ok) fail();
+    // ---- epilogue: O row / l * sV -> bf16
+    if (ok && wait_w(odone, static_cast<uint32_t>((nblk - 1) & 1))) {
+      tc_fence_after();
+      const float f = l > 0.f ? sv / l : 0.f;
+      const bool store = live && guard(qrow < p.total_q * p.Hq, p.status, 24);
+#pragma unroll
+      for (int c = 0; c < DH; c += 32) {
+        float o[32];
+        tmem_ld32(tm_o + lane_base + c, o);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * DH + c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(f32x2_to_bf16x2(o[8 * v] * f, o[8 * v + 1] * f),
+                                f32x2_to_bf16x2(o[8 * v + 2] * f, o[8 * v + 3] * f),
+                                f32x2_to_bf16x2(o[8 * v + 4] * f, o[8 * v + 5] * f),
+                                f32x2_to_bf16x2(o[8 * v + 6] * f, o[8 * v + 7] * f));
+        }
+      }
+    } else if (ok) {
+      fail();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // After an abort: wait (bounded) for the page copies still in flight and
+  // for the MMAs (the MMA lane waited for its own), then free the TMEM.
+  if (*abort_flag && tid == 0) {
+    for (int s = 0; s < S; ++s)
+      if (issued[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>((issued[s] / S) & 1));
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace tc
+}  // namespace kvq
