@@ -4,19 +4,20 @@
 // One CTA per (sequence, KV head, tile of 128 query rows); a row is a (query
 // token, query head of the group) pair, so a tile holds 128 / G tokens.  The
 // keys stream in blocks of 64 tokens (4 pages):
-//   warp 4 (producer): TMA loads of the block's 4 K and 4 V FP8 pages into a
+//   warp 8 (producer): TMA loads of the block's 4 K and 4 V FP8 pages into a
 //     3-stage ring (the decode's 128-byte-swizzled page boxes).
-//   warp 5 (MMA): allocates 256 TMEM columns (two 64-column S buffers and
+//   warps 4-7 (converters): each block's pages to f16 in shared memory, K as
+//     the B operand of QK^T (token-major) and V transposed (dim-major) as the
+//     B operand of PV, double-buffered.
+//   warp 9 (MMA): allocates 256 TMEM columns (two 64-column S buffers and
 //     the dh-column O accumulator); one elected lane issues, per block,
 //     S = Q K^T (M = 128, N = 64, K = dh in steps of 16) and, once the block's
 //     probabilities are in shared memory, O += P V (N = dh, K = 64 tokens),
 //     each completion signalled to an mbarrier by tcgen05.commit.
-//   warps 0-3 (128 threads, thread r = row r = TMEM lane r): convert the next
-//     block's pages to f16 in shared memory (K as the B operand of QK^T,
-//     token-major; V transposed, dim-major, as the B operand of PV), then
-//     run the softmax of the current block: S row from TMEM, causal / window
-//     mask, online max with a lazy rescale of the O row in TMEM, P = 2^(x-m)
-//     as f16 into shared memory (the A operand of PV).
+//   warps 0-3 (softmax; thread r = row r = TMEM lane r): Q row r to f16,
+//     then per block the S row from TMEM, causal / window mask (skipped for
+//     blocks the whole row sees), online max with a lazy rescale of the O row
+//     in TMEM, P = 2^(x-m) as f16 into shared memory (the A operand of PV).
 // Every shared-memory operand is in the K-major 128-byte-swizzle layout:
 // 8-row groups of 1024 bytes, 128-byte rows of 64 f16, 16-byte chunk c of
 // row r at chunk c ^ (r % 8); wider K in further 64-column blocks of the
@@ -31,7 +32,7 @@ namespace tc {
 constexpr int kRows = 128;      // query rows per CTA (MMA M)
 constexpr int kKeys = 64;       // tokens per key block (QK^T N, PV K)
 constexpr int kStagesTc = 3;    // FP8 page stages
-constexpr int kThreadsTc = 192; // warps 0-3 softmax/convert, 4 producer, 5 MMA
+constexpr int kThreadsTc = 320; // warps 0-3 softmax, 4-7 convert, 8 producer, 9 MMA
 constexpr uint32_t kTmemCols = 256;
 
 template <int DH>
@@ -48,10 +49,11 @@ struct Layout {
   static constexpr size_t pBytes = static_cast<size_t>(kRows) * kKeys * 2;
   static constexpr size_t stage = p + pBytes;              // FP8 pages, kStagesTc stages
   static constexpr size_t bars = stage + static_cast<size_t>(kStagesTc) * kStage;
-  // barriers: full[3], empty[3], conv[2], sfull[2], pfull, odone, fin
-  static constexpr int kBars = 2 * kStagesTc + 2 + 2 + 3;
+  // barriers: full[3], empty[3], conv[2], sfull[2], pfull, odone, fin, qready
+  static constexpr int kBars = 2 * kStagesTc + 2 + 2 + 4;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
-  // misc: tmem address, abort flag, page flags [3 stages][4 pages], issued[3]
+  // misc: tmem address, abort flag, page flags [3 stages][4 pages], issued[3],
+  // masked pages of the blocks in the two f16 buffers [2]
   static constexpr size_t total = misc + 128 + 1024;
 };
 
@@ -167,10 +169,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint64_t* pfull = bars + 2 * S + 4;  // P of the block written (128 arrivals)
   uint64_t* odone = bars + 2 * S + 5;  // PV of the block done (commit)
   uint64_t* fin = bars + 2 * S + 6;    // every MMA done (commit)
+  uint64_t* qready = bars + 2 * S + 7; // the Q tile written (128 arrivals)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lo::misc);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint32_t* pg_bad = const_cast<uint32_t*>(tmem_slot + 2);    // [S][4] page masked out
   int32_t* issued = reinterpret_cast<int32_t*>(pg_bad + S * 4);  // [S] last block issued
+  volatile uint32_t* bufmask = reinterpret_cast<volatile uint32_t*>(issued + S);  // [2]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.z, gkv = blockIdx.y;
@@ -190,10 +194,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(pfull, 128);
     mbar_init(odone, 1);
     mbar_init(fin, 1);
+    mbar_init(qready, 128);
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int p_end = pos_last / kBS;                              // last page
   const int nblk = (p_end - p_begin) / 4 + 1;                    // key blocks of 4 pages
 
-  if (warp == 5) {  // tensor memory for S (2 x 64 columns) and O (DH columns)
+  if (warp == 9) {  // tensor memory for S (2 x 64 columns) and O (DH columns)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(const_cast<uint32_t*>(tmem_slot))), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       for (int j = 0; j < nblk && !*abort_flag; ++j) {
@@ -277,12 +282,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_f16(kRows, kKeys), id_pv = idesc_f16(kRows, DH);
       const uint32_t a_q = sbase + Lo::q, a_p = sbase + Lo::p;
-      bool ok = true;
+      bool ok = wait_or_abort(qready, 0u, abort_flag);
       for (int j = 0; j <= nblk && ok; ++j) {
         if (j < nblk) {  // S[j % 2] = Q K_j^T
           ok = wait_or_abort(&conv[j & 1], static_cast<uint32_t>((j >> 1) & 1), abort_flag);
@@ -315,8 +320,83 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mma_commit(fin);  // completes when every MMA issued above has
       if (!mbar_wait(fin, 0u)) fail();
     }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ converters
+    const int ct = tid - 128;  // 0 .. 127
+    auto wait_w = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(kFull, wait_or_abort(bar, parity, abort_flag));
+    };
+    uint32_t badmask[2] = {0u, 0u};  // masked-out pages of the block in buffer 0 / 1
+    // Block j's FP8 pages -> f16 K (token rows) and V^T (dim rows), buffer j % 2.
+    auto convert = [&](int j) -> bool {
+      const int s = j % S;
+      if (!wait_w(&full[s], static_cast<uint32_t>((j / S) & 1))) return false;
+      if (j >= 2 && !wait_w(odone, static_cast<uint32_t>((j - 2) & 1)))
+        return false;  // PV of block j - 2 (the buffer's last reader) is done
+      // the stage's page flags, kept for the softmax of block j (the
+      // producer rewrites the stage's flags once the stage is released)
+      badmask[j & 1] = (pg_bad[s * 4] ? 1u : 0u) | (pg_bad[s * 4 + 1] ? 2u : 0u) |
+                       (pg_bad[s * 4 + 2] ? 4u : 0u) | (pg_bad[s * 4 + 3] ? 8u : 0u);
+      // for the softmax of block j (read after it waits for conv[j % 2])
+      if (ct == 0) bufmask[j & 1] = badmask[j & 1];
+      const uint32_t stg = sbase + Lo::stage + s * Lo::kStage;
+      const uint32_t kb = sbase + Lo::k + (j & 1) * Lo::kBytes;
+      const uint32_t vb = sbase + Lo::vt + (j & 1) * Lo::vtBytes;
+      const int tok_base = (p_begin + 4 * j) * kBS;
+      // K: 16-byte chunk (token t, dims 16c .. 16c + 15) -> 32 bytes of f16
+      constexpr int KCH = DH / 16;  // chunks per token row
+      for (int e = ct; e < kKeys * KCH; e += 128) {
+        const int t = e / KCH, c = e - t * KCH;
+        const int pg = t >> 4, tr = t & 15;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (!(badmask[j & 1] >> pg & 1u))
+          w = lds128(stg + pg * Lo::kPage8 + swz(page_off<C::kRow>(tr, 16 * c), C::kSwz));
+        uint32_t h[8];
+        fp8x4_to_f16x2x2<FMT>(w.x, h[0], h[1]);
+        fp8x4_to_f16x2x2<FMT>(w.y, h[2], h[3]);
+        fp8x4_to_f16x2x2<FMT>(w.z, h[4], h[5]);
+        fp8x4_to_f16x2x2<FMT>(w.w, h[6], h[7]);
+        sts128(kb + sw128_off(t, 16 * c, kKeys), h[0], h[1], h[2], h[3]);
+        sts128(kb + sw128_off(t, 16 * c + 8, kKeys), h[4], h[5], h[6], h[7]);
+      }
+      // V^T: tokens 8g .. 8g + 7 x dims 4a .. 4a + 3 -> four 16-byte chunks;
+      // tokens past the sequence or in masked pages are zero (p = 0 would
+      // not clear a NaN)
+      for (int e = ct; e < (kKeys / 8) * (DH / 4); e += 128) {
+        const int g8 = e / (DH / 4), a = e - g8 * (DH / 4);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int t = 8 * g8 + i, pg = t >> 4, tr = t & 15;
+          const bool ok = !(badmask[j & 1] >> pg & 1u) && tok_base + t < L;
+          w[i] = ok ? lds32(stg + (4 + pg) * Lo::kPage8 + swz(page_off<C::kRow>(tr, 4 * a), C::kSwz))
+                    : 0u;
+        }
+#pragma unroll
+        for (int d = 0; d < 4; d += 2) {  // dims 4a + d, 4a + d + 1
+          uint32_t lo_d[4], hi_d[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {  // tokens 2m, 2m + 1 of the 8
+            const uint32_t sel = static_cast<uint32_t>(d | ((4 + d) << 4) | ((d + 1) << 8) | ((5 + d) << 12));
+            fp8x4_to_f16x2x2<FMT>(prmt(w[2 * m], w[2 * m + 1], sel), lo_d[m], hi_d[m]);
+          }
+          sts128(vb + sw128_off(4 * a + d, 8 * g8, DH), lo_d[0], lo_d[1], lo_d[2], lo_d[3]);
+          sts128(vb + sw128_off(4 * a + d + 1, 8 * g8, DH), hi_d[0], hi_d[1], hi_d[2], hi_d[3]);
+        }
+      }
+      fence_proxy_async_smem();  // generic writes -> the tensor core's reads
+      mbar_arrive(&conv[j & 1]);
+      mbar_arrive(&empty[s]);
+      return true;
+    };
+
+    for (int j = 0; j < nblk; ++j)
+      if (!convert(j)) {
+        fail();
+        break;
+      }
   } else {
-    // ------------------------------------------------------------ convert + softmax
+    // ------------------------------------------------------------ softmax
     const int r = tid;  // row = TMEM lane
     const int jr = j0 + r / p.G;
     const bool live = jr < j1;
@@ -348,78 +428,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     auto wait_w = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(kFull, wait_or_abort(bar, parity, abort_flag));
     };
-    uint32_t badmask[2] = {0u, 0u};  // masked-out pages of the block in buffer 0 / 1
-    // Block j's FP8 pages -> f16 K (token rows) and V^T (dim rows), buffer j % 2.
-    auto convert = [&](int j) -> bool {
-      const int s = j % S;
-      if (!wait_w(&full[s], static_cast<uint32_t>((j / S) & 1))) return false;
-      if (j >= 2 && !wait_w(odone, static_cast<uint32_t>((j - 2) & 1)))
-        return false;  // PV of block j - 2 (the buffer's last reader) is done
-      // the stage's page flags, kept for the softmax of block j (the
-      // producer rewrites the stage's flags once the stage is released)
-      badmask[j & 1] = (pg_bad[s * 4] ? 1u : 0u) | (pg_bad[s * 4 + 1] ? 2u : 0u) |
-                       (pg_bad[s * 4 + 2] ? 4u : 0u) | (pg_bad[s * 4 + 3] ? 8u : 0u);
-      const uint32_t stg = sbase + Lo::stage + s * Lo::kStage;
-      const uint32_t kb = sbase + Lo::k + (j & 1) * Lo::kBytes;
-      const uint32_t vb = sbase + Lo::vt + (j & 1) * Lo::vtBytes;
-      const int tok_base = (p_begin + 4 * j) * kBS;
-      // K: 16-byte chunk (token t, dims 16c .. 16c + 15) -> 32 bytes of f16
-      constexpr int KCH = DH / 16;  // chunks per token row
-      for (int e = tid; e < kKeys * KCH; e += 128) {
-        const int t = e / KCH, c = e - t * KCH;
-        const int pg = t >> 4, tr = t & 15;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (!(badmask[j & 1] >> pg & 1u))
-          w = lds128(stg + pg * Lo::kPage8 + swz(page_off<C::kRow>(tr, 16 * c), C::kSwz));
-        uint32_t h[8];
-        fp8x4_to_f16x2x2<FMT>(w.x, h[0], h[1]);
-        fp8x4_to_f16x2x2<FMT>(w.y, h[2], h[3]);
-        fp8x4_to_f16x2x2<FMT>(w.z, h[4], h[5]);
-        fp8x4_to_f16x2x2<FMT>(w.w, h[6], h[7]);
-        sts128(kb + sw128_off(t, 16 * c, kKeys), h[0], h[1], h[2], h[3]);
-        sts128(kb + sw128_off(t, 16 * c + 8, kKeys), h[4], h[5], h[6], h[7]);
-      }
-      // V^T: tokens 8g .. 8g + 7 x dims 4a .. 4a + 3 -> four 16-byte chunks;
-      // tokens past the sequence or in masked pages are zero (p = 0 would
-      // not clear a NaN)
-      for (int e = tid; e < (kKeys / 8) * (DH / 4); e += 128) {
-        const int g8 = e / (DH / 4), a = e - g8 * (DH / 4);
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int t = 8 * g8 + i, pg = t >> 4, tr = t & 15;
-          const bool ok = !(badmask[j & 1] >> pg & 1u) && tok_base + t < L;
-          w[i] = ok ? lds32(stg + (4 + pg) * Lo::kPage8 + swz(page_off<C::kRow>(tr, 4 * a), C::kSwz))
-                    : 0u;
-        }
-#pragma unroll
-        for (int d = 0; d < 4; d += 2) {  // dims 4a + d, 4a + d + 1
-          uint32_t lo_d[4], hi_d[4];
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {  // tokens 2m, 2m + 1 of the 8
-            const uint32_t sel = static_cast<uint32_t>(d | ((4 + d) << 4) | ((d + 1) << 8) | ((5 + d) << 12));
-            fp8x4_to_f16x2x2<FMT>(prmt(w[2 * m], w[2 * m + 1], sel), lo_d[m], hi_d[m]);
-          }
-          sts128(vb + sw128_off(4 * a + d, 8 * g8, DH), lo_d[0], lo_d[1], lo_d[2], lo_d[3]);
-          sts128(vb + sw128_off(4 * a + d + 1, 8 * g8, DH), hi_d[0], hi_d[1], hi_d[2], hi_d[3]);
-        }
-      }
-      fence_proxy_async_smem();  // generic writes -> the tensor core's reads
-      mbar_arrive(&conv[j & 1]);
-      mbar_arrive(&empty[s]);
-      return true;
-    };
-
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    fence_proxy_async_smem();  // the Q tile
-    ok = convert(0);
+    fence_proxy_async_smem();  // the Q tile -> the tensor core
+    mbar_arrive(qready);
     for (int j = 0; j < nblk && ok; ++j) {
-      if (j + 1 < nblk) {
-        ok = convert(j + 1);
-        if (!ok) break;
+      // the block's masked pages (the converters wrote them before conv[j % 2])
+      if (!wait_w(&conv[j & 1], static_cast<uint32_t>((j >> 1) & 1))) {
+        ok = false;
+        break;
       }
-      // ---- softmax of block j
+      const uint32_t bm = bufmask[j & 1];
       if (!wait_w(&sfull[j & 1], static_cast<uint32_t>((j >> 1) & 1))) {
         ok = false;
         break;
@@ -438,12 +457,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       const int kb0 = (p_begin + 4 * j) * kBS;
       float mx = -INFINITY;
+      if (live && bm == 0u && kb0 >= lo && kb0 + kKeys - 1 <= pos) {  // the row sees the block
 #pragma unroll
-      for (int i = 0; i < kKeys; ++i) {
-        const int kp = kb0 + i;
-        const bool valid = live && kp >= lo && kp <= pos && !(badmask[j & 1] >> (i >> 4) & 1u);
-        x[i] = valid ? x[i] * lscale : -INFINITY;
-        mx = fmaxf(mx, x[i]);
+        for (int i = 0; i < kKeys; ++i) {
+          x[i] *= lscale;
+          mx = fmaxf(mx, x[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) {
+          const int kp = kb0 + i;
+          const bool valid = live && kp >= lo && kp <= pos && !(bm >> (i >> 4) & 1u);
+          x[i] = valid ? x[i] * lscale : -INFINITY;
+          mx = fmaxf(mx, x[i]);
+        }
       }
       // PV of block j - 1 must be done before P is rewritten and O touched
       if (j >= 1 && !wait_w(odone, static_cast<uint32_t>((j - 1) & 1))) {
@@ -519,7 +546,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (issued[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>((issued[s] / S) & 1));
   }
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
