@@ -17,7 +17,8 @@
 //   warps 0-3 (softmax; thread r = row r = TMEM lane r): Q row r to f16,
 //     then per block the S row from TMEM, causal / window mask (skipped for
 //     blocks the whole row sees), online max with a lazy rescale of the O row
-//     in TMEM, P = 2^(x-m) as f16 into shared memory (the A operand of PV).
+//     in TMEM, P = 2^(x-m) as f16 into one of two shared-memory tiles (the A
+//     operand of PV), so the next block's softmax need not wait for this PV.
 // Every shared-memory operand is in the K-major 128-byte-swizzle layout:
 // 8-row groups of 1024 bytes, 128-byte rows of 64 f16, 16-byte chunk c of
 // row r at chunk c ^ (r % 8); wider K in further 64-column blocks of the
@@ -45,12 +46,13 @@ struct Layout {
   static constexpr size_t kBytes = static_cast<size_t>(kKeys) * DH * 2;
   static constexpr size_t vt = k + 2 * kBytes;             // V^T 2 x [DH][64] f16
   static constexpr size_t vtBytes = static_cast<size_t>(DH) * kKeys * 2;
-  static constexpr size_t p = vt + 2 * vtBytes;            // P   [128][64] f16
+  static constexpr size_t p = vt + 2 * vtBytes;            // P   2 x [128][64] f16
   static constexpr size_t pBytes = static_cast<size_t>(kRows) * kKeys * 2;
-  static constexpr size_t stage = p + pBytes;              // FP8 pages, kStagesTc stages
+  static constexpr size_t stage = p + 2 * pBytes;          // FP8 pages, kStagesTc stages
   static constexpr size_t bars = stage + static_cast<size_t>(kStagesTc) * kStage;
-  // barriers: full[3], empty[3], conv[2], sfull[2], pfull, odone, fin, qready
-  static constexpr int kBars = 2 * kStagesTc + 2 + 2 + 4;
+  // barriers: full[3], empty[3], conv[2], sfull[2], pfull[2], bufdone[2],
+  // odone, fin, qready
+  static constexpr int kBars = 2 * kStagesTc + 2 + 2 + 2 + 2 + 3;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
   // misc: tmem address, abort flag, page flags [3 stages][4 pages], issued[3],
   // masked pages of the blocks in the two f16 buffers [2]
@@ -166,10 +168,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint64_t* empty = bars + S;          // [S] FP8 stage converted (128 arrivals)
   uint64_t* conv = bars + 2 * S;       // [2] f16 K / V^T buffer b ready (128 arrivals)
   uint64_t* sfull = bars + 2 * S + 2;  // [2] S buffer b written (commit)
-  uint64_t* pfull = bars + 2 * S + 4;  // P of the block written (128 arrivals)
-  uint64_t* odone = bars + 2 * S + 5;  // PV of the block done (commit)
-  uint64_t* fin = bars + 2 * S + 6;    // every MMA done (commit)
-  uint64_t* qready = bars + 2 * S + 7; // the Q tile written (128 arrivals)
+  // Every waiter of a barrier below waits for a phase at most one behind the
+  // barrier's next completion (which needs the waiter's own progress), so a
+  // parity wait never aliases a phase two back.
+  uint64_t* pfull = bars + 2 * S + 4;    // [2] P buffer b written (128 arrivals)
+  uint64_t* bufdone = bars + 2 * S + 6;  // [2] PV of buffer b's block done (commit)
+  uint64_t* odone = bars + 2 * S + 8;    // PV of the block done (commit)
+  uint64_t* fin = bars + 2 * S + 9;      // every MMA done (commit)
+  uint64_t* qready = bars + 2 * S + 10;  // the Q tile written (128 arrivals)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lo::misc);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint32_t* pg_bad = const_cast<uint32_t*>(tmem_slot + 2);    // [S][4] page masked out
@@ -190,8 +196,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&conv[i], 128);
       mbar_init(&sfull[i], 1);
+      mbar_init(&pfull[i], 128);
+      mbar_init(&bufdone[i], 1);
     }
-    mbar_init(pfull, 128);
     mbar_init(odone, 1);
     mbar_init(fin, 1);
     mbar_init(qready, 128);
@@ -305,15 +312,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         if (j >= 1) {  // O += P_{j-1} V_{j-1}
           const int jp = j - 1;
-          ok = wait_or_abort(pfull, static_cast<uint32_t>(jp & 1), abort_flag);
+          ok = wait_or_abort(&pfull[jp & 1], static_cast<uint32_t>((jp >> 1) & 1), abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t b_v = sbase + Lo::vt + (jp & 1) * Lo::vtBytes;
+          const uint32_t a_pj = a_p + (jp & 1) * Lo::pBytes;
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)
-            mma_f16_ss(tm_o, sw128_desc(a_p + kk * 32), sw128_desc(b_v + kk * 32), id_pv,
+            mma_f16_ss(tm_o, sw128_desc(a_pj + kk * 32), sw128_desc(b_v + kk * 32), id_pv,
                        (jp > 0 || kk > 0) ? 1u : 0u);
           mma_commit(odone);
+          mma_commit(&bufdone[jp & 1]);  // K, V^T and P buffers jp % 2 free
         }
       }
       if (!ok) fail();
@@ -331,7 +340,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     auto convert = [&](int j) -> bool {
       const int s = j % S;
       if (!wait_w(&full[s], static_cast<uint32_t>((j / S) & 1))) return false;
-      if (j >= 2 && !wait_w(odone, static_cast<uint32_t>((j - 2) & 1)))
+      if (j >= 2 && !wait_w(&bufdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1)))
         return false;  // PV of block j - 2 (the buffer's last reader) is done
       // the stage's page flags, kept for the softmax of block j (the
       // producer rewrites the stage's flags once the stage is released)
@@ -472,14 +481,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mx = fmaxf(mx, x[i]);
         }
       }
-      // PV of block j - 1 must be done before P is rewritten and O touched
-      if (j >= 1 && !wait_w(odone, static_cast<uint32_t>((j - 1) & 1))) {
+      // P buffer j % 2 is free once PV of block j - 2 is done; O may be
+      // touched once PV of block j - 1 is (only a rescale needs that)
+      const bool grow = mx > m + kRescaleThreshold;
+      const bool rescale = __any_sync(kFull, grow);
+      if (rescale ? (j >= 1 && !wait_w(odone, static_cast<uint32_t>((j - 1) & 1)))
+                  : (j >= 2 && !wait_w(&bufdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1)))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool grow = mx > m + kRescaleThreshold;
-      if (__any_sync(kFull, grow)) {  // rescale O rows (warp-collective TMEM access)
+      if (rescale) {  // rescale O rows (warp-collective TMEM access)
         const float nm = grow ? mx : m;
         const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - nm);
         if (j >= 1) {
@@ -506,11 +518,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
 #pragma unroll
       for (int c = 0; c < kKeys / 8; ++c)
-        sts128(sbase + Lo::p + sw128_off(r, 8 * c, kRows), ph[4 * c], ph[4 * c + 1], ph[4 * c + 2],
+        sts128(sbase + Lo::p + (j & 1) * Lo::pBytes + sw128_off(r, 8 * c, kRows), ph[4 * c], ph[4 * c + 1], ph[4 * c + 2],
                ph[4 * c + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(pfull);
+      mbar_arrive(&pfull[j & 1]);
     }
     if (!ok) fail();
     // ---- epilogue: O row / l * sV -> bf16
