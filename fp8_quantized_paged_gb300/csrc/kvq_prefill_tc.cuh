@@ -381,16 +381,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           w[i] = ok ? lds32(stg + (4 + pg) * Lo::kPage8 + swz(page_off<C::kRow>(tr, 4 * a), C::kSwz))
                     : 0u;
         }
+        // dim 4a + dd, the lanes' dims in rotated order: rows 4a + dd of one
+        // store then cover all eight row phases of the swizzle, so the 32
+        // lanes' 16-byte chunks fall in distinct bank groups
 #pragma unroll
-        for (int d = 0; d < 4; d += 2) {  // dims 4a + d, 4a + d + 1
-          uint32_t lo_d[4], hi_d[4];
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t dd = static_cast<uint32_t>((k + (a >> 1)) & 3);
+          const uint32_t sel = dd | ((dd + 4) << 4);  // byte dd of tokens 2m and 2m + 1
+          uint32_t h[4];
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {  // tokens 2m, 2m + 1 of the 8
-            const uint32_t sel = static_cast<uint32_t>(d | ((4 + d) << 4) | ((d + 1) << 8) | ((5 + d) << 12));
-            fp8x4_to_f16x2x2<FMT>(prmt(w[2 * m], w[2 * m + 1], sel), lo_d[m], hi_d[m]);
-          }
-          sts128(vb + sw128_off(4 * a + d, 8 * g8, DH), lo_d[0], lo_d[1], lo_d[2], lo_d[3]);
-          sts128(vb + sw128_off(4 * a + d + 1, 8 * g8, DH), hi_d[0], hi_d[1], hi_d[2], hi_d[3]);
+          for (int m = 0; m < 4; ++m)
+            h[m] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(prmt(w[2 * m], w[2 * m + 1], sel)));
+          sts128(vb + sw128_off(4 * a + static_cast<int>(dd), 8 * g8, DH), h[0], h[1], h[2], h[3]);
         }
       }
       fence_proxy_async_smem();  // generic writes -> the tensor core's reads
@@ -469,7 +471,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (live && bm == 0u && kb0 >= lo && kb0 + kKeys - 1 <= pos) {  // the row sees the block
 #pragma unroll
         for (int i = 0; i < kKeys; ++i) {
-          x[i] *= lscale;
           mx = fmaxf(mx, x[i]);
         }
       } else {
@@ -477,12 +478,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int i = 0; i < kKeys; ++i) {
           const int kp = kb0 + i;
           const bool valid = live && kp >= lo && kp <= pos && !(bm >> (i >> 4) & 1u);
-          x[i] = valid ? x[i] * lscale : -INFINITY;
+          x[i] = valid ? x[i] : -INFINITY;
           mx = fmaxf(mx, x[i]);
         }
       }
       // P buffer j % 2 is free once PV of block j - 2 is done; O may be
       // touched once PV of block j - 1 is (only a rescale needs that)
+      // the logits are x * lscale (log2 units): the scale goes into the max
+      // and into the exponent's fused multiply-add
+      mx *= lscale;
       const bool grow = mx > m + kRescaleThreshold;
       const bool rescale = __any_sync(kFull, grow);
       if (rescale ? (j >= 1 && !wait_w(odone, static_cast<uint32_t>((j - 1) & 1)))
@@ -511,8 +515,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       uint32_t ph[kKeys / 2];
 #pragma unroll
       for (int i = 0; i < kKeys; i += 2) {
-        const float p0 = (x[i] == -INFINITY) ? 0.f : fast_exp2(x[i] - m);
-        const float p1 = (x[i + 1] == -INFINITY) ? 0.f : fast_exp2(x[i + 1] - m);
+        // m = -inf only while every key so far is masked (this block's too)
+        const float p0 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i], lscale, -m));
+        const float p1 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i + 1], lscale, -m));
         l += p0 + p1;
         ph[i / 2] = f32x2_to_f16x2(p0, p1);
       }
