@@ -32,7 +32,14 @@ namespace tc {
 
 constexpr int kRows = 128;      // query rows per CTA (MMA M)
 constexpr int kKeys = 64;       // tokens per key block (QK^T N, PV K)
-constexpr int kStagesTc = 3;    // FP8 page stages
+#ifndef KVQ_TC_STAGES
+#define KVQ_TC_STAGES 3
+#endif
+#ifndef KVQ_TC_BUFS
+#define KVQ_TC_BUFS 3
+#endif
+constexpr int kStagesTc = KVQ_TC_STAGES;  // FP8 page stages
+constexpr int kBufs = KVQ_TC_BUFS;        // f16 K / V^T buffers (converters run kBufs - 1 ahead)
 constexpr int kThreadsTc = 320; // warps 0-3 softmax, 4-7 convert, 8 producer, 9 MMA
 constexpr uint32_t kTmemCols = 256;
 
@@ -42,21 +49,21 @@ struct Layout {
   static constexpr int kStage = 8 * kPage8;                // 4 K pages + 4 V pages
   static constexpr size_t q = 0;                           // Q   [128][DH] f16
   static constexpr size_t qBytes = static_cast<size_t>(kRows) * DH * 2;
-  static constexpr size_t k = q + qBytes;                  // K   2 x [64][DH] f16
+  static constexpr size_t k = q + qBytes;                  // K   kBufs x [64][DH] f16
   static constexpr size_t kBytes = static_cast<size_t>(kKeys) * DH * 2;
-  static constexpr size_t vt = k + 2 * kBytes;             // V^T 2 x [DH][64] f16
+  static constexpr size_t vt = k + kBufs * kBytes;         // V^T kBufs x [DH][64] f16
   static constexpr size_t vtBytes = static_cast<size_t>(DH) * kKeys * 2;
-  static constexpr size_t p = vt + 2 * vtBytes;            // P   2 x [128][64] f16
+  static constexpr size_t p = vt + kBufs * vtBytes;        // P   2 x [128][64] f16
   static constexpr size_t pBytes = static_cast<size_t>(kRows) * kKeys * 2;
   static constexpr size_t stage = p + 2 * pBytes;          // FP8 pages, kStagesTc stages
   static constexpr size_t bars = stage + static_cast<size_t>(kStagesTc) * kStage;
-  // barriers: full[3], empty[3], conv[2], sfull[2], pfull[2], bufdone[2],
-  // odone, fin, qready
-  static constexpr int kBars = 2 * kStagesTc + 2 + 2 + 2 + 2 + 3;
+  // barriers: full[S], empty[S], conv[kBufs], kvdone[kBufs], sfull[2],
+  // pfull[2], pdone[2], odone, fin, qready
+  static constexpr int kBars = 2 * kStagesTc + 2 * kBufs + 6 + 3;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
-  // misc: tmem address, abort flag, page flags [3 stages][4 pages], issued[3],
-  // masked pages of the blocks in the two f16 buffers [2]
-  static constexpr size_t total = misc + 128 + 1024;
+  // misc: tmem address, abort flag, page flags [S stages][4 pages], issued[S],
+  // masked pages of the blocks in the f16 buffers [kBufs]
+  static constexpr size_t total = misc + 256 + 1024;
 };
 
 // Byte offset of f16 element (row, col) in a K-major 128-byte-swizzled tile
@@ -166,21 +173,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lo::bars);
   uint64_t* full = bars;               // [S] FP8 stage landed
   uint64_t* empty = bars + S;          // [S] FP8 stage converted (128 arrivals)
-  uint64_t* conv = bars + 2 * S;       // [2] f16 K / V^T buffer b ready (128 arrivals)
-  uint64_t* sfull = bars + 2 * S + 2;  // [2] S buffer b written (commit)
+  uint64_t* conv = bars + 2 * S;            // [kBufs] f16 K / V^T buffer b ready (128 arrivals)
+  uint64_t* kvdone = conv + kBufs;          // [kBufs] PV of buffer b's block done (commit)
+  uint64_t* sfull = kvdone + kBufs;         // [2] S buffer b written (commit)
   // Every waiter of a barrier below waits for a phase at most one behind the
   // barrier's next completion (which needs the waiter's own progress), so a
   // parity wait never aliases a phase two back.
-  uint64_t* pfull = bars + 2 * S + 4;    // [2] P buffer b written (128 arrivals)
-  uint64_t* bufdone = bars + 2 * S + 6;  // [2] PV of buffer b's block done (commit)
-  uint64_t* odone = bars + 2 * S + 8;    // PV of the block done (commit)
-  uint64_t* fin = bars + 2 * S + 9;      // every MMA done (commit)
-  uint64_t* qready = bars + 2 * S + 10;  // the Q tile written (128 arrivals)
+  uint64_t* pfull = sfull + 2;   // [2] P buffer b written (128 arrivals)
+  uint64_t* pdone = sfull + 4;   // [2] PV of P buffer b's block done (commit)
+  uint64_t* odone = sfull + 6;   // PV of the block done (commit)
+  uint64_t* fin = sfull + 7;     // every MMA done (commit)
+  uint64_t* qready = sfull + 8;  // the Q tile written (128 arrivals)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lo::misc);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint32_t* pg_bad = const_cast<uint32_t*>(tmem_slot + 2);    // [S][4] page masked out
   int32_t* issued = reinterpret_cast<int32_t*>(pg_bad + S * 4);  // [S] last block issued
-  volatile uint32_t* bufmask = reinterpret_cast<volatile uint32_t*>(issued + S);  // [2]
+  volatile uint32_t* bufmask = reinterpret_cast<volatile uint32_t*>(issued + S);  // [kBufs]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.z, gkv = blockIdx.y;
@@ -193,11 +201,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(&empty[i], 128);
       issued[i] = -1;
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kBufs; ++i) {
       mbar_init(&conv[i], 128);
+      mbar_init(&kvdone[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
       mbar_init(&pfull[i], 128);
-      mbar_init(&bufdone[i], 1);
+      mbar_init(&pdone[i], 1);
     }
     mbar_init(odone, 1);
     mbar_init(fin, 1);
@@ -297,10 +308,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bool ok = wait_or_abort(qready, 0u, abort_flag);
       for (int j = 0; j <= nblk && ok; ++j) {
         if (j < nblk) {  // S[j % 2] = Q K_j^T
-          ok = wait_or_abort(&conv[j & 1], static_cast<uint32_t>((j >> 1) & 1), abort_flag);
+          ok = wait_or_abort(&conv[j % kBufs], static_cast<uint32_t>((j / kBufs) & 1), abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t b_k = sbase + Lo::k + (j & 1) * Lo::kBytes;
+          const uint32_t b_k = sbase + Lo::k + (j % kBufs) * Lo::kBytes;
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const uint32_t off_a = (ks >> 2) * (kRows * 128) + (ks & 3) * 32;
@@ -315,14 +326,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           ok = wait_or_abort(&pfull[jp & 1], static_cast<uint32_t>((jp >> 1) & 1), abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t b_v = sbase + Lo::vt + (jp & 1) * Lo::vtBytes;
+          const uint32_t b_v = sbase + Lo::vt + (jp % kBufs) * Lo::vtBytes;
           const uint32_t a_pj = a_p + (jp & 1) * Lo::pBytes;
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)
             mma_f16_ss(tm_o, sw128_desc(a_pj + kk * 32), sw128_desc(b_v + kk * 32), id_pv,
                        (jp > 0 || kk > 0) ? 1u : 0u);
           mma_commit(odone);
-          mma_commit(&bufdone[jp & 1]);  // K, V^T and P buffers jp % 2 free
+          mma_commit(&kvdone[jp % kBufs]);  // K and V^T buffer jp % kBufs free
+          mma_commit(&pdone[jp & 1]);       // P buffer jp % 2 free
         }
       }
       if (!ok) fail();
@@ -335,22 +347,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     auto wait_w = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(kFull, wait_or_abort(bar, parity, abort_flag));
     };
-    uint32_t badmask[2] = {0u, 0u};  // masked-out pages of the block in buffer 0 / 1
     // Block j's FP8 pages -> f16 K (token rows) and V^T (dim rows), buffer j % 2.
     auto convert = [&](int j) -> bool {
       const int s = j % S;
       if (!wait_w(&full[s], static_cast<uint32_t>((j / S) & 1))) return false;
-      if (j >= 2 && !wait_w(&bufdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1)))
-        return false;  // PV of block j - 2 (the buffer's last reader) is done
+      if (j >= kBufs && !wait_w(&kvdone[j % kBufs], static_cast<uint32_t>((j / kBufs - 1) & 1)))
+        return false;  // PV of block j - kBufs (the buffer's last reader) is done
       // the stage's page flags, kept for the softmax of block j (the
       // producer rewrites the stage's flags once the stage is released)
-      badmask[j & 1] = (pg_bad[s * 4] ? 1u : 0u) | (pg_bad[s * 4 + 1] ? 2u : 0u) |
+      const uint32_t bmask = (pg_bad[s * 4] ? 1u : 0u) | (pg_bad[s * 4 + 1] ? 2u : 0u) |
                        (pg_bad[s * 4 + 2] ? 4u : 0u) | (pg_bad[s * 4 + 3] ? 8u : 0u);
       // for the softmax of block j (read after it waits for conv[j % 2])
-      if (ct == 0) bufmask[j & 1] = badmask[j & 1];
+      if (ct == 0) bufmask[j % kBufs] = bmask;
       const uint32_t stg = sbase + Lo::stage + s * Lo::kStage;
-      const uint32_t kb = sbase + Lo::k + (j & 1) * Lo::kBytes;
-      const uint32_t vb = sbase + Lo::vt + (j & 1) * Lo::vtBytes;
+      const uint32_t kb = sbase + Lo::k + (j % kBufs) * Lo::kBytes;
+      const uint32_t vb = sbase + Lo::vt + (j % kBufs) * Lo::vtBytes;
       const int tok_base = (p_begin + 4 * j) * kBS;
       // K: 16-byte chunk (token t, dims 16c .. 16c + 15) -> 32 bytes of f16
       constexpr int KCH = DH / 16;  // chunks per token row
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int t = e / KCH, c = e - t * KCH;
         const int pg = t >> 4, tr = t & 15;
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (!(badmask[j & 1] >> pg & 1u))
+        if (!(bmask >> pg & 1u))
           w = lds128(stg + pg * Lo::kPage8 + swz(page_off<C::kRow>(tr, 16 * c), C::kSwz));
         uint32_t h[8];
         fp8x4_to_f16x2x2<FMT>(w.x, h[0], h[1]);
@@ -377,7 +388,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int t = 8 * g8 + i, pg = t >> 4, tr = t & 15;
-          const bool ok = !(badmask[j & 1] >> pg & 1u) && tok_base + t < L;
+          const bool ok = !(bmask >> pg & 1u) && tok_base + t < L;
           w[i] = ok ? lds32(stg + (4 + pg) * Lo::kPage8 + swz(page_off<C::kRow>(tr, 4 * a), C::kSwz))
                     : 0u;
         }
@@ -396,7 +407,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
       fence_proxy_async_smem();  // generic writes -> the tensor core's reads
-      mbar_arrive(&conv[j & 1]);
+      mbar_arrive(&conv[j % kBufs]);
       mbar_arrive(&empty[s]);
       return true;
     };
@@ -444,12 +455,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     fence_proxy_async_smem();  // the Q tile -> the tensor core
     mbar_arrive(qready);
     for (int j = 0; j < nblk && ok; ++j) {
-      // the block's masked pages (the converters wrote them before conv[j % 2])
-      if (!wait_w(&conv[j & 1], static_cast<uint32_t>((j >> 1) & 1))) {
+      // the block's masked pages (the converters wrote them before conv[j % kBufs])
+      if (!wait_w(&conv[j % kBufs], static_cast<uint32_t>((j / kBufs) & 1))) {
         ok = false;
         break;
       }
-      const uint32_t bm = bufmask[j & 1];
+      const uint32_t bm = bufmask[j % kBufs];
       if (!wait_w(&sfull[j & 1], static_cast<uint32_t>((j >> 1) & 1))) {
         ok = false;
         break;
@@ -490,7 +501,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const bool grow = mx > m + kRescaleThreshold;
       const bool rescale = __any_sync(kFull, grow);
       if (rescale ? (j >= 1 && !wait_w(odone, static_cast<uint32_t>((j - 1) & 1)))
-                  : (j >= 2 && !wait_w(&bufdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1)))) {
+                  : (j >= 2 && !wait_w(&pdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1)))) {
         ok = false;
         break;
       }
