@@ -58,8 +58,8 @@ struct Layout {
   static constexpr size_t stage = p + 2 * pBytes;          // FP8 pages, kStagesTc stages
   static constexpr size_t bars = stage + static_cast<size_t>(kStagesTc) * kStage;
   // barriers: full[S], empty[S], conv[kBufs], kvdone[kBufs], sfull[2],
-  // pfull[2], pdone[2], odone, fin, qready
-  static constexpr int kBars = 2 * kStagesTc + 2 * kBufs + 6 + 3;
+  // pfull[2], pdone[2], fin, qready
+  static constexpr int kBars = 2 * kStagesTc + 2 * kBufs + 6 + 2;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
   // misc: tmem address, abort flag, page flags [S stages][4 pages], issued[S],
   // masked pages of the blocks in the f16 buffers [kBufs]
@@ -176,14 +176,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint64_t* conv = bars + 2 * S;            // [kBufs] f16 K / V^T buffer b ready (128 arrivals)
   uint64_t* kvdone = conv + kBufs;          // [kBufs] PV of buffer b's block done (commit)
   uint64_t* sfull = kvdone + kBufs;         // [2] S buffer b written (commit)
-  // Every waiter of a barrier below waits for a phase at most one behind the
-  // barrier's next completion (which needs the waiter's own progress), so a
-  // parity wait never aliases a phase two back.
   uint64_t* pfull = sfull + 2;   // [2] P buffer b written (128 arrivals)
   uint64_t* pdone = sfull + 4;   // [2] PV of P buffer b's block done (commit)
-  uint64_t* odone = sfull + 6;   // PV of the block done (commit)
-  uint64_t* fin = sfull + 7;     // every MMA done (commit)
-  uint64_t* qready = sfull + 8;  // the Q tile written (128 arrivals)
+  uint64_t* fin = sfull + 6;     // every MMA done (commit)
+  uint64_t* qready = sfull + 7;  // the Q tile written (128 arrivals)
+  // A parity wait for phase p of a barrier is sound only while the barrier
+  // has completed p or p + 1 phases.  Every waiter therefore waits each of
+  // its barriers' phases in order, never skipping one (so p - 1 is known
+  // complete), and a barrier's phase after p needs the waiter's own later
+  // progress.  Completion order is not assumed between MMAs that write
+  // different accumulators: QK^T of a block may finish before the PV issued
+  // ahead of it, so "S is ready" says nothing about earlier PVs.
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lo::misc);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint32_t* pg_bad = const_cast<uint32_t*>(tmem_slot + 2);    // [S][4] page masked out
@@ -210,7 +213,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(&pfull[i], 128);
       mbar_init(&pdone[i], 1);
     }
-    mbar_init(odone, 1);
     mbar_init(fin, 1);
     mbar_init(qready, 128);
     *abort_flag = 0u;
@@ -332,7 +334,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           for (int kk = 0; kk < kKeys / 16; ++kk)
             mma_f16_ss(tm_o, sw128_desc(a_pj + kk * 32), sw128_desc(b_v + kk * 32), id_pv,
                        (jp > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(odone);
           mma_commit(&kvdone[jp % kBufs]);  // K and V^T buffer jp % kBufs free
           mma_commit(&pdone[jp & 1]);       // P buffer jp % 2 free
         }
@@ -478,30 +479,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
       const int kb0 = (p_begin + 4 * j) * kBS;
-      float mx = -INFINITY;
+      // eight partial maxima: independent chains (max is exact in any order)
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
       if (live && bm == 0u && kb0 >= lo && kb0 + kKeys - 1 <= pos) {  // the row sees the block
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) {
-          mx = fmaxf(mx, x[i]);
-        }
+        for (int i = 0; i < kKeys; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
       } else {
 #pragma unroll
         for (int i = 0; i < kKeys; ++i) {
           const int kp = kb0 + i;
           const bool valid = live && kp >= lo && kp <= pos && !(bm >> (i >> 4) & 1u);
           x[i] = valid ? x[i] : -INFINITY;
-          mx = fmaxf(mx, x[i]);
+          mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
         }
       }
-      // P buffer j % 2 is free once PV of block j - 2 is done; O may be
-      // touched once PV of block j - 1 is (only a rescale needs that)
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // the logits are x * lscale (log2 units): the scale goes into the max
       // and into the exponent's fused multiply-add
       mx *= lscale;
       const bool grow = mx > m + kRescaleThreshold;
       const bool rescale = __any_sync(kFull, grow);
-      if (rescale ? (j >= 1 && !wait_w(odone, static_cast<uint32_t>((j - 1) & 1)))
-                  : (j >= 2 && !wait_w(&pdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1)))) {
+      bool wok = true;
+      if (j >= 2)  // PV(j - 2), the last reader of P buffer j % 2: every block
+        wok = wait_w(&pdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1));
+      if (wok && rescale && j >= 1)  // PV(j - 1) too before O is touched
+        wok = wait_w(&pdone[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1));
+      if (!wok) {
         ok = false;
         break;
       }
@@ -524,14 +530,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       // P row -> f16 into the A tile of PV
       uint32_t ph[kKeys / 2];
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of the block
 #pragma unroll
       for (int i = 0; i < kKeys; i += 2) {
         // m = -inf only while every key so far is masked (this block's too)
         const float p0 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i], lscale, -m));
         const float p1 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i + 1], lscale, -m));
-        l += p0 + p1;
+        l4[(i >> 1) & 3] += p0 + p1;
         ph[i / 2] = f32x2_to_f16x2(p0, p1);
       }
+      l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
 #pragma unroll
       for (int c = 0; c < kKeys / 8; ++c)
         sts128(sbase + Lo::p + (j & 1) * Lo::pBytes + sw128_off(r, 8 * c, kRows), ph[4 * c], ph[4 * c + 1], ph[4 * c + 2],
@@ -542,7 +550,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     if (!ok) fail();
     // ---- epilogue: O row / l * sV -> bf16
-    if (ok && wait_w(odone, static_cast<uint32_t>((nblk - 1) & 1))) {
+    // the last two PVs, in order on their barriers
+    bool eok = ok;
+    if (eok && nblk >= 2) eok = wait_w(&pdone[(nblk - 2) & 1], static_cast<uint32_t>(((nblk - 2) >> 1) & 1));
+    if (eok) eok = wait_w(&pdone[(nblk - 1) & 1], static_cast<uint32_t>(((nblk - 1) >> 1) & 1));
+    if (eok) {
       tc_fence_after();
       const float f = l > 0.f ? sv / l : 0.f;
       const bool store = live && guard(qrow < p.total_q * p.Hq, p.status, 24);
