@@ -366,7 +366,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int tok_base = (p_begin + 4 * j) * kBS;
       // K: 16-byte chunk (token t, dims 16c .. 16c + 15) -> 32 bytes of f16
       constexpr int KCH = DH / 16;  // chunks per token row
-      for (int e = ct; e < kKeys * KCH; e += 128) {
+      static_assert((kKeys * KCH) % 128 == 0 && ((kKeys / 8) * (DH / 4)) % 128 == 0, "whole passes");
+#pragma unroll
+      for (int it = 0; it < kKeys * KCH / 128; ++it) {  // fixed count: the loads go out together
+        const int e = ct + 128 * it;
         const int t = e / KCH, c = e - t * KCH;
         const int pg = t >> 4, tr = t & 15;
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -383,7 +386,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // V^T: tokens 8g .. 8g + 7 x dims 4a .. 4a + 3 -> four 16-byte chunks;
       // tokens past the sequence or in masked pages are zero (p = 0 would
       // not clear a NaN)
-      for (int e = ct; e < (kKeys / 8) * (DH / 4); e += 128) {
+#pragma unroll
+      for (int it = 0; it < (kKeys / 8) * (DH / 4) / 128; ++it) {
+        const int e = ct + 128 * it;
         const int g8 = e / (DH / 4), a = e - g8 * (DH / 4);
         uint32_t w[8];
 #pragma unroll
