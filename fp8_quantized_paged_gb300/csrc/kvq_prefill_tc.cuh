@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // producer rewrites the stage's flags once the stage is released)
       const uint32_t bmask = (pg_bad[s * 4] ? 1u : 0u) | (pg_bad[s * 4 + 1] ? 2u : 0u) |
                        (pg_bad[s * 4 + 2] ? 4u : 0u) | (pg_bad[s * 4 + 3] ? 8u : 0u);
-      // for the softmax of block j (read after it waits for conv[j % 2])
+      // for the softmax of block j (read after it waits for conv[j % kBufs])
       if (ct == 0) bufmask[j % kBufs] = bmask;
       const uint32_t stg = sbase + Lo::stage + s * Lo::kStage;
       const uint32_t kb = sbase + Lo::k + (j % kBufs) * Lo::kBytes;
