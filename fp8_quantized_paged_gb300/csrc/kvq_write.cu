@@ -118,14 +118,39 @@ KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, const HeadScale& h) {
 // CH in the warp; mask = those lanes): the largest finite magnitude of the
 // row over the format's largest finite value (binary32 division), or 1 when
 // that is 0.
-template <int FMT, int CH>
-KVQ_DEVI float row_scale(const uint4& a, const uint4& b, uint32_t mask) {
+template <int CH>
+KVQ_DEVI float row_amax(const uint4& a, const uint4& b, uint32_t mask) {
   const uint32_t m2 = max_mag16(0u, a, b);
   uint32_t am = max(m2 & 0xFFFFu, m2 >> 16) << 16;
 #pragma unroll
   for (int off = 1; off < CH; off <<= 1) am = max(am, __shfl_xor_sync(mask, am, off));
-  const float q = __fdiv_rn(__uint_as_float(am), FMT == KVQ_FMT_E4M3 ? 448.f : 57344.f);
+  return __uint_as_float(am);
+}
+
+template <int FMT>
+KVQ_DEVI float scale_of_amax(float amax) {
+  const float q = __fdiv_rn(amax, FMT == KVQ_FMT_E4M3 ? 448.f : 57344.f);
   return q > 0.f ? q : 1.f;
+}
+
+// The K and V row scales' division constants: one half of the row's lanes
+// derives K's, the other half V's (a correctly rounded division and
+// reciprocal each), and the halves swap them.
+template <int FMT, int CH>
+KVQ_DEVI void row_scales(const uint4 (&k)[2], const uint4 (&v)[2], uint32_t mask, HeadScale& hk,
+                         HeadScale& hv) {
+  const float ak = row_amax<CH>(k[0], k[1], mask), av = row_amax<CH>(v[0], v[1], mask);
+  const bool k_half = (threadIdx.x & (CH / 2)) == 0;
+  const HeadScale h = head_scale(scale_of_amax<FMT>(k_half ? ak : av));
+  HeadScale o;
+  o.s = __shfl_xor_sync(mask, h.s, CH / 2);
+  const float r = __shfl_xor_sync(mask, h.r2.x, CH / 2);
+  o.L2 = __shfl_xor_sync(mask, h.L2, CH / 2);
+  o.fast = o.s >= 0x1p-80f && o.s <= 0x1p80f;
+  o.r2 = make_float2(r, r);
+  o.ns2 = make_float2(-o.s, -o.s);
+  hk = k_half ? h : o;
+  hv = k_half ? o : h;
 }
 
 // One thread per 16-element chunk (h, c) of the (token, KV head) rows.  The
@@ -177,10 +202,8 @@ __global__ void __launch_bounds__(256, 3) write_kernel(const WriteParams p) {
     uint4 kn[2], vn[2];
     int64_t sn = -1;
     if (tn < p.num_tokens) load(tn, kn, vn, sn);
-    if (TS) {  // every lane of the row takes part, whatever its slot
-      hk = head_scale(row_scale<FMT, CH>(k[0], k[1], row_mask));
-      hv = head_scale(row_scale<FMT, CH>(v[0], v[1], row_mask));
-    }
+    if (TS)  // every lane of the row takes part, whatever its slot
+      row_scales<FMT, CH>(k, v, row_mask, hk, hv);
     if (slot >= p.capacity) {
       if (rem == 0) flag_status(p.status, KVQ_DEV_BAD_SLOT);
     } else if (slot >= 0) {  // a negative slot is a padding token
