@@ -4,8 +4,9 @@
 // One CTA per (sequence, KV head, tile of 128 query rows); a row is a (query
 // token, query head of the group) pair, so a tile holds 128 / G tokens.  The
 // keys stream in blocks of 64 tokens (4 pages):
-//   warp 8 (producer): TMA loads of the block's 4 K and 4 V FP8 pages into a
-//     3-stage ring (the decode's 128-byte-swizzled page boxes).
+//   warp 8 (producer): block ids 32 pages at a time (one per lane), TMA loads
+//     of each block's 4 K and 4 V FP8 pages into a 3-stage ring (the
+//     decode's 128-byte-swizzled page boxes).
 //   warps 4-7 (converters): each block's pages to f16 in shared memory, K as
 //     the B operand of QK^T (token-major) and V transposed (dim-major) as the
 //     B operand of PV, double-buffered.
@@ -266,41 +267,55 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      for (int j = 0; j < nblk && !*abort_flag; ++j) {
-        const int s = j % S;
-        if (j >= S && !wait_or_abort(&empty[s], static_cast<uint32_t>(((j / S) - 1) & 1), abort_flag)) {
-          fail();
-          break;
-        }
+    // The 32 lanes look up the block ids of 8 blocks (32 pages) at once, a
+    // group ahead; lane 0 takes each block's four by shuffle and issues its
+    // TMA loads.  (One lane looking them up in turn made the page stream wait
+    // four L2 round trips per block.)
+    int my_row = -1;  // cache row of page p_begin + 4 (j - j % 8) + lane, -1 if masked out
+    for (int j = 0; j < nblk; ++j) {
+      const int s = j % S;
+      if ((j & 7) == 0) {
+        const int col = p_begin + 4 * j + lane;
+        const bool in = col <= p_end;
+        int blk = -1;
+        if (in && guard(col >= 0 && col < p.max_blocks, p.status, 21))
+          blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + col);
+        bool bad = blk < 0 || blk >= p.num_blocks;
+        if (bad && in) flag_status(p.status, KVQ_DEV_BAD_BLOCK);
+        const int32_t row = ((bad ? 0 : blk) * p.Hkv + gkv) * kBS;
+        if (!bad && !guard(row >= 0 && row + kBS <= p.rows, p.status, 22)) bad = true;
+        my_row = bad ? -1 : row;
+      }
+      int rows[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rows[i] = __shfl_sync(kFull, my_row, 4 * (j & 7) + i);
+      const bool ok = j < S || __all_sync(kFull, wait_or_abort(&empty[s], static_cast<uint32_t>(((j / S) - 1) & 1), abort_flag));
+      if (__any_sync(kFull, !ok || *abort_flag)) {  // the same decision on every lane
+        if (lane == 0) fail();
+        break;
+      }
+      if (lane == 0) {
         uint32_t bytes = 0;
-        int rows[4];
+#pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int col = p_begin + 4 * j + i;
-          int blk = -1;
-          if (col <= p_end && guard(col >= 0 && col < p.max_blocks, p.status, 21))
-            blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + col);
-          bool bad = blk < 0 || blk >= p.num_blocks;
-          if (bad && col <= p_end) flag_status(p.status, KVQ_DEV_BAD_BLOCK);
-          int32_t row = ((bad ? 0 : blk) * p.Hkv + gkv) * kBS;
-          if (!bad && !guard(row >= 0 && row + kBS <= p.rows, p.status, 22)) bad = true;
-          rows[i] = bad ? -1 : row;
-          pg_bad[s * 4 + i] = bad ? 1u : 0u;
-          if (!bad) bytes += 2 * Lo::kPage8;
+          pg_bad[s * 4 + i] = rows[i] < 0 ? 1u : 0u;
+          if (rows[i] >= 0) bytes += 2 * Lo::kPage8;
         }
         issued[s] = j;
         if (bytes == 0) {  // nothing to load: complete the phase by hand
           mbar_arrive(&full[s]);
-          continue;
-        }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        uint8_t* dst = smem + Lo::stage + static_cast<size_t>(s) * Lo::kStage;
-        for (int i = 0; i < 4; ++i) {
-          if (rows[i] < 0) continue;
-          tma_load_2d(dst + i * Lo::kPage8, &tmk, 0, rows[i], &full[s]);
-          tma_load_2d(dst + (4 + i) * Lo::kPage8, &tmv, 0, rows[i], &full[s]);
+        } else {
+          mbar_arrive_expect_tx(&full[s], bytes);
+          uint8_t* dst = smem + Lo::stage + static_cast<size_t>(s) * Lo::kStage;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (rows[i] < 0) continue;
+            tma_load_2d(dst + i * Lo::kPage8, &tmk, 0, rows[i], &full[s]);
+            tma_load_2d(dst + (4 + i) * Lo::kPage8, &tmv, 0, rows[i], &full[s]);
+          }
         }
       }
+      __syncwarp();
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
