@@ -83,8 +83,10 @@ struct Cfg {
   // stream goes to warp pos % 4 and slot pos % kStages, so every slot is
   // used by one warp only, in order, and a parity wait can never alias a
   // phase two behind.
-  static constexpr int kStages =
+  static constexpr int kStagesFit =
       kConsumerWarps * (kRingBytes / (kConsumerWarps * kSlot) > 0 ? kRingBytes / (kConsumerWarps * kSlot) : 1);
+  // at most 64 (two ring slots per producer lane; a multiple of the warp count)
+  static constexpr int kStages = kStagesFit < 64 ? kStagesFit : 64 - 64 % kConsumerWarps;
   static constexpr uint32_t kSwz = (kRow >= 128) ? 7u : 3u;  // 128B or 64B swizzle
   // Pages a consumer warp works on at once.  Two (independent MMA chains)
   // measured slower: each warp then holds two ring slots before it starts.
