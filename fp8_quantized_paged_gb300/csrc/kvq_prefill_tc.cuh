@@ -8,8 +8,8 @@
 //     of each block's 4 K and 4 V FP8 pages into a 3-stage ring (the
 //     decode's 128-byte-swizzled page boxes).
 //   warps 4-7 (converters): each block's pages to f16 in shared memory, K as
-//     the B operand of QK^T (token-major) and V transposed (dim-major) as the
-//     B operand of PV, double-buffered.
+//     the B operand of QK^T and V as the MN-major B operand of PV, both
+//     token-major in the same layout, in kBufs buffers.
 //   warp 9 (MMA): allocates 256 TMEM columns (two 64-column S buffers and
 //     the dh-column O accumulator); one elected lane issues, per block,
 //     S = Q K^T (M = 128, N = 64, K = dh in steps of 16) and, once the block's
@@ -40,7 +40,7 @@ constexpr int kKeys = 64;       // tokens per key block (QK^T N, PV K)
 #define KVQ_TC_BUFS 3
 #endif
 constexpr int kStagesTc = KVQ_TC_STAGES;  // FP8 page stages
-constexpr int kBufs = KVQ_TC_BUFS;        // f16 K / V^T buffers (converters run kBufs - 1 ahead)
+constexpr int kBufs = KVQ_TC_BUFS;        // f16 K / V buffers (converters run kBufs - 1 ahead)
 constexpr int kThreadsTc = 320; // warps 0-3 softmax, 4-7 convert, 8 producer, 9 MMA
 constexpr uint32_t kTmemCols = 256;
 
@@ -52,7 +52,7 @@ struct Layout {
   static constexpr size_t qBytes = static_cast<size_t>(kRows) * DH * 2;
   static constexpr size_t k = q + qBytes;                  // K   kBufs x [64][DH] f16
   static constexpr size_t kBytes = static_cast<size_t>(kKeys) * DH * 2;
-  static constexpr size_t vt = k + kBufs * kBytes;         // V^T kBufs x [DH][64] f16
+  static constexpr size_t vt = k + kBufs * kBytes;         // V   kBufs x [64][DH] f16
   static constexpr size_t vtBytes = static_cast<size_t>(DH) * kKeys * 2;
   static constexpr size_t p = vt + kBufs * vtBytes;        // P   2 x [128][64] f16
   static constexpr size_t pBytes = static_cast<size_t>(kRows) * kKeys * 2;
@@ -81,6 +81,18 @@ KVQ_DEVI uint64_t sw128_desc(uint32_t saddr) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
+}
+
+// Descriptor of V as the MN-major B operand of PV (N = head dims along each
+// 128-byte row, K = tokens down the rows; the K tile's layout): the leading
+// byte offset steps to the next 64 dims (64 token rows on, 8192 bytes), the
+// stride byte offset to the next 8 tokens (1024 bytes).  (The other
+// assignment of the two strides gave wrong sums; this one reproduced the
+// transposed-V kernel's output bit for bit.)
+KVQ_DEVI uint64_t sw128_desc_mn(uint32_t saddr) {
+  constexpr uint64_t lbo = kKeys * 128, sbo = 1024;
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) |
+         (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
 }
 
 // Instruction descriptor of kind::f16: f32 accumulator, f16 A and B, both
@@ -174,7 +186,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lo::bars);
   uint64_t* full = bars;               // [S] FP8 stage landed
   uint64_t* empty = bars + S;          // [S] FP8 stage converted (128 arrivals)
-  uint64_t* conv = bars + 2 * S;            // [kBufs] f16 K / V^T buffer b ready (128 arrivals)
+  uint64_t* conv = bars + 2 * S;            // [kBufs] f16 K / V buffer b ready (128 arrivals)
   uint64_t* kvdone = conv + kBufs;          // [kBufs] PV of buffer b's block done (commit)
   uint64_t* sfull = kvdone + kBufs;         // [2] S buffer b written (commit)
   uint64_t* pfull = sfull + 2;   // [2] P buffer b written (128 arrivals)
@@ -346,10 +358,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const uint32_t b_v = sbase + Lo::vt + (jp % kBufs) * Lo::vtBytes;
           const uint32_t a_pj = a_p + (jp & 1) * Lo::pBytes;
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk)
-            mma_f16_ss(tm_o, sw128_desc(a_pj + kk * 32), sw128_desc(b_v + kk * 32), id_pv,
-                       (jp > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&kvdone[jp % kBufs]);  // K and V^T buffer jp % kBufs free
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            // 16 tokens = two 8-row groups of V; B is MN-major (bit 16)
+            mma_f16_ss(tm_o, sw128_desc(a_pj + kk * 32), sw128_desc_mn(b_v + kk * 2048),
+                       id_pv | (1u << 16), (jp > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&kvdone[jp % kBufs]);  // K and V buffer jp % kBufs free
           mma_commit(&pdone[jp & 1]);       // P buffer jp % 2 free
         }
       }
@@ -363,7 +377,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     auto wait_w = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(kFull, wait_or_abort(bar, parity, abort_flag));
     };
-    // Block j's FP8 pages -> f16 K (token rows) and V^T (dim rows), buffer j % 2.
+    // Block j's FP8 pages -> f16 K and V (token rows), buffer j % kBufs.
     auto convert = [&](int j) -> bool {
       const int s = j % S;
       if (!wait_w(&full[s], static_cast<uint32_t>((j / S) & 1))) return false;
@@ -398,34 +412,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         sts128(kb + sw128_off(t, 16 * c, kKeys), h[0], h[1], h[2], h[3]);
         sts128(kb + sw128_off(t, 16 * c + 8, kKeys), h[4], h[5], h[6], h[7]);
       }
-      // V^T: tokens 8g .. 8g + 7 x dims 4a .. 4a + 3 -> four 16-byte chunks;
-      // tokens past the sequence or in masked pages are zero (p = 0 would
-      // not clear a NaN)
+      // V token-major like K (the MN-major B operand of PV); tokens past the
+      // sequence or in masked pages are zero (p = 0 would not clear a NaN)
 #pragma unroll
-      for (int it = 0; it < (kKeys / 8) * (DH / 4) / 128; ++it) {
+      for (int it = 0; it < kKeys * KCH / 128; ++it) {
         const int e = ct + 128 * it;
-        const int g8 = e / (DH / 4), a = e - g8 * (DH / 4);
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int t = 8 * g8 + i, pg = t >> 4, tr = t & 15;
-          const bool ok = !(bmask >> pg & 1u) && tok_base + t < L;
-          w[i] = ok ? lds32(stg + (4 + pg) * Lo::kPage8 + swz(page_off<C::kRow>(tr, 4 * a), C::kSwz))
-                    : 0u;
-        }
-        // dim 4a + dd, the lanes' dims in rotated order: rows 4a + dd of one
-        // store then cover all eight row phases of the swizzle, so the 32
-        // lanes' 16-byte chunks fall in distinct bank groups
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t dd = static_cast<uint32_t>((k + (a >> 1)) & 3);
-          const uint32_t sel = dd | ((dd + 4) << 4);  // byte dd of tokens 2m and 2m + 1
-          uint32_t h[4];
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            h[m] = fp8x2_to_f16x2<FMT>(static_cast<uint16_t>(prmt(w[2 * m], w[2 * m + 1], sel)));
-          sts128(vb + sw128_off(4 * a + static_cast<int>(dd), 8 * g8, DH), h[0], h[1], h[2], h[3]);
-        }
+        const int t = e / KCH, c = e - t * KCH;
+        const int pg = t >> 4, tr = t & 15;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (!(bmask >> pg & 1u) && tok_base + t < L)
+          w = lds128(stg + (4 + pg) * Lo::kPage8 + swz(page_off<C::kRow>(tr, 16 * c), C::kSwz));
+        uint32_t h[8];
+        fp8x4_to_f16x2x2<FMT>(w.x, h[0], h[1]);
+        fp8x4_to_f16x2x2<FMT>(w.y, h[2], h[3]);
+        fp8x4_to_f16x2x2<FMT>(w.z, h[4], h[5]);
+        fp8x4_to_f16x2x2<FMT>(w.w, h[6], h[7]);
+        sts128(vb + sw128_off(t, 16 * c, kKeys), h[0], h[1], h[2], h[3]);
+        sts128(vb + sw128_off(t, 16 * c + 8, kKeys), h[4], h[5], h[6], h[7]);
       }
       fence_proxy_async_smem();  // generic writes -> the tensor core's reads
       mbar_arrive(&conv[j % kBufs]);
