@@ -116,12 +116,25 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The source files each recorded kernel is built from (its translation units
+# and the headers they include).
+KERNEL_SOURCES = {
+    "kvq_decode_attn": ["kvq_common.cuh", "kvq_host.h", "kvq_host.cu", "kvq_decode.cuh",
+                        "kvq_decode.cu", "kvq_decode_variant.cu"],
+    "kvq_write": ["kvq_common.cuh", "kvq_host.h", "kvq_host.cu", "kvq_write.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of one kernel's sources (and the C header), so that a recorded
+    capture goes stale only when that kernel's code changes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_quantized_paged_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    paths = [os.path.join(csrc, n) for n in KERNEL_SOURCES[kernel]]
+    paths.append(os.path.join(ROOT, "include", "kvq.h"))
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -132,9 +145,10 @@ def recorded_traffic(kernel: str):
     try:
         with open(path) as f:
             d = json.load(f)
-        if d.get("source_hash") != kernel_source_hash():
+        k = d["kernels"][kernel]
+        if k.get("source_hash") != kernel_source_hash(kernel):
             return None
-        return d["kernels"][kernel]["bytes_per_launch"]
+        return k["bytes_per_launch"]
     except Exception:
         return None
 
