@@ -22,6 +22,7 @@ import concurrent.futures as cf
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -125,16 +126,24 @@ KERNEL_SOURCES = {
 }
 
 
+def _header_code(path: str) -> bytes:
+    """The C header without its comments and blank lines: its documentation
+    does not change the kernels."""
+    with open(path) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).strip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln).encode()
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """Hash of one kernel's sources (and the C header), so that a recorded
-    capture goes stale only when that kernel's code changes."""
+    """Hash of one kernel's sources (and the C header's code), so that a
+    recorded capture goes stale only when that kernel's code changes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_quantized_paged_gb300", "csrc")
-    paths = [os.path.join(csrc, n) for n in KERNEL_SOURCES[kernel]]
-    paths.append(os.path.join(ROOT, "include", "kvq.h"))
-    for path in paths:
-        with open(path, "rb") as f:
-            h.update(os.path.basename(path).encode() + f.read())
+    for n in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    h.update(b"kvq.h" + _header_code(os.path.join(ROOT, "include", "kvq.h")))
     return h.hexdigest()[:16]
 
 

@@ -7,12 +7,12 @@
 // format's largest finite value, s = amax / fmt_max (448 for E4M3, 57344
 // for E5M2), so quantizing those tokens with s never saturates.
 //
-// Two kernels: a reduction, one thread per 16-element chunk of a (token,
+// Three kernels: a reduction, one thread per 16-element chunk of a (token,
 // head) row striding over tokens (integer max of the bf16 magnitudes, two at
-// a time), lanes of a head combined by shuffles and one atomicMax per head
+// a time, four tokens in flight), lanes of a head combined by shuffles and one atomicMax per head
 // and warp on the magnitude's bit pattern (non-negative floats order like
-// unsigned integers); then a finalize kernel that turns the maxima into
-// scales in place.
+// unsigned integers), after a one-block kernel has zeroed those words; then
+// a finalize kernel that turns the maxima into scales in place.
 #include "kvq_common.cuh"
 #include "kvq_host.h"
 
@@ -31,8 +31,11 @@ struct CalibParams {
   uint32_t* status;
 };
 
+constexpr int kCalibTokens = 4;     // tokens a thread has in flight per step
+constexpr int kCalibBlocksPerSM = 3;
+
 template <int DH>
-__global__ void __launch_bounds__(256, 4) calib_kernel(const CalibParams p) {
+__global__ void __launch_bounds__(256, kCalibBlocksPerSM) calib_kernel(const CalibParams p) {
   constexpr int CH = DH / 16;  // chunks of a head row; divides 32
   pdl_allow_next();
   pdl_wait();  // k, v may come from the previous kernel
@@ -43,12 +46,13 @@ __global__ void __launch_bounds__(256, 4) calib_kernel(const CalibParams p) {
   const int h = rem / CH;
   const int64_t tstride = nthreads / row_units;
   uint32_t mk = 0, mv = 0;  // two 16-bit magnitudes each
-  // two tokens per step, their eight 16-byte loads issued together
-  for (int64_t t = gtid / row_units; t < p.num_tokens; t += 2 * tstride) {
-    uint4 a[2][4];
-    bool ok[2];
+  // kCalibTokens tokens per step, their 16-byte loads issued together (the
+  // kernel is bound by load latency: the more bytes in flight the better)
+  for (int64_t t = gtid / row_units; t < p.num_tokens; t += kCalibTokens * tstride) {
+    uint4 a[kCalibTokens][4];
+    bool ok[kCalibTokens];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kCalibTokens; ++i) {
       const int64_t tt = t + i * tstride;
       const int64_t src = tt * p.token_stride + rem * 16;
       ok[i] = tt < p.num_tokens && guard(src >= 0 && src + 16 <= p.in_elems, p.status, 9);
@@ -61,7 +65,7 @@ __global__ void __launch_bounds__(256, 4) calib_kernel(const CalibParams p) {
       a[i][3] = ok[i] ? __ldcs(vs + 1) : z;
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kCalibTokens; ++i) {
       mk = max_mag16(mk, a[i][0], a[i][1]);
       mv = max_mag16(mv, a[i][2], a[i][3]);
     }
@@ -79,6 +83,16 @@ __global__ void __launch_bounds__(256, 4) calib_kernel(const CalibParams p) {
     if (ak) atomicMax(p.kmax + i, ak);
     if (av) atomicMax(p.vmax + i, av);
   }
+}
+
+// The maxima words (the scale arrays themselves) start at zero.  A kernel
+// rather than a memset, so that the chain of three launches overlaps by
+// programmatic dependent launch; it waits for the kernel before it, which
+// may still read the previous scales.
+__global__ void calib_zero(uint32_t* kbits, uint32_t* vbits, int n) {
+  pdl_allow_next();
+  pdl_wait();
+  for (int i = threadIdx.x; i < 2 * n; i += blockDim.x) (i < n ? kbits[i] : vbits[i - n]) = 0u;
 }
 
 // In place: scale = amax / fmt_max (binary32, round to nearest even); 1.0
@@ -116,10 +130,9 @@ extern "C" int kvq_calibrate_scales(const void* k, const void* v, int64_t token_
     return KVQ_ERR_ALIGN;
   const int n = scale_granularity == KVQ_SCALE_PER_HEAD ? num_kv_heads : 1;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(k_scale, 0, n * sizeof(float), s) != cudaSuccess ||
-      cudaMemsetAsync(v_scale, 0, n * sizeof(float), s) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = launch_pdl(calib_zero, dim3(1), dim3(256), 0, s,
+                             reinterpret_cast<uint32_t*>(k_scale), reinterpret_cast<uint32_t*>(v_scale), n);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
   if (num_tokens > 0) {
     CalibParams p;
     p.k = static_cast<const uint16_t*>(k);
@@ -133,7 +146,7 @@ extern "C" int kvq_calibrate_scales(const void* k, const void* v, int64_t token_
     p.in_elems = (num_tokens - 1) * token_stride + static_cast<int64_t>(num_kv_heads) * head_dim;
     p.status = dev_status;
     int grid = 0, block = 0;
-    token_row_shape(num_tokens, num_kv_heads * (head_dim / 16), 4, grid, block);
+    token_row_shape(num_tokens, num_kv_heads * (head_dim / 16), kCalibBlocksPerSM, grid, block);
     e = head_dim == 128 ? launch_pdl(calib_kernel<128>, dim3(grid), dim3(block), 0, s, p)
                         : launch_pdl(calib_kernel<64>, dim3(grid), dim3(block), 0, s, p);
     if (e != cudaSuccess) return KVQ_ERR_CUDA;

@@ -185,8 +185,8 @@ KVQ_API int kvq_write_token_head(const void* k, const void* v, int64_t token_str
  *                   tokens token_stride elements apart (as for kvq_write).
  *   k_scale,v_scale fp32 device arrays, outputs: 1 float for
  *                   KVQ_SCALE_PER_TENSOR, num_kv_heads for KVQ_SCALE_PER_HEAD
- *                   (4-byte aligned).  Overwritten on the stream (a memset,
- *                   then two kernels).
+ *                   (4-byte aligned).  Overwritten on the stream (three
+ *                   kernels: zero, reduce, divide).
  *   fmt             KVQ_FMT_E4M3 or KVQ_FMT_E5M2 (else KVQ_ERR_UNSUPPORTED).
  *   dev_status      optional; an internal guard bit if a load index fails.
  * num_tokens == 0 gives scales of 1.
