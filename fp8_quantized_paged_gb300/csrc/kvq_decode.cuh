@@ -73,6 +73,14 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazily rescale O
 constexpr int kPieceCost = KVQ_PIECE_COST;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
+// atomicAdd with acquire-release semantics at GPU scope (one instruction in
+// place of a fence, the add and a second fence).
+KVQ_DEVI uint32_t atom_add_acq_rel_gpu(uint32_t* addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 template <int FMT, int DH>
 struct Cfg {
   static constexpr int kElem = (FMT == KVQ_FMT_BF16) ? 2 : 1;
@@ -530,9 +538,13 @@ KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[
   using R = PageRegs<FMT, DH>;
   constexpr bool BF = FMT == KVQ_FMT_BF16;
   static_assert(!TS || NP == 1, "per-token scales take one page per step");
-  float s[NP][4];
+  // QK^T as two independent MMA chains (even and odd k-steps), summed at
+  // the end: half the dependent latency per page
+  float s[NP][4], s2[NP][4];
 #pragma unroll
-  for (int i = 0; i < NP; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+  for (int i = 0; i < NP; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[i][j] = s2[i][j] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < (QF8 ? DH / 32 : DH / 16); ++kk) {
 #pragma unroll
@@ -541,18 +553,22 @@ KVQ_DEVI void compute_pages(const PageRegs<FMT, DH> (&r)[NP], const int (&tok0)[
       if (QF8) {  // the FP8 codes themselves: dims 8kk .. 8kk + 7 of the lane's run
         a[0] = r[i].k0[2 * kk]; a[1] = r[i].k1[2 * kk];
         a[2] = r[i].k0[2 * kk + 1]; a[3] = r[i].k1[2 * kk + 1];
-        mma_fp8<FMT>(s[i], a, qb[kk][0], qb[kk][1]);
+        mma_fp8<FMT>((kk & 1) ? s2[i] : s[i], a, qb[kk][0], qb[kk][1]);
       } else if (BF) {
         a[0] = r[i].k0[2 * kk]; a[1] = r[i].k1[2 * kk];
         a[2] = r[i].k0[2 * kk + 1]; a[3] = r[i].k1[2 * kk + 1];
-        mma_bf16(s[i], a, qb[kk][0], qb[kk][1]);
+        mma_bf16((kk & 1) ? s2[i] : s[i], a, qb[kk][0], qb[kk][1]);
       } else {
         fp8x4_to_f16x2x2<FMT>(r[i].k0[kk], a[0], a[2]);
         fp8x4_to_f16x2x2<FMT>(r[i].k1[kk], a[1], a[3]);
-        mma_f16(s[i], a, qb[kk][0], qb[kk][1]);
+        mma_f16((kk & 1) ? s2[i] : s[i], a, qb[kk][0], qb[kk][1]);
       }
     }
   }
+#pragma unroll
+  for (int i = 0; i < NP; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[i][j] += s2[i][j];
   float x[4 * NP];
 #pragma unroll
   for (int i = 0; i < NP; ++i) {
@@ -1200,15 +1216,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         // all of its pieces and resets the segment's counter.
         const int64_t sigma = static_cast<int64_t>(b) * p.Hkv + gkv;
         // The barrier above orders every thread's partial stores before
-        // thread 0's fence and arrival (release); the arrival that completes
-        // the count is followed by a fence (acquire) and the barrier below.
+        // thread 0's arrival, an acquire-release atomic at GPU scope: its
+        // release publishes them, and for the arrival that completes the
+        // count its acquire (then the barrier below) makes every piece's
+        // stores visible to the merging threads.
         const int64_t c_lo = seg_lo;  // CTA holding the segment's first unit
         const int npieces = seg_n;
         if (ctid == 0) {
-          __threadfence();
-          const uint32_t prev = atomicAdd(p.ws_cnt + sigma, 1u);
+          const uint32_t prev = atom_add_acq_rel_gpu(p.ws_cnt + sigma, 1u);
           const bool last = prev + 1 == static_cast<uint32_t>(npieces);
-          if (last) __threadfence();
           merge_s[0] = last ? 1u : 0u;
         }
         consumer_bar();
