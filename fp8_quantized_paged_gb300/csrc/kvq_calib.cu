@@ -8,8 +8,8 @@
 // for E5M2), so quantizing those tokens with s never saturates.
 //
 // Three kernels: a reduction, one thread per 16-element chunk of a (token,
-// head) row striding over tokens (integer max of the bf16 magnitudes, two at
-// a time, four tokens in flight), lanes of a head combined by shuffles and one atomicMax per head
+// head) row striding over tokens (signed 16-bit max of keys of the bf16
+// magnitudes, two at a time, four tokens in flight), lanes of a head combined by shuffles and one atomicMax per head
 // and warp on the magnitude's bit pattern (non-negative floats order like
 // unsigned integers), after a one-block kernel has zeroed those words; then
 // a finalize kernel that turns the maxima into scales in place.
@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(256, kCalibBlocksPerSM) calib_kernel(const Cal
   const int rem = static_cast<int>(gtid % row_units);
   const int h = rem / CH;
   const int64_t tstride = nthreads / row_units;
-  uint32_t mk = 0, mv = 0;  // two 16-bit magnitudes each
+  uint32_t mk = kMagKey0, mv = kMagKey0;  // two 16-bit magnitude keys each
   // kCalibTokens tokens per step, their 16-byte loads issued together (the
   // kernel is bound by load latency: the more bytes in flight the better)
   for (int64_t t = gtid / row_units; t < p.num_tokens; t += kCalibTokens * tstride) {
@@ -66,13 +66,13 @@ __global__ void __launch_bounds__(256, kCalibBlocksPerSM) calib_kernel(const Cal
     }
 #pragma unroll
     for (int i = 0; i < kCalibTokens; ++i) {
-      mk = max_mag16(mk, a[i][0], a[i][1]);
-      mv = max_mag16(mv, a[i][2], a[i][3]);
+      mk = max_key16(mk, a[i][0], a[i][1]);
+      mv = max_key16(mv, a[i][2], a[i][3]);
     }
   }
   // every thread takes part (those without tokens contribute 0): the CH
   // lanes of a head are consecutive, as the block is a multiple of Hkv * CH
-  uint32_t ak = max(mk & 0xFFFFu, mk >> 16) << 16, av = max(mv & 0xFFFFu, mv >> 16) << 16;
+  uint32_t ak = mag_of_key16(mk), av = mag_of_key16(mv);
 #pragma unroll
   for (int off = 1; off < CH; off <<= 1) {
     ak = max(ak, __shfl_xor_sync(0xFFFFFFFFu, ak, off));

@@ -268,25 +268,37 @@ KVQ_DEVI float fast_exp2(float x) {
   return r;
 }
 
-// Largest finite magnitude among bf16 values, two at a time: the magnitudes
-// of the finite values of one word (NaN and +-inf count as 0), and the
-// running per-half maxima over sixteen values (non-negative bf16 order like
-// their unsigned bit patterns).
-KVQ_DEVI uint32_t finite_mag2(uint32_t w) {
-  const uint32_t m = w & 0x7FFF7FFFu;
-  return m & __vcmpltu2(m, 0x7F807F80u);
+// Largest finite magnitude among bf16 values, two at a time, as signed
+// 16-bit keys: key = (|x| bits) + 0x80 maps the finite magnitudes
+// (0 .. 0x7F7F) onto 0x80 .. 0x7FFF in their order and +-inf / NaN
+// (0x7F80 .. 0x7FFF) onto negative values, so a running max.s16x2 that
+// starts at the key of 0 skips them.  No carry crosses the halves (a key is
+// at most 0x807F).  mag_of_key16 turns the larger half back into the
+// magnitude's bits.
+constexpr uint32_t kMagKey0 = 0x00800080u;  // both halves: the key of 0
+
+KVQ_DEVI uint32_t max_s16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.s16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-KVQ_DEVI uint32_t max_mag16(uint32_t acc, const uint4& a, const uint4& b) {
-  acc = __vmaxu2(acc, finite_mag2(a.x));
-  acc = __vmaxu2(acc, finite_mag2(a.y));
-  acc = __vmaxu2(acc, finite_mag2(a.z));
-  acc = __vmaxu2(acc, finite_mag2(a.w));
-  acc = __vmaxu2(acc, finite_mag2(b.x));
-  acc = __vmaxu2(acc, finite_mag2(b.y));
-  acc = __vmaxu2(acc, finite_mag2(b.z));
-  acc = __vmaxu2(acc, finite_mag2(b.w));
+KVQ_DEVI uint32_t max_key16(uint32_t acc, const uint4& a, const uint4& b) {
+  acc = max_s16x2(acc, (a.x & 0x7FFF7FFFu) + kMagKey0);
+  acc = max_s16x2(acc, (a.y & 0x7FFF7FFFu) + kMagKey0);
+  acc = max_s16x2(acc, (a.z & 0x7FFF7FFFu) + kMagKey0);
+  acc = max_s16x2(acc, (a.w & 0x7FFF7FFFu) + kMagKey0);
+  acc = max_s16x2(acc, (b.x & 0x7FFF7FFFu) + kMagKey0);
+  acc = max_s16x2(acc, (b.y & 0x7FFF7FFFu) + kMagKey0);
+  acc = max_s16x2(acc, (b.z & 0x7FFF7FFFu) + kMagKey0);
+  acc = max_s16x2(acc, (b.w & 0x7FFF7FFFu) + kMagKey0);
   return acc;
+}
+
+// bf16 bits of the larger of the two halves' magnitudes (both halves of a
+// running max are keys >= 0x80), placed in the high half: a binary32 value
+KVQ_DEVI uint32_t mag_of_key16(uint32_t acc) {
+  return (max(acc & 0xFFFFu, acc >> 16) - 0x80u) << 16;
 }
 
 }  // namespace kvq

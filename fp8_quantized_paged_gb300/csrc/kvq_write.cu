@@ -120,8 +120,7 @@ KVQ_DEVI uint4 quantize16(const uint4& a, const uint4& b, const HeadScale& h) {
 // that is 0.
 template <int CH>
 KVQ_DEVI float row_amax(const uint4& a, const uint4& b, uint32_t mask) {
-  const uint32_t m2 = max_mag16(0u, a, b);
-  uint32_t am = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+  uint32_t am = mag_of_key16(max_key16(kMagKey0, a, b));
 #pragma unroll
   for (int off = 1; off < CH; off <<= 1) am = max(am, __shfl_xor_sync(mask, am, off));
   return __uint_as_float(am);
