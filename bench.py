@@ -74,6 +74,14 @@ def decode_bytes_token_head(n_tokens: int) -> int:
     return decode_bytes(n_tokens) - 2 * HKV * 4 + pages * HKV * 2 * BS * 4
 
 
+def unfused_bytes(n_tokens: int) -> int:
+    """The unfused path over a cache of n_tokens: the dequant reads the FP8 K
+    and V and writes them as bf16, the bf16 decode reads them again (plus the
+    decode's Q, O, tables and lengths)."""
+    kv = n_tokens * 2 * HKV * DH
+    return kv * (1 + 2) + decode_bytes(n_tokens) - n_tokens * 2 * HKV * DH * E + kv * 2 - 2 * HKV * 4
+
+
 PREFILL_Q = 2048  # prefix-hit prefill: the last 2048 tokens of the 32768 are queries
 
 
@@ -345,6 +353,22 @@ def run_gpu(args, rank, world, local_rank):
     g_prefill = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_prefill):
         prefills()
+    # The unfused path the fused decode replaces: every layer's FP8 caches
+    # dequantized into one bf16 scratch pair, then the bf16 decode over it.
+    kb = torch.empty(L[0]["kc"].shape, dtype=torch.bfloat16, device=dev)
+    vb = torch.empty(L[0]["vc"].shape, dtype=torch.bfloat16, device=dev)
+
+    def unfused():
+        for x in L:
+            kvq.kvq_dequant_cache(x["kc"], kb, x["ks"], PH, E4)
+            kvq.kvq_dequant_cache(x["vc"], vb, x["vs"], PH, E4)
+            kvq.kvq_decode_attn(x["q"], kb, vb, bt, sl, None, None, None, 0, kvq.KVQ_FMT_BF16, 0,
+                                ws, x["out"], dev_status=status)
+
+    unfused()
+    g_unfused = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_unfused):
+        unfused()
     # Per-(token, head) scales: every layer's write into the same caches with
     # its scale caches beside them, then the decodes reading them.  Timed
     # after the per-head graphs (it rewrites the caches).
@@ -406,6 +430,7 @@ def run_gpu(args, rank, world, local_rank):
         qf8_total = timed_replays(g_decode_qf8.replay, args.steps)
         calib_total = timed_replays(g_calib.replay, args.steps)
         prefill_total = timed_replays(g_prefill.replay, args.steps)
+        unfused_total = timed_replays(g_unfused.replay, args.steps)
         g_write_th.replay()  # the caches now hold per-token-head codes
         g_decode_th.replay()
         write_th_total = timed_replays(g_write_th.replay, args.steps)
@@ -421,6 +446,7 @@ def run_gpu(args, rank, world, local_rank):
     write_th_us = rank_max(write_th_total) / args.steps * 1e3 / LAYERS
     prefill_us = rank_max(prefill_total) / args.steps * 1e3 / 4
     decode_th_us = rank_max(decode_th_total) / args.steps * 1e3 / LAYERS
+    unfused_us = rank_max(unfused_total) / args.steps * 1e3 / LAYERS
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barrier,
@@ -496,11 +522,19 @@ def run_gpu(args, rank, world, local_rank):
         "roofline_decode": roof("kvq_decode_attn", d_ach, decode_bytes(SEQ)),
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
+        "decode_unfused_ablation": {
+            "us_per_layer": round(unfused_us, 2),
+            "vs_fused": round(unfused_us / (decode_ms * 1e3 / LAYERS), 3),
+            "hbm_bytes_per_layer": unfused_bytes(SEQ),
+            "what": "kvq_dequant_cache of K and V into one bf16 scratch cache, then the bf16 "
+                    "decode over it: FP8 read, bf16 written and read again (the scratch is "
+                    "about the L2's size, so part of the re-read hits L2)"},
         "timing": "CUDA graphs (32 writes, 32 decodes) replayed; events on the replay stream; "
                   "per-kernel figures from replaying each graph alone; decode_attn_cache_ready "
                   "replays the 32 decodes with KVQ_CACHE_READY, decode_attn_q_fp8 with "
                   "KVQ_Q_FP8, kv_calibrate 32 scale calibrations, kv_write_token_head and "
-                  "decode_attn_token_head the per-(token, head) scale mode (none part of the "
+                  "decode_attn_token_head the per-(token, head) scale mode, "
+                  "decode_unfused_ablation 32 dequant + bf16 decode layers (none part of the "
                   "step)",
         "clocks": clk.summary(),
     }
