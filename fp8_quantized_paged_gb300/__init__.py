@@ -101,9 +101,49 @@ def _len(t):
     return 0 if t is None else int(t.numel())
 
 
+def _need(t, where, name, size=None, dtype=None, contiguous=True, min_numel=None):
+    """The C ABI sees only a pointer: check what it cannot, before the call
+    (element type, dense layout, length), so that a wrong tensor raises here
+    instead of being read out of bounds on the device."""
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise KvqError(KVQ_ERR_ARG, f"{where}: {name} must be {dtype}, got {t.dtype}")
+    if size is not None and t.element_size() != size:
+        raise KvqError(KVQ_ERR_ARG, f"{where}: {name} must have {size}-byte elements, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise KvqError(KVQ_ERR_SHAPE, f"{where}: {name} must be contiguous")
+    if min_numel is not None and t.numel() < min_numel:
+        raise KvqError(KVQ_ERR_SHAPE, f"{where}: {name} holds {t.numel()} elements, needs {min_numel}")
+
+
+def _cache_size(fmt):
+    """Element size of a cache in format fmt (None for an unknown format,
+    which the library itself rejects)."""
+    return {KVQ_FMT_BF16: 2, KVQ_FMT_E4M3: 1, KVQ_FMT_E5M2: 1}.get(fmt)
+
+
+def _need_all(where, *specs):
+    """_need on every (tensor, name, ...) spec, then every tensor in CUDA memory."""
+    for spec in specs:
+        _need(spec[0], where, *spec[1:])
+    for spec in specs:
+        if spec[0] is not None and not spec[0].is_cuda:
+            raise KvqError(KVQ_ERR_ARG, f"{where}: {spec[1]} must be a CUDA tensor")
+
+
 # --------------------------------------------------------------------------
 # compute entry points (torch CUDA tensors)
 # --------------------------------------------------------------------------
+
+def _check_write_args(where, k, v, slot_mapping, k_cache, v_cache, fmt, dev_status, *more):
+    import torch
+    n = k.shape[0]
+    _need_all(where, (k, "k", 2, None, False), (v, "v", 2, None, False),
+              (slot_mapping, "slot_mapping", None, torch.int64, True, n),
+              (k_cache, "k_cache", _cache_size(fmt)), (v_cache, "v_cache", _cache_size(fmt)),
+              (dev_status, "dev_status", 4, None, True, 1), *more)
+
 
 def kvq_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, scale_granularity, fmt,
               dev_status=None, stream=None, token_stride=None) -> None:
@@ -116,6 +156,8 @@ def kvq_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, scale_gran
     nb, hkv2, bs, dh2 = k_cache.shape
     if (hkv2, dh2) != (hkv, dh) or v_cache.shape != k_cache.shape or tuple(v.shape) != (n, hkv, dh):
         raise KvqError(KVQ_ERR_SHAPE, "kvq_write")
+    _check_write_args("kvq_write", k, v, slot_mapping, k_cache, v_cache, fmt, dev_status,
+                      (k_scale, "k_scale", 4), (v_scale, "v_scale", 4))
     st = _lib.kvq_write(_ptr(k), _ptr(v), stride, _ptr(slot_mapping), n, hkv, dh, _ptr(k_cache),
                         _ptr(v_cache), nb, bs, _ptr(k_scale), _len(k_scale), _ptr(v_scale),
                         _len(v_scale), scale_granularity, fmt, _ptr(dev_status), _stream(stream))
@@ -137,6 +179,9 @@ def kvq_write_token_head(k, v, slot_mapping, k_cache, v_cache, k_scale_cache, v_
     for sc in (k_scale_cache, v_scale_cache):
         if tuple(sc.shape) != (nb, hkv, bs) or not sc.is_contiguous():
             raise KvqError(KVQ_ERR_SHAPE, "kvq_write_token_head")
+    _check_write_args("kvq_write_token_head", k, v, slot_mapping, k_cache, v_cache, fmt,
+                      dev_status, (k_scale_cache, "k_scale_cache", 4),
+                      (v_scale_cache, "v_scale_cache", 4))
     st = _lib.kvq_write_token_head(_ptr(k), _ptr(v), stride, _ptr(slot_mapping), n, hkv, dh,
                                    _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(k_scale_cache),
                                    _ptr(v_scale_cache), fmt, _ptr(dev_status), _stream(stream))
@@ -155,6 +200,9 @@ def kvq_calibrate_scales(k, v, k_scale, v_scale, scale_granularity, fmt, dev_sta
     want = hkv if scale_granularity == KVQ_SCALE_PER_HEAD else 1
     if k_scale.numel() != want or v_scale.numel() != want:
         raise KvqError(KVQ_ERR_SHAPE, "kvq_calibrate_scales")
+    _need_all("kvq_calibrate_scales", (k, "k", 2, None, False), (v, "v", 2, None, False),
+              (k_scale, "k_scale", 4), (v_scale, "v_scale", 4),
+              (dev_status, "dev_status", 4, None, True, 1))
     st = _lib.kvq_calibrate_scales(_ptr(k), _ptr(v), stride, n, hkv, dh, scale_granularity, fmt,
                                    _ptr(k_scale), _ptr(v_scale), _ptr(dev_status), _stream(stream))
     _check(st, "kvq_calibrate_scales")
@@ -165,6 +213,18 @@ def kvq_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, num
                                               num_sms))
 
 
+def _check_attn_args(where, q, k_cache, v_cache, block_tables, seq_lens, B, scales, fmt, out,
+                     dev_status, *more):
+    import torch
+    _need_all(where, (q, "q", 2), (out, "out", 2),
+              (k_cache, "k_cache", _cache_size(fmt)), (v_cache, "v_cache", _cache_size(fmt)),
+              (block_tables, "block_tables", None, torch.int32),
+              (seq_lens, "seq_lens", None, torch.int32, True, B),
+              (dev_status, "dev_status", 4, None, True, 1),
+              *[(sc, name, 4) for sc, name in zip(scales, ("q_scale", "k_scale", "v_scale"))],
+              *more)
+
+
 def kvq_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, q_scale, k_scale, v_scale,
                     scale_granularity, fmt, sliding_window, workspace, out, dev_status=None,
                     stream=None, flags=0) -> None:
@@ -173,11 +233,14 @@ def kvq_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, q_scale, k_scal
     nb, hkv, bs, dh2 = k_cache.shape
     if dh2 != dh or tuple(out.shape) != (B, hq, dh) or block_tables.shape[0] != B:
         raise KvqError(KVQ_ERR_SHAPE, "kvq_decode_attn")
+    _check_attn_args("kvq_decode_attn", q, k_cache, v_cache, block_tables, seq_lens, B,
+                     (q_scale, k_scale, v_scale), fmt, out, dev_status, (workspace, "workspace"))
     st = _lib.kvq_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                               block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, dh, nb, bs,
                               _ptr(q_scale), _len(q_scale), _ptr(k_scale), _len(k_scale),
                               _ptr(v_scale), _len(v_scale), scale_granularity, fmt,
-                              sliding_window, flags, _ptr(workspace), workspace.numel(), _ptr(out),
+                              sliding_window, flags, _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(out),
                               _ptr(dev_status), _stream(stream))
     _check(st, "kvq_decode_attn")
 
@@ -191,6 +254,8 @@ def kvq_decode_attn_static(q, k_cache, v_cache, block_tables, seq_lens, q_scale,
     nb, hkv, bs, dh2 = k_cache.shape
     if dh2 != dh or tuple(out.shape) != (B, hq, dh) or block_tables.shape[0] != B:
         raise KvqError(KVQ_ERR_SHAPE, "kvq_decode_attn_static")
+    _check_attn_args("kvq_decode_attn_static", q, k_cache, v_cache, block_tables, seq_lens, B,
+                     (q_scale, k_scale, v_scale), fmt, out, dev_status)
     st = _lib.kvq_decode_attn_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                      block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, dh, nb,
                                      bs, _ptr(q_scale), _len(q_scale), _ptr(k_scale),
@@ -212,6 +277,10 @@ def kvq_prefill_attn(q, cu_q_lens, max_q_len, k_cache, v_cache, block_tables, se
     if dh2 != dh or tuple(out.shape) != (total_q, hq, dh) or cu_q_lens.shape[0] != B + 1 or \
             block_tables.shape[0] != B:
         raise KvqError(KVQ_ERR_SHAPE, "kvq_prefill_attn")
+    import torch
+    _check_attn_args("kvq_prefill_attn", q, k_cache, v_cache, block_tables, seq_lens, B,
+                     (None, k_scale, v_scale), fmt, out, dev_status,
+                     (cu_q_lens, "cu_q_lens", None, torch.int32))
     st = _lib.kvq_prefill_attn(_ptr(q), _ptr(cu_q_lens), total_q, int(max_q_len), _ptr(k_cache),
                                _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
                                _ptr(seq_lens), B, hq, hkv, dh, nb, bs, _ptr(k_scale),
@@ -224,6 +293,8 @@ def kvq_dequant_cache(src, dst_bf16, scale, scale_granularity, fmt, stream=None)
     nb, hkv, bs, dh = src.shape
     if tuple(dst_bf16.shape) != tuple(src.shape):
         raise KvqError(KVQ_ERR_SHAPE, "kvq_dequant_cache")
+    _need_all("kvq_dequant_cache", (src, "src", _cache_size(fmt)), (dst_bf16, "dst_bf16", 2),
+              (scale, "scale", 4))
     st = _lib.kvq_dequant_cache(_ptr(src), _ptr(dst_bf16), nb, hkv, bs, dh, _ptr(scale),
                                 _len(scale), scale_granularity, fmt, _stream(stream))
     _check(st, "kvq_dequant_cache")
