@@ -5,7 +5,8 @@ j sits at position pos = L_b - n_b + j and attends causally to the cached
 tokens [lo, pos] (lo from the sliding window).  Pins: torch float64 SDPA with
 an explicit causal (and window) mask over the gathered K^/V^, the decode as
 the one-query case, causality (tokens after pos do not matter), chunk-split
-invariance, and refusal of more queries than cached tokens."""
+invariance, refusal of more queries than cached tokens, block-permutation
+invariance and a uniform V (every output is that row)."""
 import numpy as np
 import pytest
 import torch
@@ -119,3 +120,38 @@ def test_more_queries_than_tokens_is_refused():
     with pytest.raises(ValueError):
         oracle.prefill_attn(q, np.array([0, 11], np.int32), K, V, st.block_tables, st.seq_lens,
                             ks, vs, PER_TENSOR, E4M3)
+
+
+def test_block_permutation_invariance():
+    """Moving the physical blocks (and the block tables with them) changes
+    nothing: the queries see the cache only through the tables."""
+    r = np.random.default_rng(240)
+    lens, nq = [60, 35], [12, 35]
+    st, K, V, ks, vs = _case(r, lens, 8, 2, 64, E4M3, PER_HEAD)
+    q = bits(r.standard_normal((sum(nq), 8, 64)))
+    cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    base = oracle.prefill_attn(q, cu, K, V, st.block_tables, st.seq_lens, ks, vs, PER_HEAD, E4M3)
+    perm = r.permutation(st.num_blocks)          # new position of each block
+    K2, V2 = np.empty_like(K), np.empty_like(V)
+    K2[perm], V2[perm] = K, V
+    bt = np.where(st.block_tables >= 0, perm[np.maximum(st.block_tables, 0)], -1).astype(np.int32)
+    moved = oracle.prefill_attn(q, cu, K2, V2, bt, st.seq_lens, ks, vs, PER_HEAD, E4M3)
+    np.testing.assert_array_equal(moved, base)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_uniform_v_gives_that_row(fmt):
+    """With every cached V row equal, each query's output is that row's
+    dequantized value whatever the logits (the weights sum to one)."""
+    r = np.random.default_rng(250 + fmt)
+    lens, nq = [50, 20], [30, 20]
+    st, K, V, ks, vs = _case(r, lens, 4, 2, 64, fmt, PER_HEAD)
+    row = V[st.block_tables[0, 0], :, 0, :].copy()   # [Hkv][dh] codes of token 0
+    V[...] = row[None, :, None, :]
+    q = bits(r.standard_normal((sum(nq), 4, 64)) * 4)
+    cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    out = oracle.prefill_attn(q, cu, K, V, st.block_tables, st.seq_lens, ks, vs, PER_HEAD, fmt)
+    want = oracle.decode(fmt, row) * vs.astype(np.float64)[:, None]   # [Hkv][dh]
+    G = 2
+    np.testing.assert_allclose(out, np.broadcast_to(np.repeat(want, G, 0)[None], out.shape),
+                               rtol=1e-14, atol=0)
