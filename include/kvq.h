@@ -271,7 +271,9 @@ KVQ_API size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_
  *   dev_status      optional; KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN,
  *                   KVQ_DEV_WAIT_TIMEOUT.
  * Limits: num_seqs <= 4096; num_seqs * num_kv_heads <= 65536;
- * num_seqs * (max_blocks_per_seq + 16) * num_kv_heads < 2^31.
+ * num_seqs * (max_blocks_per_seq + 16) * num_kv_heads < 2^31;
+ * num_blocks * num_kv_heads * block_size < 2^31 (cache rows); beyond them
+ * KVQ_ERR_UNSUPPORTED.
  */
 KVQ_API int kvq_decode_attn(const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
