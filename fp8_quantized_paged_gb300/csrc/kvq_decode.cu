@@ -20,6 +20,26 @@ extern template int launch<KVQ_FMT_BF16, 128>(const DecodeParams&, const CUtenso
                                               const CUtensorMap&, cudaStream_t);
 extern template int launch<KVQ_FMT_BF16, 64>(const DecodeParams&, const CUtensorMap&,
                                              const CUtensorMap&, cudaStream_t);
+#ifndef KVQ_DECODE_TC
+#define KVQ_DECODE_TC 0
+#endif
+namespace dtc {
+// The tensor-core kernels of the FP8 caches at head size 128 (kvq_decode_tc.cu).
+template <int FMT>
+int launch_tc(const DecodeParams&, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+extern template int launch_tc<KVQ_FMT_E4M3>(const DecodeParams&, const CUtensorMap&,
+                                            const CUtensorMap&, cudaStream_t);
+extern template int launch_tc<KVQ_FMT_E5M2>(const DecodeParams&, const CUtensorMap&,
+                                            const CUtensorMap&, cudaStream_t);
+constexpr int kCtasPerSmTc = KVQ_DTC_CTAS_PER_SM;  // CTAs per SM of the tensor-core grid
+// The launch's shared memory fits the device (a large batch's plan may not).
+bool fits_tc(int G, int B, int Hkv);
+// Cluster size of the per-segment variant for this batch, or 0 (split).
+template <int FMT>
+int choose_clu(int G, int B, int Hkv, int max_blocks);
+extern template int choose_clu<KVQ_FMT_E4M3>(int, int, int, int);
+extern template int choose_clu<KVQ_FMT_E5M2>(int, int, int, int);
+}  // namespace dtc
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -126,7 +146,13 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   const int sms = device_sm_count();
   if (sms <= 0) return KVQ_ERR_CUDA;
   const int64_t max_units = static_cast<int64_t>(num_seqs) * max_blocks_per_seq * num_kv_heads;
-  const int P = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(kCtasPerSM) * sms, max_units));
+  // The tcgen05 kernel (one CTA per SM) serves FP8 caches at head size 128
+  // with per-tensor or per-head scales when KVQ_DECODE_TC is set at build
+  // time; by default every call runs the warp-MMA kernel, which times faster.
+  const bool use_tc = KVQ_DECODE_TC && fmt != KVQ_FMT_BF16 && head_dim == 128 && !token_scales &&
+                      dtc::fits_tc(G, num_seqs, num_kv_heads);
+  const int ctas = use_tc ? dtc::kCtasPerSmTc * sms : kCtasPerSM * sms;
+  const int P = static_cast<int>(std::min<int64_t>(ctas, max_units));
   const WsLayout wl = ws_layout(num_seqs, G, num_kv_heads, head_dim, kCtasPerSM * sms);
   if (workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
 
@@ -157,7 +183,7 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   p.out = static_cast<uint16_t*>(out);
   p.status = dev_status;
   p.rows = num_blocks * num_kv_heads * kBS;
-  p.n_slots = static_cast<int64_t>(kCtasPerSM) * sms + static_cast<int64_t>(num_seqs) * num_kv_heads;
+  p.n_slots = static_cast<int64_t>(kMaxHT) * kCtasPerSM * sms + static_cast<int64_t>(num_seqs) * num_kv_heads;
 
   CUtensorMap tk, tv;
   const uint64_t rows = static_cast<uint64_t>(num_blocks) * num_kv_heads * kBS;
@@ -165,6 +191,14 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
       !make_cache_map(&tv, v_cache, fmt, head_dim, rows))
     return KVQ_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  p.clu = 0;
+  if (use_tc) {
+    p.clu = fmt == KVQ_FMT_E4M3
+                ? dtc::choose_clu<KVQ_FMT_E4M3>(G, num_seqs, num_kv_heads, max_blocks_per_seq)
+                : dtc::choose_clu<KVQ_FMT_E5M2>(G, num_seqs, num_kv_heads, max_blocks_per_seq);
+    return fmt == KVQ_FMT_E4M3 ? dtc::launch_tc<KVQ_FMT_E4M3>(p, tk, tv, s)
+                               : dtc::launch_tc<KVQ_FMT_E5M2>(p, tk, tv, s);
+  }
   switch (fmt) {
     case KVQ_FMT_E4M3:
       return head_dim == 128 ? launch<KVQ_FMT_E4M3, 128>(p, tk, tv, s)

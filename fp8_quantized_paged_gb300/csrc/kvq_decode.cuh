@@ -54,6 +54,10 @@ namespace kvq {
 #ifndef KVQ_RING_KB
 #define KVQ_RING_KB 80
 #endif
+// CTAs per SM of the tensor-core decode (kvq_decode_tc.cuh)
+#ifndef KVQ_DTC_CTAS_PER_SM
+#define KVQ_DTC_CTAS_PER_SM 1
+#endif
 
 constexpr int kBS = 16;  // tokens per page (block_size)
 constexpr int kConsumerWarps = KVQ_CONSUMER_WARPS;
@@ -64,6 +68,7 @@ constexpr int kMaxSeqs = 4096;
 constexpr int kMaxGroup = 8;
 constexpr int kMaxKvHeads = 256;
 constexpr int kMaxSegments = 65536;  // num_seqs * num_kv_heads (counter table entries)
+constexpr int kMaxHT = 8;  // KV heads one tile of the whole-block decode covers
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazily rescale O
 #ifndef KVQ_PIECE_COST
 #define KVQ_PIECE_COST 16
@@ -158,6 +163,8 @@ struct DecodeParams {
   uint32_t* status;
   int64_t rows;     // rows of the cache tensor maps (num_blocks * Hkv * 16)
   int64_t n_slots;  // partial slots in the workspace
+  int clu;          // tensor-core decode: CTAs per cluster of the per-segment variant (0: split)
+  int ncl;          // whole-block decode, cluster variant: clusters per segment
 };
 
 // Workspace: a table of kMaxSegments uint32 arrival counters, one per
@@ -174,7 +181,9 @@ inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline WsLayout ws_layout(int B, int G, int Hkv, int DH, int P) {
   WsLayout w;
-  const size_t slots = static_cast<size_t>(P) + static_cast<size_t>(B) * Hkv;
+  // partial slots in units of one KV head's G query heads: a piece of the
+  // whole-block decode carries 8 KV heads
+  const size_t slots = static_cast<size_t>(kMaxHT) * P + static_cast<size_t>(B) * Hkv;
   w.cnt = 0;  // a fixed-size table, so every batch shape reuses the same zeroed counters
   w.ml = round256(sizeof(uint32_t) * static_cast<size_t>(kMaxSegments));
   w.o = w.ml + round256(slots * G * 2 * sizeof(float));
@@ -284,19 +293,23 @@ struct CostSplit {
 
 
 
-template <bool SCALED>
+// segs: segments per sequence (the KV heads, or groups of them that one
+// unit covers together).
+template <bool SCALED, int NT = kThreads>
 KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s,
-                         int32_t* vseq_off, float* sk_s, float* sv_s, int32_t* warp_tot) {
+                         int32_t* vseq_off, float* sk_s, float* sv_s, int32_t* warp_tot,
+                         int segs = -1) {
+  if (segs < 0) segs = p.Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int h = tid; h < p.Hkv; h += kThreads) {
-    sk_s[h] = SCALED ? __ldg(p.ks + (p.per_head ? h : 0)) : 1.f;
-    sv_s[h] = SCALED ? __ldg(p.vs + (p.per_head ? h : 0)) : 1.f;
+  for (int h = tid; h < p.Hkv; h += NT) {
+    sk_s[h] = SCALED ? p.ks[p.per_head ? h : 0] : 1.f;
+    sv_s[h] = SCALED ? p.vs[p.per_head ? h : 0] : 1.f;
   }
-  const int per = (p.B + kThreads - 1) / kThreads;
+  const int per = (p.B + NT - 1) / NT;
   const int b0 = tid * per, b1 = min(p.B, b0 + per);
   int local = 0, vlocal = 0;
   for (int b = b0; b < b1; ++b) {
-    const int raw = __ldg(p.seq_lens + b);
+    const int raw = p.seq_lens[b];
     if ((raw < 0 || raw > p.max_blocks * kBS) && blockIdx.x == 0)
       flag_status(p.status, KVQ_DEV_BAD_SEQLEN);
     const int L = (raw < 0 || raw > p.max_blocks * kBS) ? 0 : raw;
@@ -304,8 +317,8 @@ KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s
     len_s[b] = L;
     seq_off[b] = local;
     vseq_off[b] = vlocal;
-    local += pages * p.Hkv;
-    vlocal += pages > 0 ? (pages + kPieceCost) * p.Hkv : 0;
+    local += pages * segs;
+    vlocal += pages > 0 ? (pages + kPieceCost) * segs : 0;
   }
   auto scan = [&](int v, int& total) {  // block-wide exclusive scan
     int incl = v;
@@ -318,7 +331,7 @@ KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s
     __syncthreads();
     int base = 0;
     total = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
       base += w < warp ? warp_tot[w] : 0;
       total += warp_tot[w];
     }
