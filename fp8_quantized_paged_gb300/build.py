@@ -17,10 +17,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
-SOURCES = ["kvq_host.cu", "kvq_write.cu", "kvq_decode.cu", "kvq_decode_tc.cu", "kvq_static.cu",
-           "kvq_calib.cu", "kvq_prefill.cu", "kvq_decode_variant.cu"]
+SOURCES = ["kvq_host.cu", "kvq_write.cu", "kvq_decode.cu", "kvq_decode_tc.cu", "kvq_decode_blk.cu",
+           "kvq_static.cu", "kvq_calib.cu", "kvq_prefill.cu", "kvq_decode_variant.cu"]
 HEADERS = ["kvq_common.cuh", "kvq_host.h", "kvq_decode.cuh", "kvq_tc.cuh", "kvq_decode_tc.cuh",
-           "kvq_prefill_tc.cuh"]
+           "kvq_decode_blk.cuh", "kvq_prefill_tc.cuh"]
 # (object, source, defines): one object per translation unit, the decode
 # variants once per (format, head size); kvq_fmt 0 = BF16, 1 = E4M3, 2 = E5M2
 UNITS = [(os.path.splitext(s)[0], s, []) for s in SOURCES if s != "kvq_decode_variant.cu"] + [

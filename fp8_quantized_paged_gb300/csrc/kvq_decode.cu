@@ -23,6 +23,9 @@ extern template int launch<KVQ_FMT_BF16, 64>(const DecodeParams&, const CUtensor
 #ifndef KVQ_DECODE_TC
 #define KVQ_DECODE_TC 0
 #endif
+#ifndef KVQ_DECODE_BLK
+#define KVQ_DECODE_BLK 0
+#endif
 namespace dtc {
 // The tensor-core kernels of the FP8 caches at head size 128 (kvq_decode_tc.cu).
 template <int FMT>
@@ -41,6 +44,19 @@ extern template int choose_clu<KVQ_FMT_E4M3>(int, int, int, int);
 extern template int choose_clu<KVQ_FMT_E5M2>(int, int, int, int);
 }  // namespace dtc
 
+namespace dtb {
+// The whole-block tensor-core kernel (kvq_decode_blk.cu): FP8 caches, head
+// size 128, four query heads per KV head, KV heads in groups of eight.
+template <int FMT>
+int launch_blk(const DecodeParams&, const CUtensorMap&, const CUtensorMap&, bool, cudaStream_t);
+extern template int launch_blk<KVQ_FMT_E4M3>(const DecodeParams&, const CUtensorMap&,
+                                             const CUtensorMap&, bool, cudaStream_t);
+extern template int launch_blk<KVQ_FMT_E5M2>(const DecodeParams&, const CUtensorMap&,
+                                             const CUtensorMap&, bool, cudaStream_t);
+// The launch's shared memory (with the plan of B sequences) fits the device.
+bool fits_blk(int B, int Hkv);
+}  // namespace dtb
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -56,17 +72,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Tensor map of one cache tensor viewed as 2D: rows of head_dim elements
-// (num_blocks * Hkv * 16 rows).  One box is 16 rows by at most 128 bytes,
-// swizzled so that the decode kernel's fragment reads are free of bank
-// conflicts; a 256-byte bf16 row takes two boxes (x = 0 and x = 64).
-static bool make_cache_map(CUtensorMap* m, const void* base, int fmt, int dh, uint64_t rows) {
+// (num_blocks * Hkv * 16 rows).  One box is box_rows rows (a page of one KV
+// head, or a block of eight) by at most 128 bytes, swizzled so that the
+// decode kernels' fragment reads are free of bank conflicts and the tensor
+// cores read the 128-byte rows directly; a 256-byte bf16 row takes two
+// boxes (x = 0 and x = 64).
+static bool make_cache_map(CUtensorMap* m, const void* base, int fmt, int dh, uint64_t rows,
+                           int box_rows = kBS) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return false;
   const int elem = fmt == KVQ_FMT_BF16 ? 2 : 1;
   const int row_bytes = dh * elem;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(dh), rows};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes > 128 ? 128 / elem : dh), kBS};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes > 128 ? 128 / elem : dh),
+                             static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t es[2] = {1, 1};
   const CUtensorMapSwizzle sw =
       row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -151,8 +171,14 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   // time; by default every call runs the warp-MMA kernel, which times faster.
   const bool use_tc = KVQ_DECODE_TC && fmt != KVQ_FMT_BF16 && head_dim == 128 && !token_scales &&
                       dtc::fits_tc(G, num_seqs, num_kv_heads);
-  const int ctas = use_tc ? dtc::kCtasPerSmTc * sms : kCtasPerSM * sms;
-  const int P = static_cast<int>(std::min<int64_t>(ctas, max_units));
+  // With KVQ_DECODE_BLK set at build time, FP8 caches at head size 128 with
+  // per-tensor or per-head scales, four query heads per KV head and KV heads
+  // in groups of eight run on the whole-block tensor-core kernel (one CTA per
+  // SM); by default the warp-MMA kernel serves them, which times faster.
+  const bool use_blk = KVQ_DECODE_BLK && !use_tc && fmt != KVQ_FMT_BF16 && head_dim == 128 && !token_scales &&
+                       G == 4 && num_kv_heads % kMaxHT == 0 && dtb::fits_blk(num_seqs, num_kv_heads);
+  const int ctas = use_blk ? sms : (use_tc ? dtc::kCtasPerSmTc * sms : kCtasPerSM * sms);
+  const int P = static_cast<int>(std::min<int64_t>(ctas, use_blk ? max_units / kMaxHT : max_units));
   const WsLayout wl = ws_layout(num_seqs, G, num_kv_heads, head_dim, kCtasPerSM * sms);
   if (workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
 
@@ -185,13 +211,26 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   p.rows = num_blocks * num_kv_heads * kBS;
   p.n_slots = static_cast<int64_t>(kMaxHT) * kCtasPerSM * sms + static_cast<int64_t>(num_seqs) * num_kv_heads;
 
-  CUtensorMap tk, tv;
   const uint64_t rows = static_cast<uint64_t>(num_blocks) * num_kv_heads * kBS;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  p.clu = 0;
+  p.ncl = 0;
+  if (use_blk) {
+    CUtensorMap bk, bv;
+    if (!make_cache_map(&bk, k_cache, fmt, head_dim, rows, kMaxHT * kBS) ||
+        !make_cache_map(&bv, v_cache, fmt, head_dim, rows, kMaxHT * kBS))
+      return KVQ_ERR_CUDA;
+    // Few segments split over many CTAs each: merge them all at once after a
+    // grid barrier; otherwise the CTA completing a segment merges it.
+    const int64_t nseg = static_cast<int64_t>(num_seqs) * (num_kv_heads / kMaxHT);
+    const bool grid_merge = P > 8 * nseg;
+    return fmt == KVQ_FMT_E4M3 ? dtb::launch_blk<KVQ_FMT_E4M3>(p, bk, bv, grid_merge, s)
+                               : dtb::launch_blk<KVQ_FMT_E5M2>(p, bk, bv, grid_merge, s);
+  }
+  CUtensorMap tk, tv;
   if (!make_cache_map(&tk, k_cache, fmt, head_dim, rows) ||
       !make_cache_map(&tv, v_cache, fmt, head_dim, rows))
     return KVQ_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  p.clu = 0;
   if (use_tc) {
     p.clu = fmt == KVQ_FMT_E4M3
                 ? dtc::choose_clu<KVQ_FMT_E4M3>(G, num_seqs, num_kv_heads, max_blocks_per_seq)

@@ -261,13 +261,15 @@ KVQ_DEVI int seq_pages(int raw_len, int max_blocks, int window) {
 // a CTA of many short segments gets fewer pages.
 // Pages before cost position v (0 <= v <= V).
 // All offsets stay below 2^31 (checked on the host), so 32-bit division does.
-KVQ_DEVI int pages_before(const int32_t* seq_off, const int32_t* vseq_off, int B, int Hkv, int v) {
+// pc: the fixed cost of a piece (kPieceCost unless the kernel says otherwise).
+KVQ_DEVI int pages_before(const int32_t* seq_off, const int32_t* vseq_off, int B, int Hkv, int v,
+                          int pc = kPieceCost) {
   if (v >= vseq_off[B]) return seq_off[B];
   const int b = find_seq(vseq_off, B, v);
   const int pages = (seq_off[b + 1] - seq_off[b]) / Hkv;
   const int r = v - vseq_off[b];
-  const int g = r / (pages + kPieceCost);
-  const int in = r - g * (pages + kPieceCost) - kPieceCost;  // < 0: in the fixed cost
+  const int g = r / (pages + pc);
+  const int in = r - g * (pages + pc) - pc;  // < 0: in the fixed cost
   return seq_off[b] + g * pages + (in < 0 ? 0 : (in > pages ? pages : in));
 }
 
@@ -294,11 +296,11 @@ struct CostSplit {
 
 
 // segs: segments per sequence (the KV heads, or groups of them that one
-// unit covers together).
+// unit covers together); pc: the fixed cost of a piece in units.
 template <bool SCALED, int NT = kThreads>
 KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s,
                          int32_t* vseq_off, float* sk_s, float* sv_s, int32_t* warp_tot,
-                         int segs = -1) {
+                         int segs = -1, int pc = kPieceCost) {
   if (segs < 0) segs = p.Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int h = tid; h < p.Hkv; h += NT) {
@@ -318,7 +320,7 @@ KVQ_DEVI void build_plan(const DecodeParams& p, int32_t* seq_off, int32_t* len_s
     seq_off[b] = local;
     vseq_off[b] = vlocal;
     local += pages * segs;
-    vlocal += pages > 0 ? (pages + kPieceCost) * segs : 0;
+    vlocal += pages > 0 ? (pages + pc) * segs : 0;
   }
   auto scan = [&](int v, int& total) {  // block-wide exclusive scan
     int incl = v;
