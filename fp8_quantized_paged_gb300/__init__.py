@@ -41,6 +41,7 @@ SIGNATURES = {
     "kvq_decode_attn_static": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i64,
                                       _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                       _u32, _vp, _vp, _vp]),
+    "kvq_decode_static_reset": (_i32, [_vp]),
     "kvq_prefill_attn": (_i32, [_vp, _vp, _i64, _i32, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
                                 _i32, _i64, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _vp,
                                 _vp, _vp]),
@@ -263,6 +264,12 @@ def kvq_decode_attn_static(q, k_cache, v_cache, block_tables, seq_lens, q_scale,
                                      scale_granularity, fmt, sliding_window, flags, _ptr(out),
                                      _ptr(dev_status), _stream(stream))
     _check(st, "kvq_decode_attn_static")
+
+
+def kvq_decode_static_reset(stream=None) -> None:
+    """Clear the static scratch array's counters on the current device (after
+    a kvq_decode_attn_static call reported KVQ_DEV_WAIT_TIMEOUT)."""
+    _check(_lib.kvq_decode_static_reset(_stream(stream)), "kvq_decode_static_reset")
 
 
 def kvq_prefill_attn(q, cu_q_lens, max_q_len, k_cache, v_cache, block_tables, seq_lens,

@@ -44,23 +44,36 @@ def _inputs():
     return [os.path.join(CSRC, s) for s in SOURCES + HEADERS] + [inc, os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# The tests' timeout build: the same sources with the test hooks compiled in
+# (a decode whose producer withholds one page on request) and bounded waits
+# cut to 2^16 polls, in a directory of its own.  Never loaded by the package.
+TEST_LIB = os.path.join(BUILD, "test", "libkvq_test.so")
+TEST_DEFINES = ["-DKVQ_TEST_HOOKS", "-DKVQ_MAX_POLLS=65536u"]
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build_test_lib(force: bool = False, verbose: bool = False) -> str:
+    return build(force=force, verbose=verbose, extra=TEST_DEFINES, lib=TEST_LIB)
+
+
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          lib: str = LIB) -> str:
+    if not force and up_to_date(lib):
+        return lib
+    out_dir = os.path.dirname(lib)
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     extra = list(extra or [])
 
     def compile_one(unit):
         name, src, defines = unit
-        obj = os.path.join(BUILD, name + ".o")
+        obj = os.path.join(out_dir, name + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *defines, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
@@ -73,13 +86,13 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with cf.ThreadPoolExecutor(max_workers=min(len(UNITS), max(2, os.cpu_count() or 2))) as ex:
         objs = list(ex.map(compile_one, UNITS))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -18,7 +18,11 @@ namespace kvq {
 // Upper bound on the polls of one mbarrier wait (each poll is a try_wait
 // that itself suspends for a hardware-chosen time).  A wait that exhausts it
 // reports KVQ_DEV_WAIT_TIMEOUT instead of hanging.
-constexpr uint32_t kMaxPolls = 1u << 22;
+// (A build may lower it with -DKVQ_MAX_POLLS, as the tests' timeout build does.)
+#ifndef KVQ_MAX_POLLS
+#define KVQ_MAX_POLLS (1u << 22)
+#endif
+constexpr uint32_t kMaxPolls = KVQ_MAX_POLLS;
 
 KVQ_DEVI uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -2,6 +2,7 @@
 // checks, the plan of the launch (grid, workspace layout, tensor maps) and
 // the dispatch to the kernel variants, which kvq_decode_variant.cu compiles
 // once per cache format and head size.
+#include <atomic>
 #include <mutex>
 
 #include "kvq_decode.cuh"
@@ -97,9 +98,23 @@ static bool make_cache_map(CUtensorMap* m, const void* base, int fmt, int dh, ui
   return r == CUDA_SUCCESS;
 }
 
+#ifdef KVQ_TEST_HOOKS
+// Test builds only: the stream position CTA 0's producer withholds (-1: none).
+static std::atomic<int> g_withhold{-1};
+#endif
+
 }  // namespace kvq
 
 using namespace kvq;
+
+#ifdef KVQ_TEST_HOOKS
+// Test builds only (not declared in kvq.h): make the next decodes withhold the
+// copy of CTA 0's page at stream position `position` (-1: none), so that a
+// bounded wait runs out and reports KVQ_DEV_WAIT_TIMEOUT.
+extern "C" __attribute__((visibility("default"))) void kvq_test_withhold_page(int position) {
+  g_withhold.store(position);
+}
+#endif
 
 extern "C" size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                             int head_dim, int num_sms) {
@@ -215,6 +230,11 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   p.clu = 0;
   p.ncl = 0;
+#ifdef KVQ_TEST_HOOKS
+  p.withhold = g_withhold.load();
+#else
+  p.withhold = -1;
+#endif
   if (use_blk) {
     CUtensorMap bk, bv;
     if (!make_cache_map(&bk, k_cache, fmt, head_dim, rows, kMaxHT * kBS) ||

@@ -165,6 +165,8 @@ struct DecodeParams {
   int64_t n_slots;  // partial slots in the workspace
   int clu;          // tensor-core decode: CTAs per cluster of the per-segment variant (0: split)
   int ncl;          // whole-block decode, cluster variant: clusters per segment
+  int withhold;     // test builds (KVQ_TEST_HOOKS) only: CTA 0 never copies its page at this
+                    // stream position, so the wait for it runs out; -1 otherwise
 };
 
 // Workspace: a table of kMaxSegments uint32 arrival counters, one per
@@ -960,6 +962,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         }
         const int slot = lane + 32 * k;
         if (!mbar_test_wait(&empty[slot], par[k])) continue;
+#ifdef KVQ_TEST_HOOKS
+        if (blockIdx.x == 0 && q[k] == p.withhold) {
+          // Test builds only: this position's copy is never issued and its
+          // full barrier never completes, so the consumer's bounded wait on
+          // it runs out.  The slot is left for the aborting consumers.
+          done[k] = true;
+          progressed = true;
+          continue;
+        }
+#endif
         const bool bad = blk[k] < 0 || blk[k] >= p.num_blocks;
         if (bad) flag_status(p.status, KVQ_DEV_BAD_BLOCK);
         int32_t row = ((bad ? 0 : blk[k]) * p.Hkv + gg[k]) * kBS;
@@ -1097,12 +1109,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
       uint32_t cur_par = static_cast<uint32_t>(((pos_base + j0) / S) & 1);
       for (int j = j0; j < n; j += NP * kConsumerWarps) {
         int slot[NP];
+        uint32_t spar[NP];
         bool have[NP];
         bool ok = true;
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
           have[i] = j + i * kConsumerWarps < n;  // warp-uniform
           slot[i] = cur_slot;
+          spar[i] = cur_par;
           if (have[i] && ok && !aborted) ok = wait_or_abort(&full[cur_slot], cur_par, abort_flag);
           cur_slot += kConsumerWarps;
           if (cur_slot >= S) {
@@ -1151,11 +1165,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
           compute_pages<FMT, DH, NP, PK, QF8, TS>(pr, tok0, bad, g, t, p.G, qb, o, st, lscale0,
                                                   lscale1, lo, L, tsk, tsv);
         } else {
+          // Aborted: a slot goes back only once its copy has landed, so the
+          // producer never re-arms a slot whose copy is still in flight (it
+          // then idles, sees the abort and stops).
           __syncwarp();
           if (lane == 0) {
 #pragma unroll
             for (int i = 0; i < NP; ++i)
-              if (have[i]) mbar_arrive(&empty[slot[i]]);
+              if (have[i] && mbar_test_wait(&full[slot[i]], spar[i])) mbar_arrive(&empty[slot[i]]);
           }
         }
       }
@@ -1297,10 +1314,9 @@ static int launch_ts(const DecodeParams& p, const CUtensorMap& tk, const CUtenso
                      cudaStream_t s) {
   constexpr bool FP8 = FMT != KVQ_FMT_BF16;
   const size_t smem = smem_bytes<FMT, DH, TS>(p.G, p.P, p.B, p.Hkv);
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  // The kernels' attributes, set once per device (again after a failure).
+  static DeviceOnce once;
+  const bool configured = once.run(current_device(), [] {
     const int maxsmem = static_cast<int>(
         smem_bytes<FMT, DH, TS>(kMaxGroup, kCtasPerSM * device_sm_count(), kMaxSeqs, kMaxKvHeads));
     // The largest shared-memory carveout, so that two CTAs fit on every SM.
@@ -1315,9 +1331,9 @@ static int launch_ts(const DecodeParams& p, const CUtensorMap& tk, const CUtenso
     if constexpr (FP8)
       ok = ok && configure(decode_kernel<FMT, DH, true, FP8, TS>) &&
            configure(decode_kernel<FMT, DH, false, FP8, TS>);
-    if (!ok) return KVQ_ERR_CUDA;
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
-  }
+    return ok;
+  });
+  if (!configured) return KVQ_ERR_CUDA;
   const dim3 grid(p.P), block(kThreads);
   cudaError_t e;
   // the FP8-domain query variants exist for FP8 caches only (QF8 = FP8)

@@ -17,10 +17,9 @@ template int choose_clu<KVQ_FMT_E5M2>(int, int, int, int);
 
 bool fits_tc(int G, int B, int Hkv) {
   static size_t cap[64];
-  static std::once_flag once[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  std::call_once(once[dev], [dev] { cap[dev] = smem_optin(); });
+  static DeviceOnce once;  // the opt-in limit, looked up until a lookup succeeds
+  const int dev = current_device();
+  if (!once.run(dev, [dev] { return (cap[dev] = smem_optin()) > 0; })) return false;
   return smem_bytes_tc(G, B, Hkv) <= cap[dev];
 }
 }  // namespace dtc

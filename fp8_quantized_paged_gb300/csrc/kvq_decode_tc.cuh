@@ -1183,12 +1183,8 @@ static cudaError_t launch_tc_kernel(K kernel, int grid, int clu, size_t smem, cu
 
 template <int FMT>
 static bool ensure_configured() {
-  static std::once_flag once[64];
-  static bool ok_dev[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  std::call_once(once[dev], [dev] { ok_dev[dev] = configure_all_tc<FMT>(); });
-  return ok_dev[dev];
+  static DeviceOnce once;  // once per device, again after a failure
+  return once.run(current_device(), [] { return configure_all_tc<FMT>(); });
 }
 
 // Clusters of `clu` CTAs (8 <= clu <= 16, one CTA per SM) of the group-size
@@ -1198,12 +1194,11 @@ static bool ensure_configured() {
 // eight of 12.)
 template <int FMT>
 static int max_active_clusters(int clu, int gw) {
-  static std::once_flag once[64];
+  static DeviceOnce once;  // queried until a query succeeds
   static int n[64][2][kCluMax + 1];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || clu < 1 || clu > kCluMax)
-    return 0;
-  std::call_once(once[dev], [dev] {
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64 || clu < 1 || clu > kCluMax) return 0;
+  const bool queried = once.run(dev, [dev] {
     const bool ok = ensure_configured<FMT>();
     for (int gi = 0; gi < 2; ++gi)
       for (int c = 0; c <= kCluMax; ++c) {
@@ -1231,8 +1226,9 @@ static int max_active_clusters(int clu, int gw) {
         }
         n[dev][gi][c] = v;
       }
+    return ok;
   });
-  return n[dev][gw > 4 ? 1 : 0][clu];
+  return queried ? n[dev][gw > 4 ? 1 : 0][clu] : 0;
 }
 
 // The cluster size of the per-segment variant for a batch of B sequences

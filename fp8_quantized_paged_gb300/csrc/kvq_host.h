@@ -4,7 +4,47 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace kvq {
+
+// Per-device one-time setup (kernel attributes, symbol addresses) that is
+// recorded only once it succeeds: run(dev, f) calls f under a lock until f
+// returns true for that device, after which it returns true at once.  A
+// failure leaves the device unmarked and clears the CUDA error it left, so
+// the next call tries again.  Devices 0 .. 63.
+class DeviceOnce {
+ public:
+  template <typename F>
+  bool run(int dev, F&& f) {
+    if (dev < 0 || dev >= kMaxDev) return false;
+    if (done_[dev].load(std::memory_order_acquire)) return true;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return true;
+    if (!f()) {
+      cudaGetLastError();
+      return false;
+    }
+    done_[dev].store(true, std::memory_order_release);
+    return true;
+  }
+
+ private:
+  static constexpr int kMaxDev = 64;
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDev]{};
+};
+
+// The current device, or -1 (its error cleared) if there is none.
+inline int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return dev;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

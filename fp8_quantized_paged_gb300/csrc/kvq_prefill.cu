@@ -433,17 +433,16 @@ template <int FMT, int DH>
 static int prefill_launch(const PrefillParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                           cudaStream_t s) {
   constexpr size_t smem = PfSmem<FMT, DH>::total;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(prefill_kernel<FMT, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(prefill_kernel<FMT, DH>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
-  }
+  static DeviceOnce once;  // the kernel's attributes, once per device (again after a failure)
+  if (!once.run(current_device(), [] {
+        return cudaFuncSetAttribute(prefill_kernel<FMT, DH>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem)) == cudaSuccess &&
+               cudaFuncSetAttribute(prefill_kernel<FMT, DH>,
+                                    cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+      }))
+    return KVQ_ERR_CUDA;
   const dim3 grid(p.tiles, p.Hkv, p.B), block(kThreads);
   if (launch_pdl(prefill_kernel<FMT, DH>, grid, block, smem, s, p, tk, tv) != cudaSuccess)
     return KVQ_ERR_CUDA;
@@ -455,16 +454,13 @@ template <int FMT, int DH>
 static int prefill_tc_launch(PrefillParams p, int max_q_len, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t s) {
   constexpr size_t smem = tc::Layout<DH>::total;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(tc::prefill_tc_kernel<FMT, DH>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
-  }
+  static DeviceOnce once;  // the kernel's attribute, once per device (again after a failure)
+  if (!once.run(current_device(), [] {
+        return cudaFuncSetAttribute(tc::prefill_tc_kernel<FMT, DH>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem)) == cudaSuccess;
+      }))
+    return KVQ_ERR_CUDA;
   const int TQ = tc::kRows / p.G;
   p.tiles = (max_q_len + TQ - 1) / TQ;
   const dim3 grid(p.tiles, p.Hkv, p.B), block(tc::kThreadsTc);

@@ -16,9 +16,8 @@
 // with cudaGetSymbolAddress while that device is current, and keeps it.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/kvq.h"
+#include "kvq_host.h"
 
 namespace {
 
@@ -27,13 +26,19 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-std::once_flag g_once[kMaxDevices];
+kvq::DeviceOnce g_once;
 void* g_scratch_ptr[kMaxDevices];
 
-// Runs once per device, with that device current.
-void look_up_scratch(int dev) {
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_scratch) == cudaSuccess) g_scratch_ptr[dev] = p;
+// The array's device address on the current device dev, looked up (with dev
+// current) until a lookup succeeds; nullptr while none has.
+void* scratch_of(int dev) {
+  const bool ok = g_once.run(dev, [dev] {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return false;
+    g_scratch_ptr[dev] = p;
+    return true;
+  });
+  return ok ? g_scratch_ptr[dev] : nullptr;
 }
 
 }  // namespace
@@ -48,19 +53,32 @@ extern "C" int kvq_decode_attn_static(const void* q, const void* k_cache, const 
                                       int scale_granularity, int fmt, int sliding_window,
                                       unsigned flags, void* out, uint32_t* dev_status,
                                       kvq_stream_t stream) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+  const int dev = kvq::current_device();
+  if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
   // Sizes whose workspace would not fit the array are refused up front.
   const size_t need =
       kvq_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, 0);
   if (need > kScratchBytes) return KVQ_ERR_WORKSPACE;
-  std::call_once(g_once[dev], look_up_scratch, dev);
-  if (!g_scratch_ptr[dev]) return KVQ_ERR_CUDA;
+  void* scratch = scratch_of(dev);
+  if (!scratch) return KVQ_ERR_CUDA;
   // The array's counters are zero at load, and every completed call leaves
-  // them zero; the rest is overwritten before it is read.
+  // them zero (kvq_decode_static_reset clears them after a timeout); the
+  // rest is overwritten before it is read.
   return kvq_decode_attn(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                          num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
                          q_scale, q_scale_len, k_scale, k_scale_len, v_scale, v_scale_len,
-                         scale_granularity, fmt, sliding_window, flags, g_scratch_ptr[dev],
-                         kScratchBytes, out, dev_status, stream);
+                         scale_granularity, fmt, sliding_window, flags, scratch, kScratchBytes,
+                         out, dev_status, stream);
+}
+
+extern "C" int kvq_decode_static_reset(kvq_stream_t stream) {
+  const int dev = kvq::current_device();
+  if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+  void* scratch = scratch_of(dev);
+  if (!scratch) return KVQ_ERR_CUDA;
+  // The counter table at the array's start: an asynchronous fill, no allocation.
+  if (cudaMemsetAsync(scratch, 0, KVQ_WS_COUNTER_BYTES, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
 }

@@ -308,8 +308,9 @@ KVQ_API int kvq_decode_attn(const void* q, const void* k_cache, const void* v_ca
  * one array, which keeps the last call's contents.  Its counters start at
  * zero (device variables are zero-initialized when the library's device
  * code is loaded) and every completed call leaves them zero, so nothing
- * needs clearing unless a call reported KVQ_DEV_WAIT_TIMEOUT.  Calls on one
- * stream are ordered; calls that
+ * needs clearing unless a call reported KVQ_DEV_WAIT_TIMEOUT: then call
+ * kvq_decode_static_reset before the next kvq_decode_attn_static on that
+ * device.  Calls on one stream are ordered; calls that
  * may overlap on the GPU (different streams, or different host threads)
  * race on it: serialize them, or give each its own workspace through
  * kvq_decode_attn.
@@ -324,6 +325,18 @@ KVQ_API int kvq_decode_attn_static(const void* q, const void* k_cache, const voi
                                    int v_scale_len, int scale_granularity, int fmt,
                                    int sliding_window, unsigned flags, void* out,
                                    uint32_t* dev_status, kvq_stream_t stream);
+
+/*
+ * kvq_decode_static_reset -- clear the counter table (the first
+ * KVQ_WS_COUNTER_BYTES bytes) of the current device's static scratch array,
+ * asynchronously on `stream` (a cudaMemsetAsync on the array's own address:
+ * nothing is allocated).  Needed only after a kvq_decode_attn_static call
+ * reported KVQ_DEV_WAIT_TIMEOUT, whose aborted CTAs may leave counts behind;
+ * enqueue it on the stream of the next static call, or order the two.
+ * Returns KVQ_OK or KVQ_ERR_CUDA (no device, or the array's address could
+ * not be looked up).
+ */
+KVQ_API int kvq_decode_static_reset(kvq_stream_t stream);
 
 /*
  * kvq_prefill_attn -- prefill, chunked-prefill and prefix-hit attention over

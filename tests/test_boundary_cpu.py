@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol(kvq):
     assert declared == {"kvq_write", "kvq_decode_workspace_size", "kvq_decode_attn",
                         "kvq_decode_attn_static", "kvq_dequant_cache", "kvq_parse_dtype",
                         "kvq_layer_fmt", "kvq_status_string", "kvq_version", "kvq_calibrate_scales",
-                        "kvq_write_token_head", "kvq_prefill_attn"}
+                        "kvq_write_token_head", "kvq_prefill_attn", "kvq_decode_static_reset"}
     raw = ctypes.CDLL(kvq.LIB_PATH)
     for name in declared:
         assert getattr(raw, name) is not None
