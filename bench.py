@@ -103,7 +103,7 @@ WORKLOAD = {
                 "one decode step per layer",
     "layers": LAYERS, "seqs": 1, "seq_len": SEQ, "num_q_heads": HQ, "num_kv_heads": HKV,
     "head_dim": DH, "block_size": BS, "kv_cache_dtype": "fp8_e4m3", "scales": "per-head amax/448",
-    "l2": "inputs larger than L2 (about 6.3 GB moved per step)",
+    "l2": f"inputs larger than L2 (about {STEP_BYTES / 1e9:.1f} GB moved per step)",
 }
 
 
@@ -451,6 +451,12 @@ def run_gpu(args, rank, world, local_rank):
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barrier,
                   rank_max)
+    # ---- the other workloads' layers (not part of the step)
+    configs = None
+    if not args.no_configs:
+        with ClockSampler(torch.cuda.current_device()) as clk_cfg:
+            configs = run_configs(kvq, torch, dev, measured_peaks()[0], max(5, args.steps // 5))
+        configs["clocks"] = clk_cfg.summary()
 
     peak, peak_src = measured_peaks()
     write_launch_us = write_ms * 1e3 / LAYERS
@@ -538,6 +544,8 @@ def run_gpu(args, rank, world, local_rank):
                   "step)",
         "clocks": clk.summary(),
     }
+    if configs is not None:
+        res["configs"] = configs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(layers[0], st, args.cpu_seconds)
     return res
@@ -559,7 +567,7 @@ def run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barri
     bt = torch.from_numpy(st.block_tables).to(dev)
     sl = torch.from_numpy(st.seq_lens).to(dev)
     comp = torch.cuda.current_stream()
-    copy = torch.cuda.Stream(device=dev)
+    copies = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]  # layers alternate
     E4, PH = kvq.KVQ_FMT_E4M3, kvq.KVQ_SCALE_PER_HEAD
     ready = [torch.cuda.Event() for _ in range(LAYERS)]
     written = [torch.cuda.Event() for _ in range(LAYERS)]   # layer's K/V consumed
@@ -570,17 +578,22 @@ def run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barri
     h2d = sum(x.numel() * 2 for x in hk + hv + hq) + hslot.numel() * 8
     d2h = hout.numel() * 2
 
-    def step():
-        with torch.cuda.stream(copy):
-            copy.wait_event(written[LAYERS - 1])  # every write of the last step read the slots
+    def copy_in():
+        with torch.cuda.stream(copies[0]):
+            copies[0].wait_event(written[LAYERS - 1])  # every write of the last step read the slots
             slot_d.copy_(hslot, non_blocking=True)
-            for i, x in enumerate(L):
-                copy.wait_event(written[i])
+        for i, x in enumerate(L):
+            cs = copies[i % 2]
+            with torch.cuda.stream(cs):
+                cs.wait_event(written[i])
                 x["k"].view(torch.int16).copy_(hk[i], non_blocking=True)
                 x["v"].view(torch.int16).copy_(hv[i], non_blocking=True)
-                copy.wait_event(decoded[i])
+                cs.wait_event(decoded[i])
                 x["q"].view(torch.int16).copy_(hq[i], non_blocking=True)
-                ready[i].record(copy)
+                ready[i].record(cs)
+
+    def step():
+        copy_in()
         for i, x in enumerate(L):
             comp.wait_event(ready[i])
             kvq.kvq_write(x["k"], x["v"], slot_d, x["kc"], x["vc"], x["ks"], x["vs"], PH, E4,
@@ -603,9 +616,154 @@ def run_e2e(args, kvq, torch, dist, dev, st, layers, L, ws, status, world, barri
         step()
     torch.cuda.synchronize()
     el = rank_max(time.perf_counter() - t)
+    # the host-to-device copies alone (both streams, no kernels): the bound of this number
+    for _ in range(2):
+        copy_in()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(n):
+        copy_in()
+    torch.cuda.synchronize()
+    el_h2d = rank_max(time.perf_counter() - t)
     return {"value": round(whole_job_gbs(world, STEP_BYTES, el * 1e3 / n), 1), "unit": "GB/s",
             "ms_per_step": round(el * 1e3 / n, 3), "steps": n,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "copy_streams": len(copies),
+            "h2d_gbs": round(world * h2d * n / el_h2d / 1e9, 1),
+            "h2d_only_ms_per_step": round(el_h2d * 1e3 / n, 3),
+            "what": "per step: every layer's K/V/Q copied from pinned host memory on two copy "
+                    "streams (layers alternate), the 32 writes and 32 decodes, the outputs read "
+                    "back; h2d_gbs times the same copies alone"}
+
+
+# ---------------------------------------------------------------- the other workloads
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def layer_bytes(st, Hq, Hkv, dh, fmt, gran, window):
+    """Algorithmic bytes of one layer's write (every token) and decode (the
+    attended tokens of every sequence): as write_bytes / decode_bytes, with the
+    layer's own shape, cache element size and window."""
+    elem = 2 if fmt == workloads.BF16 else 1
+    lens = st.seq_lens.astype(np.int64)
+    B = len(lens)
+    lo = np.where((window > 0) & (lens > window), lens - window, 0)
+    attended = int((lens - lo).sum())
+    pages = int(((lens + BS - 1) // BS - lo // BS).sum())
+    tokens = int(lens.sum())
+    nsc = 0 if fmt == workloads.BF16 else 2 * (Hkv if gran == workloads.PER_HEAD else 1)
+    write = tokens * (2 * Hkv * dh * 2 + 2 * Hkv * dh * elem + 8)
+    decode = (attended * 2 * Hkv * dh * elem + B * Hq * dh * 2 * 2 + pages * 4 + B * 4 + nsc * 4)
+    return write, decode, attended, tokens
+
+
+def run_configs(kvq, torch, dev, peak, steps):
+    """Workloads 2, 3 (E4M3 and E5M2) and 5 (an FP8 layer and a bf16 window
+    layer), one layer each: its write of every token and its decode, each as a
+    CUDA graph over enough copies of the caches that one replay moves more than
+    4x the L2 (the next call never finds its pages in L2), replayed `steps`
+    times.  Lengths, block tables, shapes, formats and scale granularities are
+    the workloads'; the seeded bf16 K/V/Q are drawn on the device in each
+    workload's recipe (N(0,1); workload 2 with four x10 outlier channels per KV
+    head in K, workload 3 with per-head standard deviations log-uniform in
+    [0.1, 10]) and the scales computed from them by kvq_calibrate_scales
+    (amax / the format's largest value), since only timings come out of it."""
+    cases = [("workload2_llama8b_e4m3", 2, 0, workloads.E4M3),
+             ("workload3_per_head_e4m3", 3, 0, workloads.E4M3),
+             ("workload3_per_head_e5m2", 3, 0, workloads.E5M2),
+             ("workload5_fp8_layer", 5, 2, workloads.E4M3),
+             ("workload5_bf16_window_layer", 5, 3, workloads.E4M3)]
+    stream = torch.cuda.current_stream()
+    out = {}
+    structures = {}
+    for name, cfg, layer, fmt3 in cases:
+        st = structures.setdefault(cfg, workloads.structure(cfg))
+        Hq, Hkv, dh = workloads.SHAPES[cfg]
+        fmt, gran, window = workloads.layer_format(cfg, layer, fmt3)
+        wb, db, attended, tokens = layer_bytes(st, Hq, Hkv, dh, fmt, gran, window)
+        B = len(st.seq_lens)
+        elem = 2 if fmt == workloads.BF16 else 1
+        kv = tokens * 2 * Hkv * dh * elem
+        n = max(1, -(-4 * L2_BYTES // kv))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1000 * cfg + layer)
+        k = torch.randn((tokens, Hkv, dh), generator=gen, device=dev)
+        v = torch.randn((tokens, Hkv, dh), generator=gen, device=dev)
+        if cfg == 2:
+            for h in range(Hkv):
+                ch = torch.randperm(dh, generator=gen, device=dev)[:4]
+                k[:, h, ch] *= 10.0
+        elif cfg == 3:
+            lo_, hi_ = np.log(0.1), np.log(10.0)
+            sk = torch.exp(lo_ + (hi_ - lo_) * torch.rand(Hkv, generator=gen, device=dev))
+            sv = torch.exp(lo_ + (hi_ - lo_) * torch.rand(Hkv, generator=gen, device=dev))
+            k *= sk[None, :, None]
+            v *= sv[None, :, None]
+        k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+        q = torch.randn((B, Hq, dh), generator=gen, device=dev).to(torch.bfloat16)
+        nsc = Hkv if gran == workloads.PER_HEAD else 1
+        ks = torch.ones(nsc, dtype=torch.float32, device=dev)
+        vs = torch.ones(nsc, dtype=torch.float32, device=dev)
+        if fmt != workloads.BF16:
+            kvq.kvq_calibrate_scales(k, v, ks, vs, gran, fmt)
+        slots = torch.from_numpy(st.slot_mapping).to(dev)
+        bt = torch.from_numpy(st.block_tables).to(dev)
+        sl = torch.from_numpy(st.seq_lens).to(dev)
+        caches = [(kvq.new_cache(st.num_blocks, Hkv, dh, fmt, dev),
+                   kvq.new_cache(st.num_blocks, Hkv, dh, fmt, dev)) for _ in range(n)]
+        ws = kvq.new_workspace(B, Hq, Hkv, dh, dev)
+        o = torch.empty((B, Hq, dh), dtype=torch.bfloat16, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def writes():
+            for kc, vc in caches:
+                kvq.kvq_write(k, v, slots, kc, vc, ks, vs, gran, fmt, dev_status=status)
+
+        def decodes():
+            for kc, vc in caches:
+                kvq.kvq_decode_attn(q, kc, vc, bt, sl, None, ks, vs, gran, fmt, window, ws, o,
+                                    dev_status=status)
+
+        writes()
+        decodes()
+        torch.cuda.synchronize()
+        gw, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gw):
+            writes()
+        with torch.cuda.graph(gd):
+            decodes()
+
+        def timed(g):
+            for _ in range(3):
+                g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(steps):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) * 1e3 / (steps * n)
+
+        w_us, d_us = timed(gw), timed(gd)
+        assert int(status.item()) == 0, f"{name}: device status {int(status.item())}"
+        w_gbs, d_gbs = wb / (w_us * 1e-6) / 1e9, db / (d_us * 1e-6) / 1e9
+        out[name] = {
+            "workload": cfg, "layer": layer, "seqs": B, "tokens": tokens,
+            "cache": {workloads.E4M3: "fp8_e4m3", workloads.E5M2: "fp8_e5m2",
+                      workloads.BF16: "bf16"}[fmt],
+            "scales": "per-head" if gran == workloads.PER_HEAD else "per-tensor",
+            "window": window, "cache_copies_rotated": n,
+            "decode_attn": {"us_per_layer": round(d_us, 2), "gbs": round(d_gbs, 1),
+                            "frac_of_peak": round(d_gbs / peak, 4),
+                            "kv_tok_s": round(attended / (d_us * 1e-6), 0),
+                            "algorithmic_bytes": db},
+            "kv_write": {"us_per_layer": round(w_us, 2), "gbs": round(w_gbs, 1),
+                         "frac_of_peak": round(w_gbs / peak, 4),
+                         "tok_s": round(tokens / (w_us * 1e-6), 0), "algorithmic_bytes": wb}}
+        del caches, k, v, q, gw, gd
+        torch.cuda.synchronize()
+    return out
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -747,6 +905,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-layer lines of workloads 2, 3 and 5")
     ap.add_argument("--ncu-case", choices=["decode", "write", "decode_long", "write_long",
                                            "write_th_long", "decode_th_long", "calib_long",
                                            "prefill_long"], default=None,

@@ -22,6 +22,7 @@ KVQ_OK, KVQ_ERR_NULL, KVQ_ERR_SHAPE, KVQ_ERR_ALIGN = 0, -1, -2, -3
 KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA, KVQ_ERR_ARG = -4, -5, -6, -7
 KVQ_DEV_BAD_SLOT, KVQ_DEV_BAD_BLOCK, KVQ_DEV_BAD_SEQLEN, KVQ_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
 KVQ_DEV_INTERNAL = 16
+KVQ_DEV_BAD_QLEN = 32
 KVQ_Q_FP8 = 1
 KVQ_CACHE_READY = 2
 KVQ_STATIC_SCRATCH_BYTES = 16 << 20

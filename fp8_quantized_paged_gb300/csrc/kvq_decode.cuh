@@ -689,18 +689,39 @@ KVQ_DEVI void load_q_raw(const DecodeParams& p, int b, int gkv, int hq, int t,
   }
 }
 
+// For the FP8 caches the f16 operand is the query times a per-head power of
+// two 2^a (a returned; the four lanes of a head agree) that puts the head's
+// largest |q| in [2^14, 2^15): exact, and every bf16 query fits f16's range
+// (elements below 2^-38 of the head's largest lose bits as f16 subnormals).
+// The caller folds 2^-a into the head's logit scale.
 template <int FMT, int DH>
-KVQ_DEVI void q_fragments(const uint32_t (&w)[DH / 8], uint32_t (&qb)[DH / 16][2]) {
+KVQ_DEVI int q_fragments(const uint32_t (&w)[DH / 8], uint32_t (&qb)[DH / 16][2]) {
+  if (FMT == KVQ_FMT_BF16) {
 #pragma unroll
-  for (int kk = 0; kk < DH / 16; ++kk) {
-    if (FMT == KVQ_FMT_BF16) {
+    for (int kk = 0; kk < DH / 16; ++kk) {
       qb[kk][0] = w[2 * kk];
       qb[kk][1] = w[2 * kk + 1];
-    } else {
-      qb[kk][0] = f32x2_to_f16x2(bf16lo_to_f32(w[2 * kk]), bf16hi_to_f32(w[2 * kk]));
-      qb[kk][1] = f32x2_to_f16x2(bf16lo_to_f32(w[2 * kk + 1]), bf16hi_to_f32(w[2 * kk + 1]));
     }
+    return 0;
   }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < DH / 8; ++i)
+    amax = fmaxf(amax, fmaxf(fabsf(bf16lo_to_f32(w[i])), fabsf(bf16hi_to_f32(w[i]))));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));  // the head's 4 lanes (t = 0..3)
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+  int a = 0;
+  if (amax > 0.f) {  // finite bf16: exponent field 0 .. 254
+    a = 14 - (static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127);
+    a = a > 126 ? 126 : (a < -126 ? -126 : a);
+  }
+  const float sc = __int_as_float((a + 127) << 23);
+#pragma unroll
+  for (int kk = 0; kk < DH / 16; ++kk) {
+    qb[kk][0] = f32x2_to_f16x2(bf16lo_to_f32(w[2 * kk]) * sc, bf16hi_to_f32(w[2 * kk]) * sc);
+    qb[kk][1] = f32x2_to_f16x2(bf16lo_to_f32(w[2 * kk + 1]) * sc, bf16hi_to_f32(w[2 * kk + 1]) * sc);
+  }
+  return a;
 }
 
 // Q of the FP8-domain mode: the lane's DH/4 query values divided by the
@@ -1085,10 +1106,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSM)
         seg_lo = cost_split.cta_of(v_first);
         seg_n = cost_split.cta_of(v_first + pages - 1) - seg_lo + 1;
       }
-      if (QF8)
+      if (QF8) {
         q_fragments_fp8<FMT, DH>(qraw, sq, qb);
-      else
-        q_fragments<FMT, DH>(qraw, qb);
+      } else {
+        const int qa = q_fragments<FMT, DH>(qraw, qb);
+        if (FMT != KVQ_FMT_BF16) {  // 2^-a of each column's head (held by its lane t = 0)
+          const int a0 = __shfl_sync(kFull, qa, 4 * (PK ? ((2 * t) & 3) : 2 * t));
+          const int a1 = __shfl_sync(kFull, qa, 4 * (PK ? ((2 * t + 1) & 3) : 2 * t + 1));
+          lscale0 *= __int_as_float((127 - a0) << 23);
+          lscale1 *= __int_as_float((127 - a1) << 23);
+        }
+      }
       if (u + n < u1) {  // next piece's Q, in flight while this piece runs
         int nb, ng, npg, np0;
         piece_at(u + n, nb, ng, npg, np0);

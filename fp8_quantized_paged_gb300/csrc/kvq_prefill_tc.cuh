@@ -161,6 +161,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int q0 = __ldg(p.cu_q + b);
   const int n = __ldg(p.cu_q + b + 1) - q0;
   const int j0 = tile * TQ;
+  // a chunk longer than the grid covers (max_q_len): its later rows stay unwritten
+  if (blockIdx.x == 0 && gkv == 0 && tid == 0 && n > p.tiles * TQ)
+    flag_status(p.status, KVQ_DEV_BAD_QLEN);
   if (n <= 0 || j0 >= n) return;  // the whole CTA, before any tensor memory is taken
   const int j1 = min(n, j0 + TQ);
   const int L = __ldg(p.seq_lens + b);

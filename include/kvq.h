@@ -101,6 +101,9 @@ typedef enum {
 #define KVQ_DEV_WAIT_TIMEOUT 8u /* a bounded pipeline wait ran out; output is invalid */
 #define KVQ_DEV_INTERNAL 16u    /* an internal index guard failed (bits 16..31 name it); */
                                 /* the access was skipped and the output is invalid      */
+#define KVQ_DEV_BAD_QLEN 32u    /* prefill: a chunk longer than max_q_len; its rows past */
+                                /* the first max_q_len (rounded up to whole tiles) were  */
+                                /* not written                                           */
 
 /* Bytes at the start of every decode workspace that must be zero before the
  * first call: the arrival counters of kvq_decode_attn, one 32-bit word per
@@ -216,7 +219,9 @@ KVQ_API size_t kvq_decode_workspace_size(int num_seqs, int num_q_heads, int num_
  * head h reads KV head h / (num_q_heads / num_kv_heads).  Token t of
  * sequence b lives in block block_tables[b][t / block_size].
  *
- *   q               bf16 [num_seqs][num_q_heads][head_dim].
+ *   q               bf16 [num_seqs][num_q_heads][head_dim], any finite values
+ *                   (for the FP8 caches each head's query is scaled by a power
+ *                   of two, exactly, before its f16 tensor-core conversion).
  *   block_tables    int32 [num_seqs][max_blocks_per_seq]; entries past
  *                   ceil(L_b / block_size) are never read.
  *   seq_lens        int32 [num_seqs]; 0 gives a zero output row.
@@ -352,18 +357,22 @@ KVQ_API int kvq_decode_static_reset(kvq_stream_t stream);
  * The tokens before the chunk are a cached prefix (a prefix hit, or the
  * earlier chunks of a chunked prefill); n_b = 1 is the decode.
  *
- *   q               bf16 [num_q_tokens][num_q_heads][head_dim].
+ *   q               bf16 [num_q_tokens][num_q_heads][head_dim].  With the
+ *                   FP8 caches each element is converted to f16 for the MMAs:
+ *                   |q| must stay below 65504 (elements below 2^-24 flush to
+ *                   zero).
  *   cu_q_lens       int32 [num_seqs + 1], device: 0 = cu_q_lens[0] <= ... <=
  *                   cu_q_lens[num_seqs] = num_q_tokens.
- *   max_q_len       host: an upper bound of every n_b (sets the grid; rows
- *                   of a longer chunk would be left unwritten).
+ *   max_q_len       host: an upper bound of every n_b (sets the grid; the
+ *                   rows of a longer chunk past it are left unwritten and
+ *                   KVQ_DEV_BAD_QLEN is raised).
  *   block_tables, seq_lens, caches, scales, fmt   as for kvq_decode_attn
  *                   (KVQ_SCALE_PER_TENSOR or KVQ_SCALE_PER_HEAD).
  *   out             bf16 [num_q_tokens][num_q_heads][head_dim].
  *   dev_status      optional; KVQ_DEV_BAD_BLOCK (page masked out),
  *                   KVQ_DEV_BAD_SEQLEN (L_b < n_b or L_b > max_blocks_per_seq
  *                   * block_size: the sequence's rows are zero),
- *                   KVQ_DEV_WAIT_TIMEOUT.
+ *                   KVQ_DEV_BAD_QLEN (n_b > max_q_len), KVQ_DEV_WAIT_TIMEOUT.
  * Group size num_q_heads / num_kv_heads in {1, 2, 4, 8}; num_seqs <= 65535.
  * No workspace: one CTA per (sequence, KV head, 64 query rows), so a short
  * chunk over a long prefix keeps few SMs busy.

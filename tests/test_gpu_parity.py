@@ -796,3 +796,52 @@ def test_prefill_bad_lengths_and_empty(kvq):
     ref = oracle.prefill_attn(q[:10], cu[:2], K, V, lay.st.block_tables[:1], lay.st.seq_lens[:1],
                               lay.k_scale, lay.v_scale, lay.gran, lay.fmt)
     check_attention(got[:10], ref, "prefill valid sequence")
+
+
+@pytest.mark.parametrize("shift", [17, 40, -30])
+@pytest.mark.parametrize("G,dh,fmt", [(4, 64, workloads.E4M3), (8, 128, workloads.E5M2),
+                                      (2, 128, workloads.E4M3)])
+def test_decode_query_outside_f16_range(kvq, shift, G, dh, fmt):
+    """The query times 2^shift and the K scales times 2^-shift: the logits, and
+    so the attention, are unchanged, but |q| lies beyond f16's largest value
+    (shift 17, 40) or below its smallest normal (shift -30).  The FP8 decode
+    scales each head's query by a power of two before its f16 conversion."""
+    lay = _custom_layer([300, 77], Hq=2 * G, Hkv=2, dh=dh, fmt=fmt, seed=60 + G)
+    d = DeviceLayer(lay)
+    d.write()
+    K, V = oracle_caches(lay)
+    f = np.float32(2.0 ** shift)
+    lay.q[:] = workloads.f32_to_bf16_bits(workloads.bf16_bits_to_f32(lay.q) * f)  # exact
+    lay.k_scale[:] = (lay.k_scale / f).astype(np.float32)                        # exact
+    d.q.copy_(to_dev(lay.q))
+    d.ks.copy_(to_dev(lay.k_scale))
+    got = bf16_out_to_f64(d.decode())
+    assert d.status_word() == 0
+    check_attention(got, oracle_decode(lay, K, V), f"q x 2^{shift}")
+
+
+def test_prefill_chunk_longer_than_max_q_len(kvq):
+    """max_q_len below a chunk's length: the grid covers fewer rows than the
+    chunk has; the status says so, and the rows it covers are right."""
+    lay = _custom_layer([300, 40], Hq=8, Hkv=2, dh=128, seed=215)
+    r = np.random.default_rng(216)
+    cu = np.array([0, 200, 210], np.int32)
+    q = workloads.f32_to_bf16_bits(r.standard_normal((210, 8, 128)).astype(np.float32))
+    d = DeviceLayer(lay)
+    d.write()
+    out = torch.full((210, 8, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kvq.kvq_prefill_attn(to_dev(q), to_dev(cu), 10, d.kc, d.vc, d.bt, d.sl, d.ks, d.vs, lay.gran,
+                         lay.fmt, 0, out, dev_status=d.status)
+    assert d.status_word() & kvq.KVQ_DEV_BAD_QLEN
+    got = bf16_out_to_f64(out)
+    K, V = oracle_caches(lay)
+    ref = oracle.prefill_attn(q, cu, K, V, lay.st.block_tables, lay.st.seq_lens, lay.k_scale,
+                              lay.v_scale, lay.gran, lay.fmt)
+    check_attention(got[200:], ref[200:], "the short chunk")
+    check_attention(got[:10], ref[:10], "the long chunk's first rows")
+    # with max_q_len covering every chunk: no flag
+    d.status.zero_()
+    kvq.kvq_prefill_attn(to_dev(q), to_dev(cu), 200, d.kc, d.vc, d.bt, d.sl, d.ks, d.vs, lay.gran,
+                         lay.fmt, 0, out, dev_status=d.status)
+    assert d.status_word() == 0
+    check_attention(bf16_out_to_f64(out), ref, "covered")
