@@ -44,8 +44,8 @@ SIGNATURES = {
                                       _u32, _vp, _vp, _vp]),
     "kvq_decode_static_reset": (_i32, [_vp]),
     "kvq_prefill_attn": (_i32, [_vp, _vp, _i64, _i32, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
-                                _i32, _i64, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _vp,
-                                _vp, _vp]),
+                                _i32, _i64, _i32, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32,
+                                _i32, _u32, _vp, _vp, _vp]),
     "kvq_dequant_cache": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
     "kvq_calibrate_scales": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                     _vp]),
@@ -275,10 +275,12 @@ def kvq_decode_static_reset(stream=None) -> None:
 
 def kvq_prefill_attn(q, cu_q_lens, max_q_len, k_cache, v_cache, block_tables, seq_lens,
                      k_scale, v_scale, scale_granularity, fmt, sliding_window, out,
-                     dev_status=None, stream=None) -> None:
+                     dev_status=None, stream=None, q_scale=None, flags=0) -> None:
     """Prefill / prefix-hit attention: q bf16 [total_q][Hq][dh], cu_q_lens int32
     [B+1] (device), max_q_len a host bound of the per-sequence query counts;
-    the queries are each sequence's last tokens, attending causally."""
+    the queries are each sequence's last tokens, attending causally.  With
+    KVQ_SCALE_PER_TOKEN_HEAD, k_scale / v_scale are the scale caches of
+    kvq_write_token_head; flags=KVQ_Q_FP8 takes q_scale ([1] or [Hq])."""
     total_q, hq, dh = q.shape
     nb, hkv, bs, dh2 = k_cache.shape
     B = seq_lens.shape[0]
@@ -287,13 +289,14 @@ def kvq_prefill_attn(q, cu_q_lens, max_q_len, k_cache, v_cache, block_tables, se
         raise KvqError(KVQ_ERR_SHAPE, "kvq_prefill_attn")
     import torch
     _check_attn_args("kvq_prefill_attn", q, k_cache, v_cache, block_tables, seq_lens, B,
-                     (None, k_scale, v_scale), fmt, out, dev_status,
+                     (q_scale, k_scale, v_scale), fmt, out, dev_status,
                      (cu_q_lens, "cu_q_lens", None, torch.int32))
     st = _lib.kvq_prefill_attn(_ptr(q), _ptr(cu_q_lens), total_q, int(max_q_len), _ptr(k_cache),
                                _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
-                               _ptr(seq_lens), B, hq, hkv, dh, nb, bs, _ptr(k_scale),
-                               _len(k_scale), _ptr(v_scale), _len(v_scale), scale_granularity,
-                               fmt, sliding_window, _ptr(out), _ptr(dev_status), _stream(stream))
+                               _ptr(seq_lens), B, hq, hkv, dh, nb, bs, _ptr(q_scale),
+                               _len(q_scale), _ptr(k_scale), _len(k_scale), _ptr(v_scale),
+                               _len(v_scale), scale_granularity, fmt, sliding_window, flags,
+                               _ptr(out), _ptr(dev_status), _stream(stream))
     _check(st, "kvq_prefill_attn")
 
 

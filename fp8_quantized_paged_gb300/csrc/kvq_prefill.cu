@@ -43,9 +43,12 @@ struct PrefillParams {
   int64_t num_blocks;
   int64_t rows;              // rows of the cache tensor maps
   int64_t total_q;
-  const float* ks;
+  const float* ks;           // [1], [Hkv], or the scale caches [num_blocks][Hkv][16] (ts)
   const float* vs;
   int per_head;
+  int ts;                    // per-(token, KV head) scales
+  const float* qs;           // KVQ_Q_FP8: query scales, [1] or [Hq]; else null
+  int q_per_head;
   float logit_scale;         // log2(e) / sqrt(dh)
   uint16_t* out;             // [total_q][Hq][DH]
   uint32_t* status;
@@ -481,13 +484,21 @@ extern "C" int kvq_prefill_attn(const void* q, const int32_t* cu_q_lens, int64_t
                                 const int32_t* block_tables, int max_blocks_per_seq,
                                 const int32_t* seq_lens, int num_seqs, int num_q_heads,
                                 int num_kv_heads, int head_dim, int64_t num_blocks,
-                                int block_size, const float* k_scale, int k_scale_len,
-                                const float* v_scale, int v_scale_len, int scale_granularity,
-                                int fmt, int sliding_window, void* out, uint32_t* dev_status,
-                                kvq_stream_t stream) {
+                                int block_size, const float* q_scale, int q_scale_len,
+                                const float* k_scale, int k_scale_len, const float* v_scale,
+                                int v_scale_len, int scale_granularity, int fmt,
+                                int sliding_window, unsigned flags, void* out,
+                                uint32_t* dev_status, kvq_stream_t stream) {
   if (fmt < KVQ_FMT_BF16 || fmt > KVQ_FMT_E5M2) return KVQ_ERR_ARG;
-  if (scale_granularity != KVQ_SCALE_PER_TENSOR && scale_granularity != KVQ_SCALE_PER_HEAD)
+  if (scale_granularity != KVQ_SCALE_PER_TENSOR && scale_granularity != KVQ_SCALE_PER_HEAD &&
+      scale_granularity != KVQ_SCALE_PER_TOKEN_HEAD)
     return KVQ_ERR_ARG;
+  if (flags & ~KVQ_Q_FP8) return KVQ_ERR_ARG;
+  const bool token_scales = scale_granularity == KVQ_SCALE_PER_TOKEN_HEAD;
+  const bool q_fp8 = (flags & KVQ_Q_FP8) != 0;
+  // per-(token, head) scales and the FP8-domain query exist for the FP8 caches only
+  if ((token_scales || q_fp8) && fmt == KVQ_FMT_BF16) return KVQ_ERR_ARG;
+  if (q_fp8 && !q_scale) return KVQ_ERR_NULL;
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || sliding_window < 0 || num_q_tokens < 0 || max_q_len < 0)
     return KVQ_ERR_ARG;
@@ -509,9 +520,12 @@ extern "C" int kvq_prefill_attn(const void* q, const int32_t* cu_q_lens, int64_t
     return KVQ_ERR_ALIGN;
   if (fmt != KVQ_FMT_BF16) {
     if (!k_scale || !v_scale) return KVQ_ERR_NULL;
-    const int want = scale_granularity == KVQ_SCALE_PER_HEAD ? num_kv_heads : 1;
+    const int64_t want = token_scales ? num_blocks * num_kv_heads * kBS
+                                      : (scale_granularity == KVQ_SCALE_PER_HEAD ? num_kv_heads : 1);
     if (k_scale_len != want || v_scale_len != want) return KVQ_ERR_SHAPE;
+    if (token_scales && (!aligned16(k_scale) || !aligned16(v_scale))) return KVQ_ERR_ALIGN;
   }
+  if (q_fp8 && q_scale_len != 1 && q_scale_len != num_q_heads) return KVQ_ERR_SHAPE;
   if (num_q_tokens == 0 || max_q_len == 0) return KVQ_OK;
   const int TQ = kPfRows / G;
   const int64_t tiles = (static_cast<int64_t>(max_q_len) + TQ - 1) / TQ;
@@ -535,6 +549,9 @@ extern "C" int kvq_prefill_attn(const void* q, const int32_t* cu_q_lens, int64_t
   p.ks = fmt == KVQ_FMT_BF16 ? nullptr : k_scale;
   p.vs = fmt == KVQ_FMT_BF16 ? nullptr : v_scale;
   p.per_head = scale_granularity == KVQ_SCALE_PER_HEAD;
+  p.ts = token_scales ? 1 : 0;
+  p.qs = q_fp8 ? q_scale : nullptr;
+  p.q_per_head = q_fp8 && q_scale_len == num_q_heads && num_q_heads > 1;
   p.logit_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
   p.out = static_cast<uint16_t*>(out);
   p.status = dev_status;

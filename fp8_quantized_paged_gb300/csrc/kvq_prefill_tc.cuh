@@ -59,7 +59,11 @@ struct Layout {
   static constexpr size_t p = vt + kBufs * vtBytes;        // P   2 x [128][64] f16
   static constexpr size_t pBytes = static_cast<size_t>(kRows) * kKeys * 2;
   static constexpr size_t stage = p + 2 * pBytes;          // FP8 pages, kStagesTc stages
-  static constexpr size_t bars = stage + static_cast<size_t>(kStagesTc) * kStage;
+  // per-(token, head) scales: each stage's [4 pages][K 16, V 16] fp32, then
+  // each f16 buffer's block [K 64, V 64] fp32 (zero where masked)
+  static constexpr size_t ssc = stage + static_cast<size_t>(kStagesTc) * kStage;
+  static constexpr size_t bsc = ssc + static_cast<size_t>(kStagesTc) * 4 * 32 * 4;
+  static constexpr size_t bars = bsc + static_cast<size_t>(kBufs) * 128 * 4;
   // barriers: full[S], empty[S], conv[kBufs], kvdone[kBufs], sfull[2],
   // pfull[2], pdone[2], fin, qready
   static constexpr int kBars = 2 * kStagesTc + 2 * kBufs + 6 + 2;
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           pg_bad[s * 4 + i] = rows[i] < 0 ? 1u : 0u;
-          if (rows[i] >= 0) bytes += 2 * Lo::kPage8;
+          if (rows[i] >= 0) bytes += 2 * Lo::kPage8 + (p.ts ? 2 * 64 : 0);
         }
         issued[s] = j;
         if (bytes == 0) {  // nothing to load: complete the phase by hand
@@ -247,6 +251,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (rows[i] < 0) continue;
             tma_load_2d(dst + i * Lo::kPage8, &tmk, 0, rows[i], &full[s]);
             tma_load_2d(dst + (4 + i) * Lo::kPage8, &tmv, 0, rows[i], &full[s]);
+            if (p.ts) {  // the page's 16 K and 16 V scales (the row is a multiple of 16)
+              float* sc = reinterpret_cast<float*>(smem + Lo::ssc) + (s * 4 + i) * 32;
+              bulk_load(sc, p.ks + rows[i], 64, &full[s]);
+              bulk_load(sc + 16, p.vs + rows[i], 64, &full[s]);
+            }
           }
         }
       }
@@ -353,6 +362,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         sts128(vb + sw128_off(t, 16 * c, kKeys), h[0], h[1], h[2], h[3]);
         sts128(vb + sw128_off(t, 16 * c + 8, kKeys), h[4], h[5], h[6], h[7]);
       }
+      if (p.ts) {  // the block's scales, for the softmax: 0 for masked pages and tokens past L
+        const int t = ct & 63, kv = ct >> 6, pg = t >> 4;
+        const float* sc = reinterpret_cast<const float*>(smem + Lo::ssc) + (s * 4 + pg) * 32;
+        const bool in = !(bmask >> pg & 1u) && tok_base + t < L;
+        reinterpret_cast<float*>(smem + Lo::bsc)[(j % kBufs) * 128 + ct] = in ? sc[kv * 16 + (t & 15)] : 0.f;
+      }
       fence_proxy_async_smem();  // generic writes -> the tensor core's reads
       mbar_arrive(&conv[j % kBufs]);
       mbar_arrive(&empty[s]);
@@ -374,7 +389,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int64_t qrow = live ? static_cast<int64_t>(q0 + jr) * p.Hq + gkv * p.G + r % p.G : -1;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
 
-    // Q row r -> f16 into the A tile
+    // FP8-domain query: the row's head scale sQ; the row's codes enc(q / sQ)
+    const float sq = p.qs ? __ldg(p.qs + (p.q_per_head ? gkv * p.G + r % p.G : 0)) : 1.f;
+    // Q row r -> f16 into the A tile (under KVQ_Q_FP8 the decoded codes, exact)
     {
       const bool ok = live && guard(qrow < p.total_q * p.Hq, p.status, 23);
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (ok ? qrow : 0) * DH);
@@ -384,13 +401,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t h[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = f32x2_to_f16x2(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]));
+        for (int i = 0; i < 4; ++i) {
+          if (p.qs)
+            h[i] = fp8x2_to_f16x2<FMT>(f32x2_to_fp8x2<FMT>(__fdiv_rn(bf16lo_to_f32(w[i]), sq),
+                                                           __fdiv_rn(bf16hi_to_f32(w[i]), sq)));
+          else
+            h[i] = f32x2_to_f16x2(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]));
+        }
         sts128(sbase + Lo::q + sw128_off(r, 8 * c, kRows), h[0], h[1], h[2], h[3]);
       }
     }
-    const float sk = __ldg(p.ks + (p.per_head ? gkv : 0));
-    const float sv = __ldg(p.vs + (p.per_head ? gkv : 0));
-    const float lscale = sk * p.logit_scale;
+    // per-(token, head) scales multiply each key's logit and each value's
+    // probability inside the loop; the fixed factors here
+    const float sk = p.ts ? 1.f : __ldg(p.ks + (p.per_head ? gkv : 0));
+    const float sv = p.ts ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
+    const float lscale = sk * sq * p.logit_scale;
+    // Per-(token, head) V scales: P's columns carry sV_t / sigma, sigma a
+    // power of two at least the largest sV_t so far (so P stays <= 2^8 in
+    // f16); when a block raises it, O is rescaled with the running maximum.
+    float sigma = 0.f;
 
     // Waits of this role are warp-uniform (the TMEM accesses after them are
     // warp-collective).
@@ -425,6 +454,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
       const int kb0 = (p_begin + 4 * j) * kBS;
+      const float* bsc = reinterpret_cast<const float*>(smem + Lo::bsc) + (j % kBufs) * 128;
+      float sig_new = sigma;
+      if (p.ts) {  // sK of each key (0 where masked); sigma over the block's sV
+        float vm = 0.f;
+#pragma unroll
+        for (int i = 0; i < kKeys; i += 4) {
+          const float4 k4 = *reinterpret_cast<const float4*>(bsc + i);
+          const float4 v4 = *reinterpret_cast<const float4*>(bsc + kKeys + i);
+          x[i] *= k4.x;
+          x[i + 1] *= k4.y;
+          x[i + 2] *= k4.z;
+          x[i + 3] *= k4.w;
+          vm = fmaxf(vm, fmaxf(fmaxf(v4.x, v4.y), fmaxf(v4.z, v4.w)));
+        }
+        if (vm > sigma) {  // the smallest power of two >= vm (vm itself when infinite)
+          const uint32_t e = __float_as_uint(vm) & 0x7F800000u;
+          sig_new = (__uint_as_float(e) == vm || e == 0x7F800000u) ? vm : __uint_as_float(e + 0x00800000u);
+        }
+      }
       // eight partial maxima: independent chains (max is exact in any order)
       float mx8[8];
 #pragma unroll
@@ -447,7 +495,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // and into the exponent's fused multiply-add
       mx *= lscale;
       const bool grow = mx > m + kRescaleThreshold;
-      const bool rescale = __any_sync(kFull, grow);
+      // sigma is the same on every row (sV depends on the token and KV head)
+      const bool rescale = __any_sync(kFull, grow) || sig_new != sigma;
       bool wok = true;
       if (j >= 2)  // PV(j - 2), the last reader of P buffer j % 2: every block
         wok = wait_w(&pdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1));
@@ -461,29 +510,38 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (rescale) {  // rescale O rows (warp-collective TMEM access)
         const float nm = grow ? mx : m;
         const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - nm);
+        // O holds sum p sV / sigma V: a larger sigma scales it by sigma / sigma_new
+        const float ao = (sigma > 0.f && sig_new != sigma) ? a * (sigma / sig_new) : a;
         if (j >= 1) {
 #pragma unroll
           for (int c = 0; c < DH; c += 32) {
             float o[32];
             tmem_ld32(tm_o + lane_base + c, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= a;
+            for (int i = 0; i < 32; ++i) o[i] *= ao;
             tmem_st32(tm_o + lane_base + c, o);
           }
         }
         l *= a;
         m = nm;
+        sigma = sig_new;
       }
       // P row -> f16 into the A tile of PV
       uint32_t ph[kKeys / 2];
       float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of the block
+#pragma unroll
+      // sV_t / sigma of each value (a power-of-two quotient: exact)
+      const float isig = sigma > 0.f ? 1.f / sigma : 0.f;
 #pragma unroll
       for (int i = 0; i < kKeys; i += 2) {
         // m = -inf only while every key so far is masked (this block's too)
         const float p0 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i], lscale, -m));
         const float p1 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i + 1], lscale, -m));
         l4[(i >> 1) & 3] += p0 + p1;
-        ph[i / 2] = f32x2_to_f16x2(p0, p1);
+        if (p.ts)
+          ph[i / 2] = f32x2_to_f16x2(p0 * (bsc[kKeys + i] * isig), p1 * (bsc[kKeys + i + 1] * isig));
+        else
+          ph[i / 2] = f32x2_to_f16x2(p0, p1);
       }
       l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
 #pragma unroll
@@ -502,7 +560,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (eok) eok = wait_w(&pdone[(nblk - 1) & 1], static_cast<uint32_t>(((nblk - 1) >> 1) & 1));
     if (eok) {
       tc_fence_after();
-      const float f = l > 0.f ? sv / l : 0.f;
+      const float f = l > 0.f ? (p.ts ? sigma : sv) / l : 0.f;
       const bool store = live && guard(qrow < p.total_q * p.Hq, p.status, 24);
 #pragma unroll
       for (int c = 0; c < DH; c += 32) {

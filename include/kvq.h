@@ -366,8 +366,15 @@ KVQ_API int kvq_decode_static_reset(kvq_stream_t stream);
  *   max_q_len       host: an upper bound of every n_b (sets the grid; the
  *                   rows of a longer chunk past it are left unwritten and
  *                   KVQ_DEV_BAD_QLEN is raised).
- *   block_tables, seq_lens, caches, scales, fmt   as for kvq_decode_attn
- *                   (KVQ_SCALE_PER_TENSOR or KVQ_SCALE_PER_HEAD).
+ *   block_tables, seq_lens, caches, q_scale, k_scale, v_scale,
+ *   scale_granularity, fmt   as for kvq_decode_attn, every granularity
+ *                   included: KVQ_SCALE_PER_TOKEN_HEAD reads the scale caches
+ *                   that kvq_write_token_head fills (a prefix hit on such a
+ *                   cache); q_scale is read only with KVQ_Q_FP8.
+ *   flags           0 or KVQ_Q_FP8 (FP8 caches only): each query element is
+ *                   encoded to the cache's format as cast_fp8(q / sQ) and
+ *                   attends as its decoded value times sQ, as in
+ *                   kvq_decode_attn.
  *   out             bf16 [num_q_tokens][num_q_heads][head_dim].
  *   dev_status      optional; KVQ_DEV_BAD_BLOCK (page masked out),
  *                   KVQ_DEV_BAD_SEQLEN (L_b < n_b or L_b > max_blocks_per_seq
@@ -382,10 +389,11 @@ KVQ_API int kvq_prefill_attn(const void* q, const int32_t* cu_q_lens, int64_t nu
                              const int32_t* block_tables, int max_blocks_per_seq,
                              const int32_t* seq_lens, int num_seqs, int num_q_heads,
                              int num_kv_heads, int head_dim, int64_t num_blocks,
-                             int block_size, const float* k_scale, int k_scale_len,
-                             const float* v_scale, int v_scale_len, int scale_granularity,
-                             int fmt, int sliding_window, void* out, uint32_t* dev_status,
-                             kvq_stream_t stream);
+                             int block_size, const float* q_scale, int q_scale_len,
+                             const float* k_scale, int k_scale_len, const float* v_scale,
+                             int v_scale_len, int scale_granularity, int fmt,
+                             int sliding_window, unsigned flags, void* out,
+                             uint32_t* dev_status, kvq_stream_t stream);
 
 /*
  * kvq_dequant_cache -- the unfused path's separate dequant kernel

@@ -150,21 +150,32 @@ def test_write_token_head_validation(kvq):
 
 def _prefill(kvq, **kw):
     args = dict(q=A, cu=A, nq=64, maxq=32, kc=A, vc=A, bt=A, maxb=4, sl=A, B=2, hq=32, hkv=8,
-                dh=128, nb=8, bs=16, ks=A, ksl=1, vs=A, vsl=1, gran=0, fmt=1, win=0, out=A)
+                dh=128, nb=8, bs=16, qs=None, qsl=0, ks=A, ksl=1, vs=A, vsl=1, gran=0, fmt=1,
+                win=0, flags=0, out=A)
     args.update(kw)
     p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
     return kvq.lib().kvq_prefill_attn(
         p(args["q"]), p(args["cu"]), args["nq"], args["maxq"], p(args["kc"]), p(args["vc"]),
         p(args["bt"]), args["maxb"], p(args["sl"]), args["B"], args["hq"], args["hkv"], args["dh"],
-        args["nb"], args["bs"], p(args["ks"]), args["ksl"], p(args["vs"]), args["vsl"],
-        args["gran"], args["fmt"], args["win"], p(args["out"]), None, None)
+        args["nb"], args["bs"], p(args["qs"]), args["qsl"], p(args["ks"]), args["ksl"],
+        p(args["vs"]), args["vsl"], args["gran"], args["fmt"], args["win"], args["flags"],
+        p(args["out"]), None, None)
 
 
 def test_prefill_validation(kvq):
     assert _prefill(kvq, q=None) == kvq.KVQ_ERR_NULL
     assert _prefill(kvq, cu=None) == kvq.KVQ_ERR_NULL
     assert _prefill(kvq, fmt=3) == kvq.KVQ_ERR_ARG
-    assert _prefill(kvq, gran=2) == kvq.KVQ_ERR_ARG   # per-token scales: decode only
+    assert _prefill(kvq, gran=2) == kvq.KVQ_ERR_SHAPE  # per-token scales want the scale caches
+    assert _prefill(kvq, gran=2, ksl=8 * 8 * 16, vsl=8 * 8 * 16, nq=0) == kvq.KVQ_OK
+    assert _prefill(kvq, gran=2, ksl=8 * 8 * 16, vsl=8 * 8 * 16, ks=A + 4) == kvq.KVQ_ERR_ALIGN
+    assert _prefill(kvq, gran=2, fmt=0) == kvq.KVQ_ERR_ARG  # bf16 cache: no scales
+    assert _prefill(kvq, gran=3) == kvq.KVQ_ERR_ARG
+    assert _prefill(kvq, flags=2) == kvq.KVQ_ERR_ARG        # KVQ_CACHE_READY: decode only
+    assert _prefill(kvq, flags=1) == kvq.KVQ_ERR_NULL       # KVQ_Q_FP8 wants q_scale
+    assert _prefill(kvq, flags=1, qs=A, qsl=5) == kvq.KVQ_ERR_SHAPE
+    assert _prefill(kvq, flags=1, qs=A, qsl=32, nq=0) == kvq.KVQ_OK
+    assert _prefill(kvq, flags=1, qs=A, qsl=1, fmt=0) == kvq.KVQ_ERR_ARG
     assert _prefill(kvq, B=0) == kvq.KVQ_ERR_ARG
     assert _prefill(kvq, nq=-1) == kvq.KVQ_ERR_ARG
     assert _prefill(kvq, win=-2) == kvq.KVQ_ERR_ARG

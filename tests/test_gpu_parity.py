@@ -845,3 +845,118 @@ def test_prefill_chunk_longer_than_max_q_len(kvq):
                          lay.fmt, 0, out, dev_status=d.status)
     assert d.status_word() == 0
     check_attention(bf16_out_to_f64(out), ref, "covered")
+
+
+# ---------------------------------------------------------------- prefill with per-(token, head)
+# scales and the FP8-domain query
+
+def _prefill_ex(kvq, lay, nq, seed, token_head=False, q_fp8=False, window=None):
+    """Prefill with the last nq[b] tokens of each sequence as queries, over a
+    cache written per tensor / per head, or per (token, head) with its scale
+    caches; optionally the FP8-domain query (q_scale = lay.q_scale).  Returns
+    (gpu float64, float64 oracle)."""
+    r = np.random.default_rng(seed)
+    cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = workloads.f32_to_bf16_bits(r.standard_normal((int(cu[-1]), lay.Hq, lay.dh)).astype(np.float32))
+    d = DeviceLayer(lay, token_head=token_head)
+    d.write()
+    out = torch.full((int(cu[-1]), lay.Hq, lay.dh), float("nan"), dtype=torch.bfloat16, device="cuda")
+    win = lay.window if window is None else window
+    ks, vs = (d.ksc, d.vsc) if token_head else (d.ks, d.vs)
+    gran = kvq.KVQ_SCALE_PER_TOKEN_HEAD if token_head else lay.gran
+    kvq.kvq_prefill_attn(to_dev(q), to_dev(cu), int(max(nq)), d.kc, d.vc, d.bt, d.sl, ks, vs, gran,
+                         lay.fmt, win, out, dev_status=d.status,
+                         q_scale=d.qs if q_fp8 else None, flags=kvq.KVQ_Q_FP8 if q_fp8 else 0)
+    status = d.status_word()
+    if token_head:
+        K, V, sK, sV = oracle_caches(lay, token_head=True)
+        ksr, vsr, granr = sK, sV, oracle.PER_TOKEN_HEAD
+    else:
+        K, V = oracle_caches(lay)
+        ksr, vsr, granr = lay.k_scale, lay.v_scale, lay.gran
+    ref = oracle.prefill_attn(q, cu, K, V, lay.st.block_tables, lay.st.seq_lens, ksr, vsr,
+                              granr, lay.fmt, window=win,
+                              q_scale=lay.q_scale if q_fp8 else None)
+    return bf16_out_to_f64(out), ref, status
+
+
+def _per_token_magnitudes(lay, seed):
+    """K and V rows scaled by factors log-uniform over 10^[-1, 1], so the
+    per-(token, head) scales span two decades inside every key block (the
+    probabilities reach the PV MMA as f16, within 2^-12 of their value: the
+    output's error bound grows with the largest |V| a row attends to)."""
+    r = np.random.default_rng(seed)
+    for x in (lay.k, lay.v):
+        f = 10.0 ** r.uniform(-1.0, 1.0, size=x.shape[:2] + (1,))
+        x[:] = workloads.f32_to_bf16_bits((workloads.bf16_bits_to_f32(x) * f).astype(np.float32))
+
+
+@pytest.mark.parametrize("fmt", [workloads.E4M3, workloads.E5M2])
+@pytest.mark.parametrize("G,dh", [(1, 64), (2, 128), (4, 128), (8, 64)])
+def test_prefill_token_head_scales(kvq, fmt, G, dh):
+    """A prefix hit, a whole prefill and a single query over a cache written
+    by kvq_write_token_head, with per-token magnitudes spanning two decades."""
+    lay = _custom_layer([70, 33, 300, 16, 129], Hq=2 * G, Hkv=2, dh=dh, fmt=fmt, seed=230 + G + dh)
+    _per_token_magnitudes(lay, 231)
+    got, ref, st = _prefill_ex(kvq, lay, [70, 5, 37, 1, 0], seed=232, token_head=True)
+    assert st == 0
+    check_attention(got, ref, f"token-head prefill G={G} dh={dh}")
+
+
+@pytest.mark.parametrize("token_head", [False, True])
+@pytest.mark.parametrize("gran", [workloads.PER_TENSOR, workloads.PER_HEAD])
+def test_prefill_q_fp8(kvq, token_head, gran):
+    lay = _custom_layer([300, 70, 129], Hq=32, Hkv=8, dh=128, gran=gran, seed=240)
+    lay.q_scale[:] = np.linspace(0.005, 0.02, lay.q_scale.size).astype(np.float32)
+    got, ref, st = _prefill_ex(kvq, lay, [64, 70, 1], seed=241, token_head=token_head, q_fp8=True)
+    assert st == 0
+    check_attention(got, ref, f"q fp8 prefill token_head={token_head}")
+
+
+@pytest.mark.parametrize("window", [1, 100])
+def test_prefill_token_head_window_and_bad_block(kvq, window):
+    lay = _custom_layer([600, 40], Hq=8, Hkv=2, dh=128, seed=250)
+    _per_token_magnitudes(lay, 251)
+    got, ref, st = _prefill_ex(kvq, lay, [150, 40], seed=252, token_head=True, window=window)
+    assert st == 0
+    check_attention(got, ref, f"token-head prefill window={window}")
+    # an out-of-range block id in the prefix: its 16 tokens are masked out;
+    # the reference re-packs the other tokens (the queries keep their order)
+    bt = lay.st.block_tables.copy()
+    bt[0, 20] = lay.st.num_blocks + 3
+    r = np.random.default_rng(253)
+    cu = np.array([0, 150, 190], np.int32)
+    q = workloads.f32_to_bf16_bits(r.standard_normal((190, 8, 128)).astype(np.float32))
+    d = DeviceLayer(lay, token_head=True)
+    d.write()
+    out = torch.full((190, 8, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kvq.kvq_prefill_attn(to_dev(q), to_dev(cu), 150, d.kc, d.vc, to_dev(bt), d.sl, d.ksc, d.vsc,
+                         kvq.KVQ_SCALE_PER_TOKEN_HEAD, lay.fmt, 0, out, dev_status=d.status)
+    assert d.status_word() == kvq.KVQ_DEV_BAD_BLOCK
+    K, V, sK, sV = oracle_caches(lay, token_head=True)
+    lens = lay.st.seq_lens
+    keep = [np.array([t for t in range(lens[0]) if not 320 <= t < 336]), np.arange(lens[1])]
+    st2 = workloads._structure(np.array([len(k) for k in keep]), np.random.default_rng(254))
+    K2 = oracle.new_cache(st2.num_blocks, 2, 16, 128, lay.fmt)
+    V2 = oracle.new_cache(st2.num_blocks, 2, 16, 128, lay.fmt)
+    sK2 = np.zeros((st2.num_blocks, 2, 16), np.float32)
+    sV2 = np.zeros_like(sK2)
+    for b, toks in enumerate(keep):
+        for i, t in enumerate(toks):
+            bo, oo = int(lay.st.block_tables[b, t // 16]), t % 16
+            bn, on = int(st2.block_tables[b, i // 16]), i % 16
+            K2[bn, :, on], V2[bn, :, on] = K[bo, :, oo], V[bo, :, oo]
+            sK2[bn, :, on], sV2[bn, :, on] = sK[bo, :, oo], sV[bo, :, oo]
+    ref = oracle.prefill_attn(q, cu, K2, V2, st2.block_tables, st2.seq_lens, sK2, sV2,
+                              oracle.PER_TOKEN_HEAD, lay.fmt)
+    check_attention(bf16_out_to_f64(out), ref, "token-head prefill, masked block")
+
+
+def test_prefill_one_query_matches_decode_token_head_and_q_fp8(kvq):
+    """n_b = 1 queries over a per-(token, head) cache with the FP8-domain query:
+    the prefill's rows equal the decode's (both against the oracle)."""
+    lay = _custom_layer([300, 1, 45, 1000], Hq=32, Hkv=8, dh=128, seed=260)
+    lay.q_scale[:] = np.linspace(0.01, 0.03, lay.q_scale.size).astype(np.float32)
+    got, ref, st = _prefill_ex(kvq, lay, [1, 1, 1, 1], seed=261, token_head=True, q_fp8=True)
+    assert st == 0
+    check_attention(got, ref, "prefill n=1, token-head, q fp8")
