@@ -460,9 +460,12 @@ template <int FMT, int DH>
 static int prefill_tc_launch(PrefillParams p, int max_q_len, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t s) {
   constexpr size_t smem = tc::Layout<DH>::total;
-  static DeviceOnce once;  // the kernel's attribute, once per device (again after a failure)
+  static DeviceOnce once;  // the kernels' attribute, once per device (again after a failure)
   if (!once.run(current_device(), [] {
-        return cudaFuncSetAttribute(tc::prefill_tc_kernel<FMT, DH>,
+        return cudaFuncSetAttribute(tc::prefill_tc_kernel<FMT, DH, false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem)) == cudaSuccess &&
+               cudaFuncSetAttribute(tc::prefill_tc_kernel<FMT, DH, true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem)) == cudaSuccess;
       }))
@@ -470,8 +473,10 @@ static int prefill_tc_launch(PrefillParams p, int max_q_len, const CUtensorMap& 
   const int TQ = tc::kRows / p.G;
   p.tiles = (max_q_len + TQ - 1) / TQ;
   const dim3 grid(p.tiles, p.Hkv, p.B), block(tc::kThreadsTc);
-  if (launch_pdl(tc::prefill_tc_kernel<FMT, DH>, grid, block, smem, s, p, tk, tv) != cudaSuccess)
-    return KVQ_ERR_CUDA;
+  const cudaError_t e =
+      p.ts ? launch_pdl(tc::prefill_tc_kernel<FMT, DH, true>, grid, block, smem, s, p, tk, tv)
+           : launch_pdl(tc::prefill_tc_kernel<FMT, DH, false>, grid, block, smem, s, p, tk, tv);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

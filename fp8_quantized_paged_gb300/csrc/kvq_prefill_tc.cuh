@@ -93,7 +93,9 @@ KVQ_DEVI uint64_t sw128_desc_mn(uint32_t saddr) {
          (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
 }
 
-template <int FMT, int DH>
+// TS: per-(token, head) scales (p.ts), a separate instance so that the other
+// scale modes keep their loop free of the per-key scaling.
+template <int FMT, int DH, bool TS>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p,
                       const __grid_constant__ CUtensorMap tmk,
@@ -238,7 +240,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           pg_bad[s * 4 + i] = rows[i] < 0 ? 1u : 0u;
-          if (rows[i] >= 0) bytes += 2 * Lo::kPage8 + (p.ts ? 2 * 64 : 0);
+          if (rows[i] >= 0) bytes += 2 * Lo::kPage8 + (TS ? 2 * 64 : 0);
         }
         issued[s] = j;
         if (bytes == 0) {  // nothing to load: complete the phase by hand
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (rows[i] < 0) continue;
             tma_load_2d(dst + i * Lo::kPage8, &tmk, 0, rows[i], &full[s]);
             tma_load_2d(dst + (4 + i) * Lo::kPage8, &tmv, 0, rows[i], &full[s]);
-            if (p.ts) {  // the page's 16 K and 16 V scales (the row is a multiple of 16)
+            if (TS) {  // the page's 16 K and 16 V scales (the row is a multiple of 16)
               float* sc = reinterpret_cast<float*>(smem + Lo::ssc) + (s * 4 + i) * 32;
               bulk_load(sc, p.ks + rows[i], 64, &full[s]);
               bulk_load(sc + 16, p.vs + rows[i], 64, &full[s]);
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         sts128(vb + sw128_off(t, 16 * c, kKeys), h[0], h[1], h[2], h[3]);
         sts128(vb + sw128_off(t, 16 * c + 8, kKeys), h[4], h[5], h[6], h[7]);
       }
-      if (p.ts) {  // the block's scales, for the softmax: 0 for masked pages and tokens past L
+      if (TS) {  // the block's scales, for the softmax: 0 for masked pages and tokens past L
         const int t = ct & 63, kv = ct >> 6, pg = t >> 4;
         const float* sc = reinterpret_cast<const float*>(smem + Lo::ssc) + (s * 4 + pg) * 32;
         const bool in = !(bmask >> pg & 1u) && tok_base + t < L;
@@ -413,8 +415,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     // per-(token, head) scales multiply each key's logit and each value's
     // probability inside the loop; the fixed factors here
-    const float sk = p.ts ? 1.f : __ldg(p.ks + (p.per_head ? gkv : 0));
-    const float sv = p.ts ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
+    const float sk = TS ? 1.f : __ldg(p.ks + (p.per_head ? gkv : 0));
+    const float sv = TS ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
     const float lscale = sk * sq * p.logit_scale;
     // Per-(token, head) V scales: P's columns carry sV_t / sigma, sigma a
     // power of two at least the largest sV_t so far (so P stays <= 2^8 in
@@ -456,7 +458,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int kb0 = (p_begin + 4 * j) * kBS;
       const float* bsc = reinterpret_cast<const float*>(smem + Lo::bsc) + (j % kBufs) * 128;
       float sig_new = sigma;
-      if (p.ts) {  // sK of each key (0 where masked); sigma over the block's sV
+      if (TS) {  // sK of each key (0 where masked); sigma over the block's sV
         float vm = 0.f;
 #pragma unroll
         for (int i = 0; i < kKeys; i += 4) {
@@ -529,7 +531,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // P row -> f16 into the A tile of PV
       uint32_t ph[kKeys / 2];
       float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of the block
-#pragma unroll
       // sV_t / sigma of each value (a power-of-two quotient: exact)
       const float isig = sigma > 0.f ? 1.f / sigma : 0.f;
 #pragma unroll
@@ -538,7 +539,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const float p0 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i], lscale, -m));
         const float p1 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i + 1], lscale, -m));
         l4[(i >> 1) & 3] += p0 + p1;
-        if (p.ts)
+        if (TS)
           ph[i / 2] = f32x2_to_f16x2(p0 * (bsc[kKeys + i] * isig), p1 * (bsc[kKeys + i + 1] * isig));
         else
           ph[i / 2] = f32x2_to_f16x2(p0, p1);
@@ -560,7 +561,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (eok) eok = wait_w(&pdone[(nblk - 1) & 1], static_cast<uint32_t>(((nblk - 1) >> 1) & 1));
     if (eok) {
       tc_fence_after();
-      const float f = l > 0.f ? (p.ts ? sigma : sv) / l : 0.f;
+      const float f = l > 0.f ? (TS ? sigma : sv) / l : 0.f;
       const bool store = live && guard(qrow < p.total_q * p.Hq, p.status, 24);
 #pragma unroll
       for (int c = 0; c < DH; c += 32) {
