@@ -192,7 +192,17 @@ extern "C" int kvq_decode_attn(const void* q, const void* k_cache, const void* v
   // SM); by default the warp-MMA kernel serves them, which times faster.
   const bool use_blk = KVQ_DECODE_BLK && !use_tc && fmt != KVQ_FMT_BF16 && head_dim == 128 && !token_scales &&
                        G == 4 && num_kv_heads % kMaxHT == 0 && dtb::fits_blk(num_seqs, num_kv_heads);
-  const int ctas = use_blk ? sms : (use_tc ? dtc::kCtasPerSmTc * sms : kCtasPerSM * sms);
+  int ctas = use_blk ? sms : (use_tc ? dtc::kCtasPerSmTc * sms : kCtasPerSM * sms);
+  // Under KVQ_CACHE_READY this grid's CTAs take the slots that the previous
+  // call's CTAs free as they exit, and prefetch their first pages there; the
+  // CTAs still merging a split segment hold a slot each to the end.  With few
+  // (sequence, KV head) segments (each split over four or more CTAs) every
+  // segment has such a merger, so the grid leaves that many slots to them:
+  // otherwise its last CTAs would start only after the merges, with nothing
+  // prefetched, and finish last.
+  const int64_t segments = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  if ((flags & KVQ_CACHE_READY) && !use_blk && !use_tc && 4 * segments <= ctas)
+    ctas -= static_cast<int>(segments);
   const int P = static_cast<int>(std::min<int64_t>(ctas, use_blk ? max_units / kMaxHT : max_units));
   const WsLayout wl = ws_layout(num_seqs, G, num_kv_heads, head_dim, kCtasPerSM * sms);
   if (workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
