@@ -455,11 +455,12 @@ static int prefill_launch(const PrefillParams& p, const CUtensorMap& tk, const C
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
-// The FP8 caches' prefill on the tcgen05 tensor cores (128 query rows a CTA).
+// The FP8 caches' prefill on the tcgen05 tensor cores (two tiles of 128
+// query rows a CTA).
 template <int FMT, int DH>
 static int prefill_tc_launch(PrefillParams p, int max_q_len, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t s) {
-  constexpr size_t smem = tc::Layout<DH>::total;
+  constexpr size_t smem = tc::Layout<DH, false>::total, smem_ts = tc::Layout<DH, true>::total;
   static DeviceOnce once;  // the kernels' attribute, once per device (again after a failure)
   if (!once.run(current_device(), [] {
         return cudaFuncSetAttribute(tc::prefill_tc_kernel<FMT, DH, false>,
@@ -467,14 +468,14 @@ static int prefill_tc_launch(PrefillParams p, int max_q_len, const CUtensorMap& 
                                     static_cast<int>(smem)) == cudaSuccess &&
                cudaFuncSetAttribute(tc::prefill_tc_kernel<FMT, DH, true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem)) == cudaSuccess;
+                                    static_cast<int>(smem_ts)) == cudaSuccess;
       }))
     return KVQ_ERR_CUDA;
   const int TQ = tc::kRows / p.G;
   p.tiles = (max_q_len + TQ - 1) / TQ;
-  const dim3 grid(p.tiles, p.Hkv, p.B), block(tc::kThreadsTc);
+  const dim3 grid((p.tiles + tc::kTiles - 1) / tc::kTiles, p.Hkv, p.B), block(tc::kThreadsTc);
   const cudaError_t e =
-      p.ts ? launch_pdl(tc::prefill_tc_kernel<FMT, DH, true>, grid, block, smem, s, p, tk, tv)
+      p.ts ? launch_pdl(tc::prefill_tc_kernel<FMT, DH, true>, grid, block, smem_ts, s, p, tk, tv)
            : launch_pdl(tc::prefill_tc_kernel<FMT, DH, false>, grid, block, smem, s, p, tk, tv);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

@@ -1,25 +1,30 @@
 // kvq_prefill_tc.cuh -- the prefill kernel of the FP8 caches on the 5th-
 // generation tensor cores (tcgen05, accumulators in tensor memory).
 //
-// One CTA per (sequence, KV head, tile of 128 query rows); a row is a (query
-// token, query head of the group) pair, so a tile holds 128 / G tokens.  The
-// keys stream in blocks of 64 tokens (4 pages):
-//   warp 8 (producer): block ids 32 pages at a time (one per lane), TMA loads
+// One CTA per (sequence, KV head, pair of adjacent tiles of 128 query rows);
+// a row is a (query token, query head of the group) pair, so a tile holds
+// 128 / G tokens.  The keys stream in blocks of 64 tokens (4 pages), each
+// converted once for both tiles:
+//   warp 12 (producer): block ids 32 pages at a time (one per lane), TMA loads
 //     of each block's 4 K and 4 V FP8 pages into a 3-stage ring (the
 //     decode's 128-byte-swizzled page boxes).
-//   warps 4-7 (converters): each block's pages to f16 in shared memory, K as
+//   warps 8-11 (converters): each block's pages to f16 in shared memory, K as
 //     the B operand of QK^T and V as the MN-major B operand of PV, both
-//     token-major in the same layout, in kBufs buffers.
-//   warp 9 (MMA): allocates 256 TMEM columns (two 64-column S buffers and
-//     the dh-column O accumulator); one elected lane issues, per block,
-//     S = Q K^T (M = 128, N = 64, K = dh in steps of 16) and, once the block's
-//     probabilities are in shared memory, O += P V (N = dh, K = 64 tokens),
-//     each completion signalled to an mbarrier by tcgen05.commit.
-//   warps 0-3 (softmax; thread r = row r = TMEM lane r): Q row r to f16,
-//     then per block the S row from TMEM, causal / window mask (skipped for
-//     blocks the whole row sees), online max with a lazy rescale of the O row
-//     in TMEM, P = 2^(x-m) as f16 into one of two shared-memory tiles (the A
-//     operand of PV), so the next block's softmax need not wait for this PV.
+//     token-major in the same layout, in 2 or 3 buffers.
+//   warps 13 and 14 (MMA of tiles 0 and 1; warp 13 allocates the 512 TMEM
+//     columns: per tile two 64-column S buffers and the dh-column O
+//     accumulator): one elected lane each issues, per block of its tile,
+//     S = Q K^T (M = 128, N = 64, K = dh in steps of 16) and, once the
+//     tile's probabilities are in, O += P V (A = P from tensor memory,
+//     N = dh, K = 64 tokens), each completion signalled to an mbarrier by
+//     tcgen05.commit.  A tile skips the blocks none of its rows sees.
+//   warps 0-3 and 4-7 (softmax of tiles 0 and 1; thread r of a tile = row r
+//     = TMEM lane r): Q row r to f16, then per block the S row from TMEM,
+//     causal / window mask (skipped for blocks the whole row sees), online
+//     max with a lazy rescale of the O row in TMEM, P = 2^(x-m) as f16 back
+//     into the first 32 columns of the S buffer it came from (the A operand
+//     of PV), which the next QK^T into that buffer, issued after the PV,
+//     overwrites only once the PV has read it.
 // Every shared-memory operand is in the K-major 128-byte-swizzle layout:
 // 8-row groups of 1024 bytes, 128-byte rows of 64 f16, 16-byte chunk c of
 // row r at chunk c ^ (r % 8); wider K in further 64-column blocks of the
@@ -33,43 +38,41 @@
 namespace kvq {
 namespace tc {
 
-constexpr int kRows = 128;      // query rows per CTA (MMA M)
+constexpr int kRows = 128;      // query rows per tile (MMA M)
+constexpr int kTiles = 2;       // query tiles per CTA
 constexpr int kKeys = 64;       // tokens per key block (QK^T N, PV K)
-#ifndef KVQ_TC_STAGES
-#define KVQ_TC_STAGES 3
-#endif
-#ifndef KVQ_TC_BUFS
-#define KVQ_TC_BUFS 3
-#endif
-constexpr int kStagesTc = KVQ_TC_STAGES;  // FP8 page stages
-constexpr int kBufs = KVQ_TC_BUFS;        // f16 K / V buffers (converters run kBufs - 1 ahead)
-constexpr int kThreadsTc = 320; // warps 0-3 softmax, 4-7 convert, 8 producer, 9 MMA
-constexpr uint32_t kTmemCols = 256;
+// warps 0-7 softmax (4 per tile), 8-11 convert, 12 producer, 13-14 MMA (one per tile)
+constexpr int kThreadsTc = 480;
+constexpr int kConvWarp = 8, kProdWarp = 12, kMmaWarp = 13;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTileCols = 256;  // per tile: S buffers at +0, +64; O at +128
 
-template <int DH>
+// Shared memory: the two Q tiles, kB f16 K / V buffers (the converters run
+// kB - 1 blocks ahead of the PVs) and kS FP8 page stages.
+template <int DH, bool TS>
 struct Layout {
+  static constexpr int kS = 3;
+  static constexpr int kB = 3;
   static constexpr int kPage8 = kBS * DH;                  // bytes of one FP8 page
   static constexpr int kStage = 8 * kPage8;                // 4 K pages + 4 V pages
-  static constexpr size_t q = 0;                           // Q   [128][DH] f16
+  static constexpr size_t q = 0;                           // Q   kTiles x [128][DH] f16
   static constexpr size_t qBytes = static_cast<size_t>(kRows) * DH * 2;
-  static constexpr size_t k = q + qBytes;                  // K   kBufs x [64][DH] f16
+  static constexpr size_t k = q + kTiles * qBytes;         // K   kB x [64][DH] f16
   static constexpr size_t kBytes = static_cast<size_t>(kKeys) * DH * 2;
-  static constexpr size_t vt = k + kBufs * kBytes;         // V   kBufs x [64][DH] f16
+  static constexpr size_t vt = k + kB * kBytes;            // V   kB x [64][DH] f16
   static constexpr size_t vtBytes = static_cast<size_t>(DH) * kKeys * 2;
-  static constexpr size_t p = vt + kBufs * vtBytes;        // P   2 x [128][64] f16
-  static constexpr size_t pBytes = static_cast<size_t>(kRows) * kKeys * 2;
-  static constexpr size_t stage = p + 2 * pBytes;          // FP8 pages, kStagesTc stages
+  static constexpr size_t stage = vt + kB * vtBytes;       // FP8 pages, kS stages
   // per-(token, head) scales: each stage's [4 pages][K 16, V 16] fp32, then
   // each f16 buffer's block [K 64, V 64] fp32 (zero where masked)
-  static constexpr size_t ssc = stage + static_cast<size_t>(kStagesTc) * kStage;
-  static constexpr size_t bsc = ssc + static_cast<size_t>(kStagesTc) * 4 * 32 * 4;
-  static constexpr size_t bars = bsc + static_cast<size_t>(kBufs) * 128 * 4;
-  // barriers: full[S], empty[S], conv[kBufs], kvdone[kBufs], sfull[2],
-  // pfull[2], pdone[2], fin, qready
-  static constexpr int kBars = 2 * kStagesTc + 2 * kBufs + 6 + 2;
+  static constexpr size_t ssc = stage + static_cast<size_t>(kS) * kStage;
+  static constexpr size_t bsc = ssc + (TS ? static_cast<size_t>(kS) * 4 * 32 * 4 : 0);
+  static constexpr size_t bars = bsc + (TS ? static_cast<size_t>(kB) * 128 * 4 : 0);
+  // barriers: full[S], empty[S], conv[kB], kvdone[kB], sfull[kTiles][2],
+  // pfull[kTiles][2], pdone[kTiles][2], fin, qready
+  static constexpr int kBars = 2 * kS + 2 * kB + 6 * kTiles + 2;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
   // misc: tmem address, abort flag, page flags [S stages][4 pages], issued[S],
-  // masked pages of the blocks in the f16 buffers [kBufs]
+  // masked pages of the blocks in the f16 buffers [kB]
   static constexpr size_t total = misc + 256 + 1024;
 };
 
@@ -100,9 +103,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillParams p,
                       const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-  using Lo = Layout<DH>;
+  using Lo = Layout<DH, TS>;
   using C = Cfg<FMT, DH>;
-  constexpr int S = kStagesTc;
+  constexpr int S = Lo::kS;
+  constexpr int kBufs = Lo::kB;
   constexpr int KSTEPS = DH / 16;  // QK^T MMAs per block
   static_assert(C::kRow == DH && C::kPage == Lo::kPage8, "FP8 pages");
   extern __shared__ uint8_t smem_raw[];
@@ -113,19 +117,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint64_t* full = bars;               // [S] FP8 stage landed
   uint64_t* empty = bars + S;          // [S] FP8 stage converted (128 arrivals)
   uint64_t* conv = bars + 2 * S;            // [kBufs] f16 K / V buffer b ready (128 arrivals)
-  uint64_t* kvdone = conv + kBufs;          // [kBufs] PV of buffer b's block done (commit)
-  uint64_t* sfull = kvdone + kBufs;         // [2] S buffer b written (commit)
-  uint64_t* pfull = sfull + 2;   // [2] P buffer b written (128 arrivals)
-  uint64_t* pdone = sfull + 4;   // [2] PV of P buffer b's block done (commit)
-  uint64_t* fin = sfull + 6;     // every MMA done (commit)
-  uint64_t* qready = sfull + 7;  // the Q tile written (128 arrivals)
+  uint64_t* kvdone = conv + kBufs;          // [kBufs] buffer b's block released by both issuers
+  uint64_t* sfull = kvdone + kBufs;         // [kTiles][2] S buffer of a tile written (commit)
+  uint64_t* pfull = sfull + 2 * kTiles;     // [kTiles][2] P in a tile's S buffer (128 arrivals)
+  uint64_t* pdone = pfull + 2 * kTiles;     // [kTiles][2] PV from a tile's S buffer done (commit)
+  uint64_t* fin = pdone + 2 * kTiles;       // every MMA done (a commit of each issuer)
+  uint64_t* qready = fin + 1;               // both Q tiles written (256 arrivals)
   // A parity wait for phase p of a barrier is sound only while the barrier
   // has completed p or p + 1 phases.  Every waiter therefore waits each of
   // its barriers' phases in order, never skipping one (so p - 1 is known
   // complete), and a barrier's phase after p needs the waiter's own later
-  // progress.  Completion order is not assumed between MMAs that write
-  // different accumulators: QK^T of a block may finish before the PV issued
-  // ahead of it, so "S is ready" says nothing about earlier PVs.
+  // progress; barriers used once per block come in pairs (even and odd
+  // blocks), so that no waiter can fall two phases behind.  A tile's
+  // softmax, which may start after block 0, waits for a
+  // block's conversion only once the block's S is in (the MMA lane issued
+  // QK^T after that conversion): the phase is then complete, and the next
+  // one needs this tile's PV of the block.  Completion order is not assumed
+  // between MMAs that write different accumulators: QK^T of a block may
+  // finish before the PV issued ahead of it, so "S is ready" says nothing
+  // about earlier PVs.
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lo::misc);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint32_t* pg_bad = const_cast<uint32_t*>(tmem_slot + 2);    // [S][4] page masked out
@@ -134,7 +144,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.z, gkv = blockIdx.y;
-  const int tile = p.tiles - 1 - static_cast<int>(blockIdx.x);  // longest tiles first
+  const int pairs = (p.tiles + kTiles - 1) / kTiles;
+  const int pair = pairs - 1 - static_cast<int>(blockIdx.x);  // longest pairs first
   const int TQ = kRows / p.G;
 
   if (tid == 0) {
@@ -145,19 +156,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     for (int i = 0; i < kBufs; ++i) {
       mbar_init(&conv[i], 128);
-      mbar_init(&kvdone[i], 1);
+      mbar_init(&kvdone[i], kTiles);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sfull[i], 1);
-      mbar_init(&pfull[i], 128);
-      mbar_init(&pdone[i], 1);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&sfull[2 * t], 1);
+      mbar_init(&sfull[2 * t + 1], 1);
+      mbar_init(&pfull[2 * t], 128);
+      mbar_init(&pfull[2 * t + 1], 128);
+      mbar_init(&pdone[2 * t], 1);
+      mbar_init(&pdone[2 * t + 1], 1);
     }
-    mbar_init(fin, 1);
-    mbar_init(qready, 128);
+    mbar_init(fin, kTiles);
+    mbar_init(qready, kTiles * 128);
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kProdWarp && lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
@@ -166,15 +180,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   const int q0 = __ldg(p.cu_q + b);
   const int n = __ldg(p.cu_q + b + 1) - q0;
-  const int j0 = tile * TQ;
+  const int j0 = pair * kTiles * TQ;  // first query token of tile 0
   // a chunk longer than the grid covers (max_q_len): its later rows stay unwritten
   if (blockIdx.x == 0 && gkv == 0 && tid == 0 && n > p.tiles * TQ)
     flag_status(p.status, KVQ_DEV_BAD_QLEN);
   if (n <= 0 || j0 >= n) return;  // the whole CTA, before any tensor memory is taken
-  const int j1 = min(n, j0 + TQ);
+  const int j1 = min(n, j0 + kTiles * TQ);  // past the pair's last query token
   const int L = __ldg(p.seq_lens + b);
   if (!(L >= n && L <= p.max_blocks * kBS)) {
-    if (tile == 0 && gkv == 0 && tid == 0) flag_status(p.status, KVQ_DEV_BAD_SEQLEN);
+    if (pair == 0 && gkv == 0 && tid == 0) flag_status(p.status, KVQ_DEV_BAD_SEQLEN);
     for (int i = tid; i < (j1 - j0) * p.G * DH; i += kThreadsTc) {
       const int r = i / DH, d = i - r * DH;
       const int64_t orow = static_cast<int64_t>(q0 + j0 + r / p.G) * p.Hq + gkv * p.G + r % p.G;
@@ -187,8 +201,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int p_begin = window_lo(p.window, pos_first + 1) / kBS;  // first page
   const int p_end = pos_last / kBS;                              // last page
   const int nblk = (p_end - p_begin) / 4 + 1;                    // key blocks of 4 pages
+  // Tile t's blocks [jb[t], je[t]): from its first row's window start to its
+  // last row (empty for a tile past the chunk).  Adjacent tiles leave no
+  // block between them uncovered.
+  int jb[kTiles], je[kTiles];
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    const int a = j0 + t * TQ, e = min(n, a + TQ);
+    if (a >= n) {
+      jb[t] = je[t] = 0;
+    } else {
+      jb[t] = (window_lo(p.window, base + a + 1) / kBS - p_begin) / 4;
+      je[t] = ((base + e - 1) / kBS - p_begin) / 4 + 1;
+    }
+  }
 
-  if (warp == 9) {  // tensor memory for S (2 x 64 columns) and O (DH columns)
+  if (warp == kMmaWarp) {  // tensor memory: per tile S (2 x 64 columns) and O (DH columns)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(const_cast<uint32_t*>(tmem_slot))), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -197,7 +225,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_o = tmem + 128;  // O: columns 128 .. 128 + DH - 1
 
   auto fail = [&](void) {
     if (!*abort_flag) {
@@ -206,7 +233,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   };
 
-  if (warp == 8) {
+  if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
     // The 32 lanes look up the block ids of 8 blocks (32 pages) at once, a
     // group ahead; lane 0 takes each block's four by shuffle and issues its
@@ -263,51 +290,80 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       __syncwarp();
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // One elected lane per tile (warp kMmaWarp + t), in the tile's order
+    // QK(0), QK(1), PV(0), QK(2), PV(1), ...: P lives in its S buffer, and a
+    // later MMA may overwrite an earlier one's operand before that one has
+    // read it, so QK^T of tile block i waits for the PV of block i - 2.  A
+    // block's K / V buffer goes back to the converters once both issuers
+    // have released it (kvdone counts one commit of each, in block order).
+    const int t = warp - kMmaWarp;
     if (lane == 0) {
       const uint32_t id_qk = idesc_f16(kRows, kKeys), id_pv = idesc_f16(kRows, DH);
-      const uint32_t a_q = sbase + Lo::q, a_p = sbase + Lo::p;
+      const int nI = je[t] - jb[t];
       bool ok = wait_or_abort(qready, 0u, abort_flag);
-      for (int j = 0; j <= nblk && ok; ++j) {
-        if (j < nblk) {  // S[j % 2] = Q K_j^T
-          ok = wait_or_abort(&conv[j % kBufs], static_cast<uint32_t>((j / kBufs) & 1), abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t b_k = sbase + Lo::k + (j % kBufs) * Lo::kBytes;
+      int pv = 0;  // PVs issued (tile blocks)
+      auto issue_pv = [&]() -> bool {
+        const int i = pv, jp = jb[t] + i;
+        if (!wait_or_abort(&pfull[2 * t + (i & 1)], static_cast<uint32_t>((i >> 1) & 1), abort_flag))
+          return false;
+        tc_fence_after();
+        const uint32_t b_v = sbase + Lo::vt + (jp % kBufs) * Lo::vtBytes;
+        const uint32_t a_pt = tmem + t * kTileCols + (i & 1) * kKeys;  // P: 8 columns per 16 tokens
 #pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {
-            const uint32_t off_a = (ks >> 2) * (kRows * 128) + (ks & 3) * 32;
-            const uint32_t off_b = (ks >> 2) * (kKeys * 128) + (ks & 3) * 32;
-            mma_f16_ss(tmem + (j & 1) * kKeys, sw128_desc(a_q + off_a), sw128_desc(b_k + off_b),
-                       id_qk, ks > 0 ? 1u : 0u);
-          }
-          mma_commit(&sfull[j & 1]);
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          // 16 tokens = two 8-row groups of V; B is MN-major (bit 16)
+          mma_f16_ts(tmem + t * kTileCols + 128, a_pt + kk * 8, sw128_desc_mn(b_v + kk * 2048),
+                     id_pv | (1u << 16), (i > 0 || kk > 0) ? 1u : 0u);
         }
-        if (j >= 1) {  // O += P_{j-1} V_{j-1}
-          const int jp = j - 1;
-          ok = wait_or_abort(&pfull[jp & 1], static_cast<uint32_t>((jp >> 1) & 1), abort_flag);
+        mma_commit(&pdone[2 * t + (i & 1)]);  // the S buffer's P read, O updated
+        mma_commit(&kvdone[jp % kBufs]);      // this tile is done with the K / V buffer
+        ++pv;
+        return true;
+      };
+      for (int j = 0; j < nblk && ok; ++j) {
+        const int i = j - jb[t];
+        if (i >= 2 && i < nI) {  // PVs up to block i - 2 first: they need no conversion
+          while (ok && pv <= i - 2) ok = issue_pv();
           if (!ok) break;
-          tc_fence_after();
-          const uint32_t b_v = sbase + Lo::vt + (jp % kBufs) * Lo::vtBytes;
-          const uint32_t a_pj = a_p + (jp & 1) * Lo::pBytes;
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            // 16 tokens = two 8-row groups of V; B is MN-major (bit 16)
-            mma_f16_ss(tm_o, sw128_desc(a_pj + kk * 32), sw128_desc_mn(b_v + kk * 2048),
-                       id_pv | (1u << 16), (jp > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&kvdone[jp % kBufs]);  // K and V buffer jp % kBufs free
-          mma_commit(&pdone[jp & 1]);       // P buffer jp % 2 free
         }
+        if (j >= je[t]) {  // past the tile's blocks: its last PVs, in order, then release
+          while (ok && pv < nI) ok = issue_pv();
+          if (!ok) break;
+        }
+        // every conversion phase in order, used or not (kvdone needs this issuer's
+        // release of each block; the next phase of a buffer needs it)
+        ok = wait_or_abort(&conv[j % kBufs], static_cast<uint32_t>((j / kBufs) & 1), abort_flag);
+        if (!ok) break;
+        if (i < 0 || i >= nI) {
+          mma_commit(&kvdone[j % kBufs]);  // a block the tile does not see: released at once
+          continue;
+        }
+        if (i >= 2) {  // the S buffer's last P has been read (PV of block i - 2)
+          ok = wait_or_abort(&pdone[2 * t + (i & 1)], static_cast<uint32_t>(((i - 2) >> 1) & 1), abort_flag);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const uint32_t b_k = sbase + Lo::k + (j % kBufs) * Lo::kBytes;
+        const uint32_t a_q = sbase + Lo::q + t * Lo::qBytes;
+        const uint32_t d_s = tmem + t * kTileCols + (i & 1) * kKeys;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const uint32_t off_a = (ks >> 2) * (kRows * 128) + (ks & 3) * 32;
+          const uint32_t off_b = (ks >> 2) * (kKeys * 128) + (ks & 3) * 32;
+          mma_f16_ss(d_s, sw128_desc(a_q + off_a), sw128_desc(b_k + off_b), id_qk, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&sfull[2 * t + (i & 1)]);
       }
+      while (ok && pv < nI) ok = issue_pv();
       if (!ok) fail();
-      mma_commit(fin);  // completes when every MMA issued above has
+      mma_commit(fin);  // completes when every MMA issued above (by both issuers) has
       if (!mbar_wait(fin, 0u)) fail();
     }
-  } else if (warp >= 4) {
+  } else if (warp >= kConvWarp) {
     // ------------------------------------------------------------ converters
-    const int ct = tid - 128;  // 0 .. 127
+    const int ct = tid - kConvWarp * 32;  // 0 .. 127
     auto wait_w = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(kFull, wait_or_abort(bar, parity, abort_flag));
     };
@@ -316,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int s = j % S;
       if (!wait_w(&full[s], static_cast<uint32_t>((j / S) & 1))) return false;
       if (j >= kBufs && !wait_w(&kvdone[j % kBufs], static_cast<uint32_t>((j / kBufs - 1) & 1)))
-        return false;  // PV of block j - kBufs (the buffer's last reader) is done
+        return false;  // the PVs of block j - kBufs (the buffer's last readers) are done
       // the stage's page flags, kept for the softmax of block j (the
       // producer rewrites the stage's flags once the stage is released)
       const uint32_t bmask = (pg_bad[s * 4] ? 1u : 0u) | (pg_bad[s * 4 + 1] ? 2u : 0u) |
@@ -383,17 +439,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = tid;  // row = TMEM lane
-    const int jr = j0 + r / p.G;
-    const bool live = jr < j1;
+    const int t = warp >> 2;   // this warp group's tile
+    const int r = tid & 127;   // row = TMEM lane
+    const int jr = j0 + t * TQ + r / p.G;
+    const bool live = jr < n;
     const int pos = live ? base + jr : -1;
     const int lo = live ? window_lo(p.window, pos + 1) : 0;
     const int64_t qrow = live ? static_cast<int64_t>(q0 + jr) * p.Hq + gkv * p.G + r % p.G : -1;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tm_s = tmem + lane_base + t * kTileCols;  // S buffers of this tile
+    const uint32_t tm_o = tm_s + 128;                          // O of this tile
 
     // FP8-domain query: the row's head scale sQ; the row's codes enc(q / sQ)
     const float sq = p.qs ? __ldg(p.qs + (p.q_per_head ? gkv * p.G + r % p.G : 0)) : 1.f;
-    // Q row r -> f16 into the A tile (under KVQ_Q_FP8 the decoded codes, exact)
+    // Q row r -> f16 into the tile's A tile (under KVQ_Q_FP8 the decoded codes, exact)
     {
       const bool ok = live && guard(qrow < p.total_q * p.Hq, p.status, 23);
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (ok ? qrow : 0) * DH);
@@ -410,7 +469,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           else
             h[i] = f32x2_to_f16x2(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]));
         }
-        sts128(sbase + Lo::q + sw128_off(r, 8 * c, kRows), h[0], h[1], h[2], h[3]);
+        sts128(sbase + Lo::q + t * Lo::qBytes + sw128_off(r, 8 * c, kRows), h[0], h[1], h[2], h[3]);
       }
     }
     // per-(token, head) scales multiply each key's logit and each value's
@@ -432,27 +491,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     bool ok = true;
     fence_proxy_async_smem();  // the Q tile -> the tensor core
     mbar_arrive(qready);
-    for (int j = 0; j < nblk && ok; ++j) {
+    const int nI = je[t] - jb[t];  // this tile's blocks
+    for (int i = 0; i < nI && ok; ++i) {
+      const int j = jb[t] + i;
+      if (!wait_w(&sfull[2 * t + (i & 1)], static_cast<uint32_t>((i >> 1) & 1))) {
+        ok = false;
+        break;
+      }
       // the block's masked pages (the converters wrote them before conv[j % kBufs])
       if (!wait_w(&conv[j % kBufs], static_cast<uint32_t>((j / kBufs) & 1))) {
         ok = false;
         break;
       }
       const uint32_t bm = bufmask[j % kBufs];
-      if (!wait_w(&sfull[j & 1], static_cast<uint32_t>((j >> 1) & 1))) {
-        ok = false;
-        break;
-      }
       tc_fence_after();
       float x[kKeys];
       {
         float t0[32], t1[32];
-        tmem_ld32(tmem + lane_base + (j & 1) * kKeys, t0);
-        tmem_ld32(tmem + lane_base + (j & 1) * kKeys + 32, t1);
+        tmem_ld32(tm_s + (i & 1) * kKeys, t0);
+        tmem_ld32(tm_s + (i & 1) * kKeys + 32, t1);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = t0[i];
-          x[32 + i] = t1[i];
+        for (int e = 0; e < 32; ++e) {
+          x[e] = t0[e];
+          x[32 + e] = t1[e];
         }
       }
       const int kb0 = (p_begin + 4 * j) * kBS;
@@ -461,13 +522,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (TS) {  // sK of each key (0 where masked); sigma over the block's sV
         float vm = 0.f;
 #pragma unroll
-        for (int i = 0; i < kKeys; i += 4) {
-          const float4 k4 = *reinterpret_cast<const float4*>(bsc + i);
-          const float4 v4 = *reinterpret_cast<const float4*>(bsc + kKeys + i);
-          x[i] *= k4.x;
-          x[i + 1] *= k4.y;
-          x[i + 2] *= k4.z;
-          x[i + 3] *= k4.w;
+        for (int e = 0; e < kKeys; e += 4) {
+          const float4 k4 = *reinterpret_cast<const float4*>(bsc + e);
+          const float4 v4 = *reinterpret_cast<const float4*>(bsc + kKeys + e);
+          x[e] *= k4.x;
+          x[e + 1] *= k4.y;
+          x[e + 2] *= k4.z;
+          x[e + 3] *= k4.w;
           vm = fmaxf(vm, fmaxf(fmaxf(v4.x, v4.y), fmaxf(v4.z, v4.w)));
         }
         if (vm > sigma) {  // the smallest power of two >= vm (vm itself when infinite)
@@ -478,17 +539,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // eight partial maxima: independent chains (max is exact in any order)
       float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
       if (live && bm == 0u && kb0 >= lo && kb0 + kKeys - 1 <= pos) {  // the row sees the block
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
+        for (int e = 0; e < kKeys; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
       } else {
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) {
-          const int kp = kb0 + i;
-          const bool valid = live && kp >= lo && kp <= pos && !(bm >> (i >> 4) & 1u);
-          x[i] = valid ? x[i] : -INFINITY;
-          mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
+        for (int e = 0; e < kKeys; ++e) {
+          const int kp = kb0 + e;
+          const bool valid = live && kp >= lo && kp <= pos && !(bm >> (e >> 4) & 1u);
+          x[e] = valid ? x[e] : -INFINITY;
+          mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
         }
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -499,12 +560,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const bool grow = mx > m + kRescaleThreshold;
       // sigma is the same on every row (sV depends on the token and KV head)
       const bool rescale = __any_sync(kFull, grow) || sig_new != sigma;
-      bool wok = true;
-      if (j >= 2)  // PV(j - 2), the last reader of P buffer j % 2: every block
-        wok = wait_w(&pdone[j & 1], static_cast<uint32_t>(((j >> 1) - 1) & 1));
-      if (wok && rescale && j >= 1)  // PV(j - 1) too before O is touched
-        wok = wait_w(&pdone[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1));
-      if (!wok) {
+      // Rescaling O waits for its last writer, the tile's PV of block i - 1.
+      // (Parity waits on pdone are sound although this role skips phases:
+      // S of block i is in, so PV of i - 2 -- issued before it -- is done.)
+      if (rescale && i >= 1 &&
+          !wait_w(&pdone[2 * t + ((i - 1) & 1)], static_cast<uint32_t>(((i - 1) >> 1) & 1))) {
         ok = false;
         break;
       }
@@ -514,51 +574,51 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - nm);
         // O holds sum p sV / sigma V: a larger sigma scales it by sigma / sigma_new
         const float ao = (sigma > 0.f && sig_new != sigma) ? a * (sigma / sig_new) : a;
-        if (j >= 1) {
+        if (i >= 1) {  // 16 columns at a time (x is live here)
+#pragma unroll 1
+          for (int c = 0; c < DH; c += 16) {
+            uint32_t o[16];
+            tmem_ld16(tm_o + c, o);
 #pragma unroll
-          for (int c = 0; c < DH; c += 32) {
-            float o[32];
-            tmem_ld32(tm_o + lane_base + c, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= ao;
-            tmem_st32(tm_o + lane_base + c, o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * ao);
+            tmem_st16(tm_o + c, o);
           }
         }
         l *= a;
         m = nm;
         sigma = sig_new;
       }
-      // P row -> f16 into the A tile of PV
-      uint32_t ph[kKeys / 2];
+      // P row -> f16 into the S buffer's first 32 columns (the A operand of
+      // PV), 8 keys at a time
       float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of the block
       // sV_t / sigma of each value (a power-of-two quotient: exact)
       const float isig = sigma > 0.f ? 1.f / sigma : 0.f;
 #pragma unroll
-      for (int i = 0; i < kKeys; i += 2) {
-        // m = -inf only while every key so far is masked (this block's too)
-        const float p0 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i], lscale, -m));
-        const float p1 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[i + 1], lscale, -m));
-        l4[(i >> 1) & 3] += p0 + p1;
-        if (TS)
-          ph[i / 2] = f32x2_to_f16x2(p0 * (bsc[kKeys + i] * isig), p1 * (bsc[kKeys + i + 1] * isig));
-        else
-          ph[i / 2] = f32x2_to_f16x2(p0, p1);
+      for (int c = 0; c < kKeys / 8; ++c) {
+        uint32_t ph[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const int e = 8 * c + 2 * e2;
+          // m = -inf only while every key so far is masked (this block's too)
+          const float p0 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[e], lscale, -m));
+          const float p1 = (m == -INFINITY) ? 0.f : fast_exp2(fmaf(x[e + 1], lscale, -m));
+          l4[e2] += p0 + p1;
+          if (TS)
+            ph[e2] = f32x2_to_f16x2(p0 * (bsc[kKeys + e] * isig), p1 * (bsc[kKeys + e + 1] * isig));
+          else
+            ph[e2] = f32x2_to_f16x2(p0, p1);
+        }
+        tmem_st4(tm_s + (i & 1) * kKeys + 4 * c, ph[0], ph[1], ph[2], ph[3]);
       }
       l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-#pragma unroll
-      for (int c = 0; c < kKeys / 8; ++c)
-        sts128(sbase + Lo::p + (j & 1) * Lo::pBytes + sw128_off(r, 8 * c, kRows), ph[4 * c], ph[4 * c + 1], ph[4 * c + 2],
-               ph[4 * c + 3]);
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&pfull[j & 1]);
+      mbar_arrive(&pfull[2 * t + (i & 1)]);
     }
     if (!ok) fail();
-    // ---- epilogue: O row / l * sV -> bf16
-    // the last two PVs, in order on their barriers
-    bool eok = ok;
-    if (eok && nblk >= 2) eok = wait_w(&pdone[(nblk - 2) & 1], static_cast<uint32_t>(((nblk - 2) >> 1) & 1));
-    if (eok) eok = wait_w(&pdone[(nblk - 1) & 1], static_cast<uint32_t>(((nblk - 1) >> 1) & 1));
+    // ---- epilogue: O row / l * sV -> bf16, after the tile's last PV
+    bool eok = ok && nI > 0;
+    if (eok) eok = wait_w(&pdone[2 * t + ((nI - 1) & 1)], static_cast<uint32_t>(((nI - 1) >> 1) & 1));
     if (eok) {
       tc_fence_after();
       const float f = l > 0.f ? (TS ? sigma : sv) / l : 0.f;
@@ -566,7 +626,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
       for (int c = 0; c < DH; c += 32) {
         float o[32];
-        tmem_ld32(tm_o + lane_base + c, o);
+        tmem_ld32(tm_o + c, o);
         if (store) {
           uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * DH + c);
 #pragma unroll
@@ -577,7 +637,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                                 f32x2_to_bf16x2(o[8 * v + 6] * f, o[8 * v + 7] * f));
         }
       }
-    } else if (ok) {
+    } else if (ok && nI > 0) {
       fail();
     }
   }
@@ -591,7 +651,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (issued[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>((issued[s] / S) & 1));
   }
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");

@@ -60,6 +60,18 @@ KVQ_DEVI void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint
       : "memory");
 }
 
+// A from tensor memory (M rows in the 128 lanes, K along the columns, two
+// f16 per 32-bit column, the lower half the even k), B from shared memory.
+KVQ_DEVI void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 KVQ_DEVI void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                         uint32_t accumulate) {
   asm volatile(
@@ -105,6 +117,13 @@ KVQ_DEVI void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
+}
+
+// Store 4 consecutive columns of this thread's lane (no wait: several stores
+// may be in flight; tmem_st_wait() completes them).
+KVQ_DEVI void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
+               ::"r"(taddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 KVQ_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
