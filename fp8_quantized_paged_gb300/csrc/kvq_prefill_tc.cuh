@@ -144,8 +144,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.z, gkv = blockIdx.y;
-  const int pairs = (p.tiles + kTiles - 1) / kTiles;
-  const int pair = pairs - 1 - static_cast<int>(blockIdx.x);  // longest pairs first
+  // p.tpc tiles a CTA (1 or kTiles; with 1, tile 1's warps have no rows)
+  const int groups = (p.tiles + p.tpc - 1) / p.tpc;
+  const int pair = groups - 1 - static_cast<int>(blockIdx.x);  // longest first
   const int TQ = kRows / p.G;
 
   if (tid == 0) {
@@ -180,12 +181,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   const int q0 = __ldg(p.cu_q + b);
   const int n = __ldg(p.cu_q + b + 1) - q0;
-  const int j0 = pair * kTiles * TQ;  // first query token of tile 0
+  const int j0 = pair * p.tpc * TQ;  // first query token of tile 0
   // a chunk longer than the grid covers (max_q_len): its later rows stay unwritten
   if (blockIdx.x == 0 && gkv == 0 && tid == 0 && n > p.tiles * TQ)
     flag_status(p.status, KVQ_DEV_BAD_QLEN);
   if (n <= 0 || j0 >= n) return;  // the whole CTA, before any tensor memory is taken
-  const int j1 = min(n, j0 + kTiles * TQ);  // past the pair's last query token
+  const int j1 = min(n, j0 + p.tpc * TQ);  // past the CTA's last query token
   const int L = __ldg(p.seq_lens + b);
   if (!(L >= n && L <= p.max_blocks * kBS)) {
     if (pair == 0 && gkv == 0 && tid == 0) flag_status(p.status, KVQ_DEV_BAD_SEQLEN);
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) {
     const int a = j0 + t * TQ, e = min(n, a + TQ);
-    if (a >= n) {
+    if (t >= p.tpc || a >= n) {
       jb[t] = je[t] = 0;
     } else {
       jb[t] = (window_lo(p.window, base + a + 1) / kBS - p_begin) / 4;
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int t = warp >> 2;   // this warp group's tile
     const int r = tid & 127;   // row = TMEM lane
     const int jr = j0 + t * TQ + r / p.G;
-    const bool live = jr < n;
+    const bool live = t < p.tpc && jr < n;
     const int pos = live ? base + jr : -1;
     const int lo = live ? window_lo(p.window, pos + 1) : 0;
     const int64_t qrow = live ? static_cast<int64_t>(q0 + jr) * p.Hq + gkv * p.G + r % p.G : -1;
