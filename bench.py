@@ -842,8 +842,8 @@ def run_ncu_case(case: str):
     'decode_long' and 'write_long' one layer of the long-context workload
     (32768 tokens: 128 MiB of bf16 K/V in, 64 MiB of FP8 cache); on that
     layer 'write_th_long' / 'decode_th_long' use per-(token, head) scales,
-    'calib_long' calibrates per-head scales and 'prefill_long' runs a
-    prefix-hit prefill of the last 512 tokens."""
+    'calib_long' calibrates per-head scales and 'prefill_long' runs the
+    bench's prefix-hit prefill (the last 2048 tokens as queries)."""
     import torch
 
     import fp8_quantized_paged_gb300 as kvq
@@ -885,7 +885,7 @@ def run_ncu_case(case: str):
         for _ in range(3):
             kvq.kvq_calibrate_scales(k, v, cal_k, cal_v, kvq.KVQ_SCALE_PER_HEAD, lay.fmt)
     if case == "prefill_long":
-        nq = 512
+        nq = 2048
         pq = torch.randn((nq, lay.Hq, lay.dh), device=dev).to(torch.bfloat16)
         pout = torch.empty_like(pq)
         cu = torch.tensor([0, nq], dtype=torch.int32, device=dev)

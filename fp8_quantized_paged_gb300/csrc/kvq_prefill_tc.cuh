@@ -1,30 +1,30 @@
 // kvq_prefill_tc.cuh -- the prefill kernel of the FP8 caches on the 5th-
 // generation tensor cores (tcgen05, accumulators in tensor memory).
 //
-// One CTA per (sequence, KV head, pair of adjacent tiles of 128 query rows);
-// a row is a (query token, query head of the group) pair, so a tile holds
-// 128 / G tokens.  The keys stream in blocks of 64 tokens (4 pages), each
-// converted once for both tiles:
+// One CTA per (sequence, KV head, one or two adjacent tiles of 128 query
+// rows); a row is a (query token, query head of the group) pair, so a tile
+// holds 128 / G tokens.  The keys stream in blocks of 64 tokens (4 pages),
+// each converted once for both tiles:
 //   warp 12 (producer): block ids 32 pages at a time (one per lane), TMA loads
 //     of each block's 4 K and 4 V FP8 pages into a 3-stage ring (the
 //     decode's 128-byte-swizzled page boxes).
 //   warps 8-11 (converters): each block's pages to f16 in shared memory, K as
 //     the B operand of QK^T and V as the MN-major B operand of PV, both
-//     token-major in the same layout, in 2 or 3 buffers.
+//     token-major in the same layout, in 3 buffers.
 //   warps 13 and 14 (MMA of tiles 0 and 1; warp 13 allocates the 512 TMEM
-//     columns: per tile two 64-column S buffers and the dh-column O
-//     accumulator): one elected lane each issues, per block of its tile,
-//     S = Q K^T (M = 128, N = 64, K = dh in steps of 16) and, once the
-//     tile's probabilities are in, O += P V (A = P from tensor memory,
-//     N = dh, K = 64 tokens), each completion signalled to an mbarrier by
-//     tcgen05.commit.  A tile skips the blocks none of its rows sees.
+//     columns: per tile a 64-column S, two 32-column P buffers and the
+//     dh-column O accumulator): one elected lane each issues, per block of
+//     its tile, S = Q K^T (M = 128, N = 64, K = dh in steps of 16) once the
+//     softmax has read the previous S, and O += P V (A = P from tensor
+//     memory, N = dh, K = 64 tokens) once the block's P is in, each
+//     completion signalled to an mbarrier by tcgen05.commit.  A tile skips
+//     the blocks none of its rows sees.
 //   warps 0-3 and 4-7 (softmax of tiles 0 and 1; thread r of a tile = row r
-//     = TMEM lane r): Q row r to f16, then per block the S row from TMEM,
-//     causal / window mask (skipped for blocks the whole row sees), online
-//     max with a lazy rescale of the O row in TMEM, P = 2^(x-m) as f16 back
-//     into the first 32 columns of the S buffer it came from (the A operand
-//     of PV), which the next QK^T into that buffer, issued after the PV,
-//     overwrites only once the PV has read it.
+//     = TMEM lane r): Q row r to f16, then per block the S row from TMEM
+//     (released at once), causal / window mask (skipped for blocks the whole
+//     row sees), online max with a lazy rescale of the O row in TMEM, and
+//     P = 2^(x-m) as f16 into P buffer i % 2 once the PV of block i - 2 has
+//     read it.
 // Every shared-memory operand is in the K-major 128-byte-swizzle layout:
 // 8-row groups of 1024 bytes, 128-byte rows of 64 f16, 16-byte chunk c of
 // row r at chunk c ^ (r % 8); wider K in further 64-column blocks of the
@@ -45,7 +45,7 @@ constexpr int kKeys = 64;       // tokens per key block (QK^T N, PV K)
 constexpr int kThreadsTc = 480;
 constexpr int kConvWarp = 8, kProdWarp = 12, kMmaWarp = 13;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTileCols = 256;  // per tile: S buffers at +0, +64; O at +128
+constexpr uint32_t kTileCols = 256;  // per tile: S at +0, P buffers at +64, +96, O at +128
 
 // Shared memory: the two Q tiles, kB f16 K / V buffers (the converters run
 // kB - 1 blocks ahead of the PVs) and kS FP8 page stages.
@@ -67,7 +67,7 @@ struct Layout {
   static constexpr size_t ssc = stage + static_cast<size_t>(kS) * kStage;
   static constexpr size_t bsc = ssc + (TS ? static_cast<size_t>(kS) * 4 * 32 * 4 : 0);
   static constexpr size_t bars = bsc + (TS ? static_cast<size_t>(kB) * 128 * 4 : 0);
-  // barriers: full[S], empty[S], conv[kB], kvdone[kB], sfull[kTiles][2],
+  // barriers: full[S], empty[S], conv[kB], kvdone[kB], sfull[kTiles], sfree[kTiles],
   // pfull[kTiles][2], pdone[kTiles][2], fin, qready
   static constexpr int kBars = 2 * kS + 2 * kB + 6 * kTiles + 2;
   static constexpr size_t misc = bars + kBars * sizeof(uint64_t);
@@ -118,17 +118,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint64_t* empty = bars + S;          // [S] FP8 stage converted (128 arrivals)
   uint64_t* conv = bars + 2 * S;            // [kBufs] f16 K / V buffer b ready (128 arrivals)
   uint64_t* kvdone = conv + kBufs;          // [kBufs] buffer b's block released by both issuers
-  uint64_t* sfull = kvdone + kBufs;         // [kTiles][2] S buffer of a tile written (commit)
-  uint64_t* pfull = sfull + 2 * kTiles;     // [kTiles][2] P in a tile's S buffer (128 arrivals)
-  uint64_t* pdone = pfull + 2 * kTiles;     // [kTiles][2] PV from a tile's S buffer done (commit)
+  uint64_t* sfull = kvdone + kBufs;         // [kTiles] a tile's S written (commit)
+  uint64_t* sfree = sfull + kTiles;         // [kTiles] a tile's S read (128 arrivals)
+  uint64_t* pfull = sfree + kTiles;         // [kTiles][2] P buffer of a tile written (128 arrivals)
+  uint64_t* pdone = pfull + 2 * kTiles;     // [kTiles][2] PV from a tile's P buffer done (commit)
   uint64_t* fin = pdone + 2 * kTiles;       // every MMA done (a commit of each issuer)
   uint64_t* qready = fin + 1;               // both Q tiles written (256 arrivals)
   // A parity wait for phase p of a barrier is sound only while the barrier
   // has completed p or p + 1 phases.  Every waiter therefore waits each of
   // its barriers' phases in order, never skipping one (so p - 1 is known
   // complete), and a barrier's phase after p needs the waiter's own later
-  // progress; barriers used once per block come in pairs (even and odd
-  // blocks), so that no waiter can fall two phases behind.  A tile's
+  // progress; P buffers and their barriers come in pairs (even and odd
+  // blocks), so that no waiter can fall two phases behind, and a tile's
+  // single S buffer is rewritten only after its softmax has read it.  A tile's
   // softmax, which may start after block 0, waits for a
   // block's conversion only once the block's S is in (the MMA lane issued
   // QK^T after that conversion): the phase is then complete, and the next
@@ -160,8 +162,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(&kvdone[i], kTiles);
     }
     for (int t = 0; t < kTiles; ++t) {
-      mbar_init(&sfull[2 * t], 1);
-      mbar_init(&sfull[2 * t + 1], 1);
+      mbar_init(&sfull[t], 1);
+      mbar_init(&sfree[t], 128);
       mbar_init(&pfull[2 * t], 128);
       mbar_init(&pfull[2 * t + 1], 128);
       mbar_init(&pdone[2 * t], 1);
@@ -294,14 +296,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp >= kMmaWarp) {
     // ------------------------------------------------------------ MMA issuers
     // One elected lane per tile (warp kMmaWarp + t), in the tile's order
-    // QK(0), QK(1), PV(0), QK(2), PV(1), ...: P lives in its S buffer, and a
-    // later MMA may overwrite an earlier one's operand before that one has
-    // read it, so QK^T of tile block i waits for the PV of block i - 2.  A
-    // block's K / V buffer goes back to the converters once both issuers
-    // have released it (kvdone counts one commit of each, in block order).
+    // QK(0), QK(1), PV(0), QK(2), PV(1), ...: QK^T of tile block i once the
+    // softmax has read the tile's S of block i - 1 (one S buffer), PV of
+    // block i - 1 once its P is in (two P buffers, which the softmax reuses
+    // only after the PV two blocks back).  A block's K / V buffer goes back
+    // to the converters once both issuers have released it (kvdone counts
+    // one commit of each, in block order).
     const int t = warp - kMmaWarp;
     if (lane == 0) {
       const uint32_t id_qk = idesc_f16(kRows, kKeys), id_pv = idesc_f16(kRows, DH);
+      const uint32_t tm_t = tmem + t * kTileCols;  // S at +0, P buffers at +64 and +96, O at +128
       const int nI = je[t] - jb[t];
       bool ok = wait_or_abort(qready, 0u, abort_flag);
       int pv = 0;  // PVs issued (tile blocks)
@@ -311,24 +315,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           return false;
         tc_fence_after();
         const uint32_t b_v = sbase + Lo::vt + (jp % kBufs) * Lo::vtBytes;
-        const uint32_t a_pt = tmem + t * kTileCols + (i & 1) * kKeys;  // P: 8 columns per 16 tokens
+        const uint32_t a_pt = tm_t + kKeys + (i & 1) * (kKeys / 2);  // P: 8 columns per 16 tokens
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           // 16 tokens = two 8-row groups of V; B is MN-major (bit 16)
-          mma_f16_ts(tmem + t * kTileCols + 128, a_pt + kk * 8, sw128_desc_mn(b_v + kk * 2048),
+          mma_f16_ts(tm_t + 128, a_pt + kk * 8, sw128_desc_mn(b_v + kk * 2048),
                      id_pv | (1u << 16), (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&pdone[2 * t + (i & 1)]);  // the S buffer's P read, O updated
+        mma_commit(&pdone[2 * t + (i & 1)]);  // the P buffer read, O updated
         mma_commit(&kvdone[jp % kBufs]);      // this tile is done with the K / V buffer
         ++pv;
         return true;
       };
       for (int j = 0; j < nblk && ok; ++j) {
         const int i = j - jb[t];
-        if (i >= 2 && i < nI) {  // PVs up to block i - 2 first: they need no conversion
-          while (ok && pv <= i - 2) ok = issue_pv();
-          if (!ok) break;
-        }
         if (j >= je[t]) {  // past the tile's blocks: its last PVs, in order, then release
           while (ok && pv < nI) ok = issue_pv();
           if (!ok) break;
@@ -341,21 +341,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mma_commit(&kvdone[j % kBufs]);  // a block the tile does not see: released at once
           continue;
         }
-        if (i >= 2) {  // the S buffer's last P has been read (PV of block i - 2)
-          ok = wait_or_abort(&pdone[2 * t + (i & 1)], static_cast<uint32_t>(((i - 2) >> 1) & 1), abort_flag);
+        if (i >= 1) {  // the softmax has read S of block i - 1
+          ok = wait_or_abort(&sfree[t], static_cast<uint32_t>((i - 1) & 1), abort_flag);
           if (!ok) break;
         }
         tc_fence_after();
         const uint32_t b_k = sbase + Lo::k + (j % kBufs) * Lo::kBytes;
         const uint32_t a_q = sbase + Lo::q + t * Lo::qBytes;
-        const uint32_t d_s = tmem + t * kTileCols + (i & 1) * kKeys;
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
           const uint32_t off_a = (ks >> 2) * (kRows * 128) + (ks & 3) * 32;
           const uint32_t off_b = (ks >> 2) * (kKeys * 128) + (ks & 3) * 32;
-          mma_f16_ss(d_s, sw128_desc(a_q + off_a), sw128_desc(b_k + off_b), id_qk, ks > 0 ? 1u : 0u);
+          mma_f16_ss(tm_t, sw128_desc(a_q + off_a), sw128_desc(b_k + off_b), id_qk, ks > 0 ? 1u : 0u);
         }
-        mma_commit(&sfull[2 * t + (i & 1)]);
+        mma_commit(&sfull[t]);
+        if (i >= 1) ok = issue_pv();  // PV of block i - 1
       }
       while (ok && pv < nI) ok = issue_pv();
       if (!ok) fail();
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int lo = live ? window_lo(p.window, pos + 1) : 0;
     const int64_t qrow = live ? static_cast<int64_t>(q0 + jr) * p.Hq + gkv * p.G + r % p.G : -1;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tm_s = tmem + lane_base + t * kTileCols;  // S buffers of this tile
+    const uint32_t tm_s = tmem + lane_base + t * kTileCols;  // S of this tile (P buffers at +64, +96)
     const uint32_t tm_o = tm_s + 128;                          // O of this tile
 
     // FP8-domain query: the row's head scale sQ; the row's codes enc(q / sQ)
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int nI = je[t] - jb[t];  // this tile's blocks
     for (int i = 0; i < nI && ok; ++i) {
       const int j = jb[t] + i;
-      if (!wait_w(&sfull[2 * t + (i & 1)], static_cast<uint32_t>((i >> 1) & 1))) {
+      if (!wait_w(&sfull[t], static_cast<uint32_t>(i & 1))) {
         ok = false;
         break;
       }
@@ -509,14 +509,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       float x[kKeys];
       {
         float t0[32], t1[32];
-        tmem_ld32(tm_s + (i & 1) * kKeys, t0);
-        tmem_ld32(tm_s + (i & 1) * kKeys + 32, t1);
+        tmem_ld32(tm_s, t0);
+        tmem_ld32(tm_s + 32, t1);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           x[e] = t0[e];
           x[32 + e] = t1[e];
         }
       }
+      tc_fence_before();
+      mbar_arrive(&sfree[t]);  // S read: the next QK^T may overwrite it
       const int kb0 = (p_begin + 4 * j) * kBS;
       const float* bsc = reinterpret_cast<const float*>(smem + Lo::bsc) + (j % kBufs) * 128;
       float sig_new = sigma;
@@ -562,8 +564,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // sigma is the same on every row (sV depends on the token and KV head)
       const bool rescale = __any_sync(kFull, grow) || sig_new != sigma;
       // Rescaling O waits for its last writer, the tile's PV of block i - 1.
-      // (Parity waits on pdone are sound although this role skips phases:
-      // S of block i is in, so PV of i - 2 -- issued before it -- is done.)
+      // (This role waits for every PV, two blocks back, before it rewrites
+      // that PV's P buffer below; this extra wait comes after the one for
+      // block i - 3 on the same barrier, so its parity wait is sound.)
       if (rescale && i >= 1 &&
           !wait_w(&pdone[2 * t + ((i - 1) & 1)], static_cast<uint32_t>(((i - 1) >> 1) & 1))) {
         ok = false;
@@ -589,8 +592,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         m = nm;
         sigma = sig_new;
       }
-      // P row -> f16 into the S buffer's first 32 columns (the A operand of
-      // PV), 8 keys at a time
+      // P row -> f16 into P buffer i % 2 (the A operand of PV), 8 keys at a
+      // time, once the PV of block i - 2 has read that buffer
+      if (i >= 2 && !wait_w(&pdone[2 * t + (i & 1)], static_cast<uint32_t>(((i - 2) >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tm_p = tm_s + kKeys + (i & 1) * (kKeys / 2);
       float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of the block
       // sV_t / sigma of each value (a power-of-two quotient: exact)
       const float isig = sigma > 0.f ? 1.f / sigma : 0.f;
@@ -609,7 +618,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           else
             ph[e2] = f32x2_to_f16x2(p0, p1);
         }
-        tmem_st4(tm_s + (i & 1) * kKeys + 4 * c, ph[0], ph[1], ph[2], ph[3]);
+        tmem_st4(tm_p + 4 * c, ph[0], ph[1], ph[2], ph[3]);
       }
       l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
       tmem_st_wait();
