@@ -478,9 +478,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const float sk = TS ? 1.f : __ldg(p.ks + (p.per_head ? gkv : 0));
     const float sv = TS ? 1.f : __ldg(p.vs + (p.per_head ? gkv : 0));
     const float lscale = sk * sq * p.logit_scale;
-    // Per-(token, head) V scales: P's columns carry sV_t / sigma, sigma a
-    // power of two at least the largest sV_t so far (so P stays <= 2^8 in
-    // f16); when a block raises it, O is rescaled with the running maximum.
+    // Per-(token, head) V scales: P's columns carry 2^7 sV_t / sigma, sigma a
+    // power of two at least the largest sV_t so far, so P stays <= 2^15 in
+    // f16 while the keys with small sV_t / sigma keep their precision (out of
+    // f16's subnormal range down to 2^-21); the epilogue takes the 2^7 off.
+    // When a block raises sigma, O is rescaled with the running maximum.
     float sigma = 0.f;
 
     // Waits of this role are warp-uniform (the TMEM accesses after them are
@@ -601,8 +603,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc_fence_after();
       const uint32_t tm_p = tm_s + kKeys + (i & 1) * (kKeys / 2);
       float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of the block
-      // sV_t / sigma of each value (a power-of-two quotient: exact)
-      const float isig = sigma > 0.f ? 1.f / sigma : 0.f;
+      // 2^7 sV_t / sigma of each value (power-of-two factors: exact)
+      const float isig = sigma > 0.f ? 128.f / sigma : 0.f;
 #pragma unroll
       for (int c = 0; c < kKeys / 8; ++c) {
         uint32_t ph[4];
@@ -631,7 +633,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (eok) eok = wait_w(&pdone[2 * t + ((nI - 1) & 1)], static_cast<uint32_t>(((nI - 1) >> 1) & 1));
     if (eok) {
       tc_fence_after();
-      const float f = l > 0.f ? (TS ? sigma : sv) / l : 0.f;
+      const float f = l > 0.f ? (TS ? sigma * 0.0078125f : sv) / l : 0.f;
       const bool store = live && guard(qrow < p.total_q * p.Hq, p.status, 24);
 #pragma unroll
       for (int c = 0; c < DH; c += 32) {

@@ -33,10 +33,11 @@ def bf16_out_to_f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def check_attention(got, ref, what=""):
+def check_attention(got, ref, what="", extra=0.0):
+    """extra: a further absolute term of the bound, per element (broadcast)."""
     got = np.asarray(got, np.float64)
     err = np.abs(got - ref)
-    bound = ABS_TOL + REL_TOL * np.abs(ref)
+    bound = ABS_TOL + REL_TOL * np.abs(ref) + extra
     bad = ~(err <= bound)
     assert not bad.any(), (
         f"{what}: {int(bad.sum())} of {err.size} elements out of tolerance; "
@@ -149,3 +150,24 @@ def oracle_decode(lay, K, V, pairs=None, window=None, seq_lens=None, block_table
                               lay.fmt,
                               lay.window if window is None else window, pairs=pairs,
                               q_scale=lay.q_scale if q_fp8 else None)
+
+
+def prefill_p_bound(lay: workloads.Layer, cu_q) -> np.ndarray:
+    """The FP8 prefill's extra error term, per (query token, query head, dim).
+
+    Its probabilities reach the PV MMA as f16, each within 2^-12 (half an
+    f16 ulp) of its value, so an output element sum_t p_t V_t[d] / l can
+    be off by up to 2^-12 max_t |V_t[d]| beyond the accumulation's rounding.
+    max_t runs over the sequence's tokens of the query head's KV head, from
+    the bf16 inputs, times 1.125 for the FP8 rounding of V (half an E5M2
+    ulp, relative)."""
+    st = lay.st
+    B = len(st.seq_lens)
+    v = np.abs(workloads.bf16_bits_to_f32(lay.v)).astype(np.float64)  # [N, Hkv, dh]
+    vmax = np.zeros((B, lay.Hkv, lay.dh))
+    np.maximum.at(vmax, st.token_seq, v)
+    G = lay.Hq // lay.Hkv
+    cu_q = np.asarray(cu_q)
+    seq_of_q = np.repeat(np.arange(B), np.diff(cu_q))
+    per_q = np.repeat(vmax[seq_of_q], G, axis=1)  # [total_q, Hq, dh]
+    return 1.125 * 2.0 ** -12 * per_q

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import workloads
-from kvq_testlib import (DeviceLayer, bf16_out_to_f64, check_attention, oracle_caches,
+from kvq_testlib import (prefill_p_bound, DeviceLayer, bf16_out_to_f64, check_attention, oracle_caches,
                          oracle_decode, to_dev, to_np)
 
 pytestmark = pytest.mark.gpu
@@ -880,6 +880,13 @@ def _prefill_ex(kvq, lay, nq, seed, token_head=False, q_fp8=False, window=None):
     return bf16_out_to_f64(out), ref, status
 
 
+def _check_prefill(got, ref, lay, nq, what):
+    """The attention tolerance plus the f16 probabilities' term (large |V|
+    rows, as with per-token magnitudes over two decades, reach it)."""
+    cu = np.concatenate([[0], np.cumsum(nq)])
+    check_attention(got, ref, what, extra=prefill_p_bound(lay, cu))
+
+
 def _per_token_magnitudes(lay, seed):
     """K and V rows scaled by factors log-uniform over 10^[-1, 1], so the
     per-(token, head) scales span two decades inside every key block (the
@@ -900,7 +907,32 @@ def test_prefill_token_head_scales(kvq, fmt, G, dh):
     _per_token_magnitudes(lay, 231)
     got, ref, st = _prefill_ex(kvq, lay, [70, 5, 37, 1, 0], seed=232, token_head=True)
     assert st == 0
-    check_attention(got, ref, f"token-head prefill G={G} dh={dh}")
+    _check_prefill(got, ref, lay, [70, 5, 37, 1, 0], f"token-head prefill G={G} dh={dh}")
+
+
+@pytest.mark.parametrize("mode", ["per_head", "token_head", "window", "q_fp8", "e5m2_dh64"])
+def test_prefill_tile_pairs(kvq, mode):
+    """Enough query tiles that the FP8 prefill runs two tiles a CTA (16
+    sequences x 2 tiles of 128 rows x 8 KV heads: 256 single-tile CTAs are
+    two waves on a GB300, 128 pairs one), with chunks that fill both tiles,
+    part of the second, or only the first."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    waves = lambda ctas: -(-ctas // sms)  # noqa: E731
+    assert 8 * waves(1 * 8 * 16) < 7 * waves(2 * 8 * 16), "the launch would not pair tiles"
+    r = np.random.default_rng(270)
+    nq = [256, 200, 129, 128, 64, 1, 256, 256, 130, 255, 17, 256, 192, 256, 100, 256]
+    lens = [q + int(r.integers(0, 300)) for q in nq]
+    fmt = workloads.E5M2 if mode == "e5m2_dh64" else workloads.E4M3
+    dh = 64 if mode == "e5m2_dh64" else 128
+    lay = _custom_layer(lens, Hq=8, Hkv=8, dh=dh, fmt=fmt, seed=271)
+    if mode == "q_fp8":
+        lay.q_scale[:] = np.linspace(0.005, 0.02, lay.q_scale.size).astype(np.float32)
+    if mode == "token_head":
+        _per_token_magnitudes(lay, 272)
+    got, ref, st = _prefill_ex(kvq, lay, nq, seed=273, token_head=mode == "token_head",
+                               q_fp8=mode == "q_fp8", window=100 if mode == "window" else None)
+    assert st == 0
+    _check_prefill(got, ref, lay, nq, f"prefill in tile pairs ({mode})")
 
 
 @pytest.mark.parametrize("token_head", [False, True])
@@ -910,7 +942,7 @@ def test_prefill_q_fp8(kvq, token_head, gran):
     lay.q_scale[:] = np.linspace(0.005, 0.02, lay.q_scale.size).astype(np.float32)
     got, ref, st = _prefill_ex(kvq, lay, [64, 70, 1], seed=241, token_head=token_head, q_fp8=True)
     assert st == 0
-    check_attention(got, ref, f"q fp8 prefill token_head={token_head}")
+    _check_prefill(got, ref, lay, [64, 70, 1], f"q fp8 prefill token_head={token_head}")
 
 
 @pytest.mark.parametrize("window", [1, 100])
@@ -919,7 +951,7 @@ def test_prefill_token_head_window_and_bad_block(kvq, window):
     _per_token_magnitudes(lay, 251)
     got, ref, st = _prefill_ex(kvq, lay, [150, 40], seed=252, token_head=True, window=window)
     assert st == 0
-    check_attention(got, ref, f"token-head prefill window={window}")
+    _check_prefill(got, ref, lay, [150, 40], f"token-head prefill window={window}")
     # an out-of-range block id in the prefix: its 16 tokens are masked out;
     # the reference re-packs the other tokens (the queries keep their order)
     bt = lay.st.block_tables.copy()
