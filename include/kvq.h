@@ -381,8 +381,13 @@ KVQ_API int kvq_decode_static_reset(kvq_stream_t stream);
  *                   * block_size: the sequence's rows are zero),
  *                   KVQ_DEV_BAD_QLEN (n_b > max_q_len), KVQ_DEV_WAIT_TIMEOUT.
  * Group size num_q_heads / num_kv_heads in {1, 2, 4, 8}; num_seqs <= 65535.
- * No workspace: one CTA per (sequence, KV head, 64 query rows), so a short
- * chunk over a long prefix keeps few SMs busy.
+ * No workspace.  The FP8 caches run one CTA per (sequence, KV head, one or
+ * two tiles of 128 query rows -- two when that needs fewer waves of CTAs),
+ * the bf16 cache one per 64 query rows; a short chunk over a long prefix
+ * keeps few SMs busy.  Precision: each probability reaches the PV MMA as one
+ * f16 (the decode uses two f16 parts), so an output element may differ from
+ * exact arithmetic over the dequantized cache by up to 2^-12 times the
+ * largest |V| the row attends to, beyond its bf16 rounding.
  */
 KVQ_API int kvq_prefill_attn(const void* q, const int32_t* cu_q_lens, int64_t num_q_tokens,
                              int max_q_len, const void* k_cache, const void* v_cache,
